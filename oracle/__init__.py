@@ -1,0 +1,213 @@
+"""FP64 CPU oracle for exact attention forward -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The
+product path (``exact_attention_forward_fa_gb300``) never imports, links or
+executes anything here, and this package imports nothing from it.
+
+The arithmetic lives in ``fa_oracle.c`` (plain C11, FP64, built here with
+gcc).  This module only marshals numpy arrays into it.  What each function
+computes, and the passage it follows, is stated in ``fa_oracle.c``:
+
+* ``attention`` / ``attention_rows`` / ``attention_probs``: the plain
+  definition (materialised S and P rows), "FlashAttention-3 on Hopper"
+  sec. 3.1, 3.2, 4.6, 4.7.
+* ``attention_online``: the tiled online recurrence with the conditional
+  rescale rule, "FlashAttention-3 on Hopper" sec. 4.2 and "FlashAttention
+  v1-v4" (conditional rescale).
+* ``hadamard_rotate``, ``e4m3_encode`` / ``e4m3_decode``,
+  ``quantize_e4m3_tiles``: the FP8 pre-pass pieces, "FlashAttention-3 on
+  Hopper" sec. 6.1, 6.3, 6.4.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fa_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int)
+
+
+def build(force: bool = False) -> str:
+    """Compile fa_oracle.c into liboracle.so (gcc, no FMA contraction)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared",
+           "-Wall", "-o", tmp, _SRC, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB_PATH)
+    lib.oracle_attention_head.argtypes = [
+        _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_double,
+        ctypes.c_int, _ip, ctypes.c_int, _dp, ctypes.c_long, _dp, _dp]
+    lib.oracle_attention_head.restype = ctypes.c_int
+    lib.oracle_attention_fwd.argtypes = [
+        _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int]
+    lib.oracle_attention_fwd.restype = ctypes.c_int
+    lib.oracle_attention_online_head.argtypes = [
+        _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_double,
+        ctypes.c_int, _ip, _ip, ctypes.c_int, ctypes.c_double, _dp,
+        ctypes.c_long, _dp, ctypes.POINTER(ctypes.c_long)]
+    lib.oracle_attention_online_head.restype = ctypes.c_int
+    lib.oracle_hadamard_rotate.argtypes = [
+        _dp, _dp, ctypes.c_long, ctypes.c_int, ctypes.c_long, _dp]
+    lib.oracle_hadamard_rotate.restype = ctypes.c_int
+    lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint]
+    lib.oracle_e4m3_decode.restype = ctypes.c_double
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint
+    lib.oracle_quantize_e4m3_tiles.argtypes = [
+        _dp, ctypes.POINTER(ctypes.c_ubyte), ctypes.POINTER(ctypes.c_float),
+        ctypes.c_long, ctypes.c_int, ctypes.c_long, ctypes.c_int]
+    lib.oracle_quantize_e4m3_tiles.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _f64(x) -> np.ndarray:
+    """Exact widening to a C-contiguous float64 array (bf16/fp16/fp32 -> f64)."""
+    if hasattr(x, "detach"):                      # a torch tensor
+        import torch
+        x = x.detach().to("cpu").to(torch.float64).numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_dp)
+
+
+def attention(q, k, v, alpha: float, causal: bool, n_threads: int = 1):
+    """O [B,N,H,d] and LSE [B,H,N] in float64 from Q/K/V [B,N,H,d]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, H, d = q.shape
+    o = np.zeros_like(q)
+    lse = np.zeros((B, H, N), dtype=np.float64)
+    rc = _load().oracle_attention_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                      _ptr(lse), B, H, N, d, float(alpha),
+                                      int(bool(causal)), int(n_threads))
+    if rc:
+        raise RuntimeError(f"oracle_attention_fwd failed ({rc})")
+    return o, lse
+
+
+def attention_head(q, k, v, alpha: float, causal: bool, rows=None,
+                   want_probs: bool = False):
+    """One head: q [Nq,d], k/v [Nk,d].  Returns (O, LSE[, P]).
+
+    With ``rows`` only those query rows are computed (O has len(rows) rows).
+    Causal masking is bottom-right aligned: key j is hidden from query i
+    when j > i + (Nk - Nq).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Nq, d = q.shape
+    Nk = k.shape[0]
+    if rows is None:
+        n = Nq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        n = len(rows_arr)
+    o = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    probs = np.zeros((Nq, Nk), dtype=np.float64) if want_probs else None
+    rc = _load().oracle_attention_head(
+        _ptr(q), _ptr(k), _ptr(v), Nq, Nk, d, d, d, d, float(alpha),
+        int(bool(causal)),
+        rows_arr.ctypes.data_as(_ip) if rows_arr is not None else None,
+        n, _ptr(o), d, _ptr(lse), _ptr(probs) if want_probs else None)
+    if rc:
+        raise RuntimeError(f"oracle_attention_head failed ({rc})")
+    return (o, lse, probs) if want_probs else (o, lse)
+
+
+def attention_rows(q, k, v, alpha: float, causal: bool, b: int, h: int, rows):
+    """Rows ``rows`` of head (b, h) of [B,N,H,d] tensors (torch or numpy)."""
+    def head(x):
+        x = x[b, :, h, :]
+        return _f64(x)
+    return attention_head(head(q), head(k), head(v), alpha, causal, rows=rows)
+
+
+def attention_online(q, k, v, alpha: float, causal: bool, tiles, tau: float):
+    """Tiled online recurrence over key tiles ``tiles`` = [(lo, hi), ...]
+    in processing order.  Returns (O, LSE, number of reference moves)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Nq, d = q.shape
+    Nk = k.shape[0]
+    lo = np.ascontiguousarray(np.array([t[0] for t in tiles], dtype=np.int32))
+    hi = np.ascontiguousarray(np.array([t[1] for t in tiles], dtype=np.int32))
+    o = np.zeros((Nq, d), dtype=np.float64)
+    lse = np.zeros((Nq,), dtype=np.float64)
+    nres = ctypes.c_long(0)
+    rc = _load().oracle_attention_online_head(
+        _ptr(q), _ptr(k), _ptr(v), Nq, Nk, d, d, d, d, float(alpha),
+        int(bool(causal)), lo.ctypes.data_as(_ip), hi.ctypes.data_as(_ip),
+        len(tiles), float(tau), _ptr(o), d, _ptr(lse), ctypes.byref(nres))
+    if rc:
+        raise RuntimeError(f"oracle_attention_online_head failed ({rc})")
+    return o, lse, int(nres.value)
+
+
+def hadamard_rotate(x, signs):
+    """x [..., d] -> x (1/sqrt d) H diag(signs), H Sylvester-ordered."""
+    x = _f64(x)
+    d = x.shape[-1]
+    flat = np.ascontiguousarray(x.reshape(-1, d))
+    y = np.zeros_like(flat)
+    s = _f64(signs).reshape(d)
+    rc = _load().oracle_hadamard_rotate(_ptr(flat), _ptr(y), flat.shape[0], d,
+                                        d, _ptr(s))
+    if rc:
+        raise RuntimeError("oracle_hadamard_rotate failed")
+    return y.reshape(x.shape)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.vectorize(lambda t: lib.oracle_e4m3_decode(int(t)),
+                        otypes=[np.float64])(c)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    lib = _load()
+    a = np.asarray(x, dtype=np.float64)
+    return np.vectorize(lambda t: lib.oracle_e4m3_encode(float(t)),
+                        otypes=[np.uint8])(a)
+
+
+def quantize_e4m3_tiles(x, tile_rows: int = 128):
+    """x [n_rows, d] (one head) -> (codes uint8 [n_rows, d], scales f32)."""
+    x = _f64(x)
+    n, d = x.shape
+    codes = np.zeros((n, d), dtype=np.uint8)
+    n_tiles = (n + tile_rows - 1) // tile_rows
+    scales = np.zeros((n_tiles,), dtype=np.float32)
+    rc = _load().oracle_quantize_e4m3_tiles(
+        _ptr(x), codes.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte)),
+        scales.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), n, d, d,
+        tile_rows)
+    if rc:
+        raise RuntimeError("oracle_quantize_e4m3_tiles failed")
+    return codes, scales
