@@ -1,0 +1,140 @@
+"""Python binding of libfa (exact attention forward on GB300, sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libfa.so``.  The names mirror the C ABI in ``include/fa.h``.
+If the library has not been built, every entry point raises -- there is no
+fallback implementation.
+
+Tensors are [B, N, H, d] (batch, sequence, head, head dim) and contiguous;
+LSE is float32 [B, H, N].
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_TOO_LARGE = 4
+FA_ERR_CUDA = 5
+FA_ERR_TIMEOUT = 6
+
+FA_BF16 = 0
+FA_FP16 = 1
+
+# Every symbol include/fa.h declares (checked by the tests).
+EXPORTS = ("fa_fwd", "fa_check_status", "fa_status_detail", "fa_status_string",
+           "fa_version")
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+def load():
+    """Load libfa.so (raises if it was not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+            "(the CUDA path has no fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_check_status.argtypes = [vp]
+    lib.fa_check_status.restype = i
+    lib.fa_status_detail.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.fa_status_detail.restype = None
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = i
+    _lib = lib
+    return lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def status_string(code: int) -> str:
+    return load().fa_status_string(int(code)).decode()
+
+
+def fa_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, alpha: float,
+           causal: int, dtype: int, stream=None) -> int:
+    """Direct call of the C entry point; returns the fa_status code.
+
+    Pointer arguments may be torch tensors or integer device addresses;
+    ``lse`` may be None.  ``stream`` is a torch stream, a raw cudaStream_t
+    integer, or None for torch's current stream."""
+    return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                         int(B), int(H), int(N), int(d), float(alpha),
+                         int(causal), int(dtype), _stream(stream))
+
+
+def fa_check_status(stream=None) -> int:
+    return load().fa_check_status(_stream(stream))
+
+
+def fa_status_detail() -> list[int]:
+    out = (ctypes.c_uint32 * 4)()
+    load().fa_status_detail(out)
+    return list(out)
+
+
+def fa_version() -> int:
+    return load().fa_version()
+
+
+def attention(q, k, v, causal: bool = False, alpha: float | None = None,
+              out=None, lse=None, want_lse: bool = True, stream=None):
+    """Convenience wrapper over ``fa_fwd`` for torch tensors on the GPU.
+
+    Allocates O (and LSE) with torch when not given, launches, and raises
+    FaError on a non-OK status.  Returns (O, LSE or None)."""
+    import torch
+    if q.dtype == torch.bfloat16:
+        dt = FA_BF16
+    elif q.dtype == torch.float16:
+        dt = FA_FP16
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    B, N, H, d = q.shape
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = fa_fwd(q, k, v, out, lse, B, H, N, d, alpha, int(bool(causal)), dt,
+                stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+    return out, lse

@@ -1,0 +1,186 @@
+// fa_api.cu -- the C ABI declared in include/fa.h: argument validation,
+// per-device properties, TMA tensor-map encoding, kernel selection, launch,
+// and the device status word read by fa_check_status.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_launch.cuh"
+
+namespace {
+
+constexpr int kVersion = 100;   // 0.1.0
+
+// Set by kernels whose bounded waits give up: [0] code, [1] role,
+// [2] wait site, [3] block index.  One instance per device context.
+__device__ uint32_t g_fa_status[4];
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t *status = nullptr;   // device address of g_fa_status
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+uint32_t g_last_detail[4] = {0, 0, 0, 0};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+fa_status get_device(DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        void *sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_fa_status) != cudaSuccess) return FA_ERR_CUDA;
+        d.status = static_cast<uint32_t *>(sym);
+        if (g_encode == nullptr) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return FA_ERR_CUDA;
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+        d.ready = true;
+    }
+    if (!(d.cc_major == 10 && d.cc_minor == 3)) return FA_ERR_UNSUPPORTED;
+    *out = &d;
+    return FA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 4-D map over a [B][N][H][d] tensor of 2-byte elements: dims {d, H, N, B},
+// box {64, 1, 128, 1} (a 128-row x 128-byte tile), 128-byte swizzle, rows
+// beyond N read as zero.
+fa_status encode_bshd(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int B,
+                      int H, int N, int d) {
+    const cuuint64_t esz = 2;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {esz * d, esz * d * H, esz * d * H * static_cast<cuuint64_t>(N)};
+    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, dt, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return kVersion; }
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+        case FA_ERR_TOO_LARGE: return "FA_ERR_TOO_LARGE";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                 int H, int N, int d, float alpha, int causal, fa_dtype dtype,
+                 void *stream) {
+    // ---- host-side validation: nothing is launched on failure ----
+    if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_MISALIGNED;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_MISALIGNED;
+    // TMA: every global stride < 2^40 bytes; kernel indexing uses 64-bit
+    // offsets, the unit counter is a 32-bit int.
+    const uint64_t batch_stride = 2ull * d * H * static_cast<uint64_t>(N);
+    if (batch_stride >= (1ull << 40)) return FA_ERR_TOO_LARGE;
+    const uint64_t n_qt = (static_cast<uint64_t>(N) + 127) / 128;
+    const uint64_t units = static_cast<uint64_t>(B) * H * ((n_qt + 1) / 2);
+    if (units > 0x7fffffffull || static_cast<uint64_t>(B) * H * N > 0x7fffffffffffull)
+        return FA_ERR_TOO_LARGE;
+
+    DeviceInfo *dev = nullptr;
+    fa_status st = get_device(&dev);
+    if (st != FA_OK) return st;
+
+    fa::FwdLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const CUtensorMapDataType dt =
+        dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if ((st = encode_bshd(&L.q, q, dt, B, H, N, d)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.k, k, dt, B, H, N, d)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.v, v, dt, B, H, N, d)) != FA_OK) return st;
+    L.args.o = o;
+    L.args.lse = lse;
+    L.args.status = dev->status;
+    L.args.B = B;
+    L.args.H = H;
+    L.args.N = N;
+    L.args.n_kv = static_cast<int>(n_qt);
+    L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
+    L.args.n_units = static_cast<int>(units);
+    L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
+    L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.causal = causal != 0;
+    L.bf16 = dtype == FA_BF16;
+
+    cudaError_t e = (d == 64) ? fa::launch_fwd_d64(L) : fa::launch_fwd_d128(L);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_check_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+    DeviceInfo *dev = nullptr;
+    fa_status st = get_device(&dev);
+    if (st != FA_OK) return st;
+    uint32_t h[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(h, dev->status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (h[0] == 0) return FA_OK;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        std::memcpy(g_last_detail, h, sizeof(h));
+    }
+    const uint32_t zero[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(dev->status, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return FA_ERR_CUDA;
+    return FA_ERR_TIMEOUT;
+}
+
+void fa_status_detail(uint32_t out[4]) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    std::memcpy(out, g_last_detail, sizeof(g_last_detail));
+}
+
+}  // extern "C"

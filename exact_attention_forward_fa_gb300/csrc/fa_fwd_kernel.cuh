@@ -1,0 +1,418 @@
+// fa_fwd_kernel.cuh -- exact attention forward on sm_103a (tcgen05 + TMA).
+//
+// What it computes ("FlashAttention-3 on Hopper", sec. 4.1-4.7): for every
+// (batch b, head h) and query row i,
+//     O_i = sum_j softmax_j(alpha q_i . k_j) v_j,   LSE_i = log sum_j exp(.)
+// over visible keys j (causal: j <= i), tile by tile with an online softmax
+// so no N x N matrix is stored.
+//
+// How (the Blackwell forward schedule of "FlashAttention v1-v4", FA4
+// sections "TMEM", "forward schedule: two Q tiles, two softmax groups" and
+// "conditional rescale", re-planned for GB300):
+//   * Persistent grid, one CTA per SM.  A work unit is a pair of 128-row Q
+//     tiles (tile L = 2p, tile H = 2p+1) of one (b, h); both share one
+//     stream of 128-key K/V tiles, visited in descending order so that the
+//     masked tiles (sequence tail, causal diagonal) come first
+//     ("FlashAttention-3 on Hopper", sec. 4.7).
+//   * Warp 8 (one lane) is the TMA producer: Q_L/Q_H once per unit, then
+//     K_j and V_j into a ring of shared-memory stages guarded by full/empty
+//     mbarriers ("FlashAttention-3 on Hopper", sec. 4.3.1).
+//   * Warp 9 (one lane) issues every tcgen05.mma: S_X = Q_X K_j^T into
+//     TMEM, O_X += P_X V_j with P_X read from TMEM (TS form).  Per step the
+//     order is PV_L(j+1), QK_L(j), PV_H(j+1), QK_H(j), so each softmax group
+//     has the other tile's two GEMMs to hide behind.
+//   * Warps 0-3 / 4-7 are the softmax groups for tiles L / H: thread t owns
+//     row t (TMEM lane t), reads its 128 scores with tcgen05.ld, masks,
+//     takes the row max, applies the conditional-rescale rule with threshold
+//     tau = 8 (log2 units), evaluates exp2 on MUFU, accumulates the row sum
+//     in FP32, writes P (bf16/fp16) back over its S columns with tcgen05.st,
+//     and rescales its O row in TMEM when the reference point moved.  After
+//     the last tile it normalises O by 1/l and stores O and LSE.
+//   * TMEM (512 columns): S_L [0,128), S_H [128,256), O_L [256,256+D),
+//     O_H [256+D, 256+2D); P_X (64 columns of packed pairs) overlays the
+//     first half of S_X.
+// Every mbarrier wait is bounded (fa_device.cuh).
+#pragma once
+
+#include "fa_device.cuh"
+
+namespace fa {
+
+struct FwdArgs {
+    void *o;             // [B][N][H][D]
+    float *lse;          // [B][H][N] or nullptr
+    uint32_t *status;    // device status word (4 x u32)
+    int B, H, N;
+    int n_kv;            // ceil(N / 128) key tiles
+    int n_pairs;         // ceil(ceil(N / 128) / 2) Q-tile pairs per head
+    int n_units;         // B * H * n_pairs
+    float scale_log2;    // alpha * log2(e)
+};
+
+template <int D, bool kCausal, bool kBF16>
+struct FwdCfg {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int BM = 128;                      // query rows per tile
+    static constexpr int BN = 128;                      // keys per tile
+    static constexpr int NCH = D / 64;                  // 128-byte column chunks
+    static constexpr uint32_t CHUNK_BYTES = 128u * 128u;  // 128 rows x 128 B
+    static constexpr uint32_t TILE_BYTES = NCH * CHUNK_BYTES;
+    static constexpr int NSTAGE = (D == 64) ? 8 : 5;
+    static constexpr int NTHREADS = 320;
+
+    // shared memory map (offsets from a 1024-B aligned base)
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t KV_OFF = 2 * TILE_BYTES;
+    static constexpr uint32_t BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
+    // barrier indices
+    static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4,
+                         B_KVEMPTY = 4 + NSTAGE, B_SFULL = 4 + 2 * NSTAGE,
+                         B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
+                         B_OEMPTY = B_OFULL + 2, B_MMADONE = B_OEMPTY + 2,
+                         NBAR = B_MMADONE + 1;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
+    static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;   // + align slack
+
+    // TMEM columns
+    static constexpr uint32_t TMEM_COLS = 512;
+    __host__ __device__ static constexpr uint32_t col_s(int x) { return x ? 128u : 0u; }
+    __host__ __device__ static constexpr uint32_t col_o(int x) { return 256u + (x ? D : 0u); }
+
+    static constexpr uint32_t IDESC_QK = idesc_f16(128, 128, kBF16, false, false);
+    static constexpr uint32_t IDESC_PV = idesc_f16(128, D, kBF16, false, true);
+    static constexpr float TAU = 8.0f;
+};
+
+// The geometry of one work unit, identical in every role.
+struct Unit {
+    int b, h;
+    int m[2];       // Q tile indices (L, H)
+    bool act[2];    // tile holds at least one real row
+    int T;          // key tiles visited (descending from T-1 to 0)
+    int t0[2];      // first step at which tile X takes part (T if never)
+};
+
+template <bool kCausal>
+__device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
+    Unit U;
+    const int BH = a.B * a.H;
+    int p, bh;
+    if (kCausal) {          // longest-first: the last pairs of every head first
+        p = a.n_pairs - 1 - u / BH;
+        bh = u % BH;
+    } else {                // consecutive units share a head's K/V in L2
+        p = u % a.n_pairs;
+        bh = u / a.n_pairs;
+    }
+    U.b = bh / a.H;
+    U.h = bh % a.H;
+    int hi[2];
+    for (int x = 0; x < 2; ++x) {
+        U.m[x] = 2 * p + x;
+        U.act[x] = U.m[x] * 128 < a.N;
+        hi[x] = U.act[x] ? (kCausal ? min(a.n_kv, U.m[x] + 1) : a.n_kv) : 0;
+    }
+    U.T = max(hi[0], hi[1]);
+    for (int x = 0; x < 2; ++x) U.t0[x] = U.act[x] ? U.T - hi[x] : U.T;
+    return U;
+}
+
+template <int D, bool kCausal, bool kBF16>
+__global__ void __launch_bounds__(320, 1)
+fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+              const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+    using C = FwdCfg<D, kCausal, kBF16>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF + 4);
+
+    // ---- prologue: TMEM allocation (warp 9) and barrier init (thread 0) ----
+    if (warp == 9) tmem_alloc(base + C::MISC_OFF, C::TMEM_COLS);
+    if (tid == 0) {
+        *abort_flag = 0u;
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(C::B_QFULL + x), 1);
+            mbar_init(bar(C::B_QEMPTY + x), 1);
+            mbar_init(bar(C::B_SFULL + x), 1);
+            mbar_init(bar(C::B_PFULL + x), 4);
+            mbar_init(bar(C::B_OFULL + x), 1);
+            mbar_init(bar(C::B_OEMPTY + x), 4);
+        }
+        for (int s = 0; s < C::NSTAGE; ++s) {
+            mbar_init(bar(C::B_KVFULL + s), 1);
+            mbar_init(bar(C::B_KVEMPTY + s), 1);
+        }
+        mbar_init(bar(C::B_MMADONE), 1);
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 8) {
+        // =================== TMA producer (one lane) ===================
+        if (lane == 0) {
+            WaitCtx w{abort_flag, a.status, kRoleProducer};
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            int qn[2] = {0, 0};
+            uint32_t slot = 0, phase = 0;
+            uint32_t armed = 0, armed_par = 0;      // per-slot: ever armed / parity
+            bool q_armed[2] = {false, false};
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+                const Unit U = make_unit<kCausal>(u, a);
+                for (int x = 0; x < 2 && ok; ++x) {
+                    if (!U.act[x]) continue;
+                    ok = mbar_wait(bar(C::B_QEMPTY + x), (qn[x] & 1) ^ 1, w, 1);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(C::B_QFULL + x), C::TILE_BYTES);
+                    for (int c = 0; c < C::NCH; ++c)
+                        tma_load_4d(&tm_q, base + C::Q_OFF + x * C::TILE_BYTES + c * C::CHUNK_BYTES,
+                                    bar(C::B_QFULL + x), c * 64, U.h, U.m[x] * 128, U.b);
+                    q_armed[x] = true;
+                    ++qn[x];
+                }
+                for (int t = 0; t < U.T && ok; ++t) {
+                    const int j = U.T - 1 - t;
+                    for (int kv = 0; kv < 2; ++kv) {
+                        ok = mbar_wait(bar(C::B_KVEMPTY + slot), phase ^ 1, w, 2);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(bar(C::B_KVFULL + slot), C::TILE_BYTES);
+                        const CUtensorMap *tm = kv ? &tm_v : &tm_k;
+                        for (int c = 0; c < C::NCH; ++c)
+                            tma_load_4d(tm, base + C::KV_OFF + slot * C::TILE_BYTES + c * C::CHUNK_BYTES,
+                                        bar(C::B_KVFULL + slot), c * 64, U.h, j * 128, U.b);
+                        armed |= 1u << slot;
+                        armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
+                        if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
+                    }
+                }
+            }
+            // Let every copy this lane issued land before the CTA can exit.
+            for (int s = 0; s < C::NSTAGE; ++s)
+                if (armed & (1u << s))
+                    mbar_wait_quiet(bar(C::B_KVFULL + s), (armed_par >> s) & 1u, 500000000ull);
+            for (int x = 0; x < 2; ++x)
+                if (q_armed[x])
+                    mbar_wait_quiet(bar(C::B_QFULL + x), (qn[x] - 1) & 1, 500000000ull);
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // =================== MMA issuer (one lane) ===================
+        if (lane == 0) {
+            WaitCtx w{abort_flag, a.status, kRoleMma};
+            int qn[2] = {0, 0}, un[2] = {0, 0};
+            uint32_t pph[2] = {0, 0};
+            uint32_t slot = 0, phase = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+                const Unit U = make_unit<kCausal>(u, a);
+                for (int t = 0; t <= U.T && ok; ++t) {
+                    const bool has_v = t > 0, has_k = t < U.T;
+                    uint32_t vslot = 0, vph = 0, kslot = 0, kph = 0;
+                    if (has_v) { vslot = slot; vph = phase; if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; } }
+                    if (has_k) { kslot = slot; kph = phase; if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; } }
+                    bool v_ready = false, k_ready = false;
+                    for (int x = 0; x < 2 && ok; ++x) {
+                        // ---- O_x += P_x V_(t-1) ----
+                        if (has_v && t - 1 >= U.t0[x]) {
+                            if (!v_ready) { ok = mbar_wait(bar(C::B_KVFULL + vslot), vph, w, 10); v_ready = true; }
+                            if (ok && t - 1 == U.t0[x])
+                                ok = mbar_wait(bar(C::B_OEMPTY + x), (un[x] & 1) ^ 1, w, 11);
+                            if (ok) ok = mbar_wait(bar(C::B_PFULL + x), pph[x], w, 12);
+                            if (!ok) break;
+                            pph[x] ^= 1;
+                            tc_fence_after();
+                            const uint32_t vbase = base + C::KV_OFF + vslot * C::TILE_BYTES;
+#pragma unroll
+                            for (int kk = 0; kk < C::BN / 16; ++kk) {
+                                const uint64_t bd = smem_desc_sw128(vbase + kk * 2048u, C::CHUNK_BYTES, 1024u);
+                                mma_ts_f16(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u, bd,
+                                           C::IDESC_PV, (t - 1 > U.t0[x] || kk > 0) ? 1u : 0u);
+                            }
+                            if (t == U.T) mma_commit(bar(C::B_OFULL + x));
+                        }
+                        // ---- S_x = Q_x K_t^T ----
+                        if (has_k && t >= U.t0[x]) {
+                            if (!k_ready) { ok = mbar_wait(bar(C::B_KVFULL + kslot), kph, w, 13); k_ready = true; }
+                            if (ok && t == U.t0[x]) {
+                                ok = mbar_wait(bar(C::B_QFULL + x), qn[x] & 1, w, 14);
+                                ++qn[x];
+                            }
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint32_t qb = base + C::Q_OFF + x * C::TILE_BYTES;
+                            const uint32_t kb = base + C::KV_OFF + kslot * C::TILE_BYTES;
+#pragma unroll
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32u;
+                                mma_ss_f16(tbase + C::col_s(x), smem_desc_sw128(qb + off, 16u, 1024u),
+                                           smem_desc_sw128(kb + off, 16u, 1024u), C::IDESC_QK,
+                                           kk > 0 ? 1u : 0u);
+                            }
+                            mma_commit(bar(C::B_SFULL + x));
+                            if (t == U.T - 1) mma_commit(bar(C::B_QEMPTY + x));
+                        }
+                    }
+                    if (!ok) break;
+                    if (has_k) mma_commit(bar(C::B_KVEMPTY + kslot));
+                    if (has_v) mma_commit(bar(C::B_KVEMPTY + vslot));
+                }
+                for (int x = 0; x < 2; ++x) if (U.act[x]) ++un[x];
+            }
+            // Drain: every issued MMA completes before TMEM is released.
+            mma_commit(bar(C::B_MMADONE));
+            mbar_wait_quiet(bar(C::B_MMADONE), 0, 500000000ull);
+        }
+        __syncwarp();
+    } else {
+        // =================== softmax group x (warps 4x .. 4x+3) ===================
+        const int x = warp >> 2;
+        const int row = tid & 127;                       // TMEM lane == tile row
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tbase + lane_off + C::col_s(x);
+        const uint32_t tO = tbase + lane_off + C::col_o(x);
+        WaitCtx w{abort_flag, a.status, x ? kRoleSoftmax1 : kRoleSoftmax0};
+        const float sl2 = a.scale_log2;
+        uint32_t sph = 0, oph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            const Unit U = make_unit<kCausal>(u, a);
+            if (!U.act[x]) continue;
+            float r = -INFINITY, l = 0.f;
+            for (int t = U.t0[x]; t < U.T; ++t) {
+                const int j = U.T - 1 - t;
+                ok = mbar_wait(bar(C::B_SFULL + x), sph, w, 20);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                sph ^= 1;
+                tc_fence_after();
+                uint32_t s[128];
+                tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+                tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+                tmem_ld_wait();
+                float *sf = reinterpret_cast<float *>(s);
+                // ---- masks: sequence tail and causal diagonal ----
+                int lim = 128;
+                if (j == a.n_kv - 1) lim = min(lim, a.N - j * 128);
+                if (kCausal && j == U.m[x]) lim = min(lim, row + 1);
+                if (lim < 128) {
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) if (c >= lim) sf[c] = -INFINITY;
+                }
+                // ---- row max ----
+                float m0 = sf[0], m1 = sf[1], m2 = sf[2], m3 = sf[3];
+#pragma unroll
+                for (int c = 4; c < 128; c += 8) {
+                    m0 = max3(m0, sf[c + 0], sf[c + 4]);
+                    m1 = max3(m1, sf[c + 1], sf[c + 5]);
+                    m2 = max3(m2, sf[c + 2], sf[c + 6]);
+                    m3 = max3(m3, sf[c + 3], sf[c + 7]);
+                }
+                const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+                const float bnew = mx * sl2;                    // -inf stays -inf
+                // ---- conditional rescale: move r only if the max grew by > tau ----
+                float rn, corr;
+                if (r == -INFINITY) { rn = bnew; corr = 1.f; }
+                else { rn = (bnew > r + C::TAU) ? bnew : r; corr = ex2_approx(r - rn); }
+                const bool need = (r != -INFINITY) && (rn != r);
+                const float rs = (rn == -INFINITY) ? 0.f : rn;
+                // ---- exponentials, row sum, P ----
+                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+                uint32_t p[64];
+#pragma unroll
+                for (int c = 0; c < 128; c += 4) {
+                    const float e0 = ex2_approx(fmaf(sf[c + 0], sl2, -rs));
+                    const float e1 = ex2_approx(fmaf(sf[c + 1], sl2, -rs));
+                    const float e2 = ex2_approx(fmaf(sf[c + 2], sl2, -rs));
+                    const float e3 = ex2_approx(fmaf(sf[c + 3], sl2, -rs));
+                    l0 += e0; l1 += e1; l2 += e2; l3 += e3;
+                    p[c / 2] = pack2<kBF16>(e0, e1);
+                    p[c / 2 + 1] = pack2<kBF16>(e2, e3);
+                }
+                l = l * corr + ((l0 + l1) + (l2 + l3));
+                tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+                tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                // ---- correction of O (its previous PV completed before S_FULL) ----
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                    for (int ch = 0; ch < D / 32; ++ch) {
+                        uint32_t ov[32];
+                        tmem_ld32(tO + ch * 32, ov);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
+                        tmem_st32(tO + ch * 32, ov);
+                    }
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_PFULL + x));
+                r = rn;
+            }
+            if (!ok) break;
+            // ---- epilogue: O / l -> global, LSE ----
+            ok = mbar_wait(bar(C::B_OFULL + x), oph, w, 21);
+            if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+            oph ^= 1;
+            tc_fence_after();
+            const bool live = (l > 0.f) && (l == l);
+            const float inv = live ? 1.f / l : 0.f;
+            const int grow = U.m[x] * 128 + row;
+            using elem_t = uint16_t;
+            elem_t *orow = reinterpret_cast<elem_t *>(a.o) +
+                           ((static_cast<size_t>(U.b) * a.N + grow) * a.H + U.h) * D;
+#pragma unroll 1
+            for (int ch = 0; ch < D / 32; ++ch) {
+                uint32_t ov[32];
+                tmem_ld32(tO + ch * 32, ov);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack2<kBF16>(__uint_as_float(ov[2 * i]) * inv,
+                                         __uint_as_float(ov[2 * i + 1]) * inv);
+                if (grow < a.N) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + x));
+            if (a.lse != nullptr && grow < a.N) {
+                const float lse = live ? (r + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+                a.lse[(static_cast<size_t>(U.b) * a.H + U.h) * a.N + grow] = lse;
+            }
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+}  // namespace fa

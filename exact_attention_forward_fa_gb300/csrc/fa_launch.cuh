@@ -1,0 +1,53 @@
+// fa_launch.cuh -- host-side launch record shared by the C-ABI translation
+// unit (fa_api.cu) and the per-head-dim kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+struct FwdLaunch {
+    CUtensorMap q, k, v;   // 4-D maps {d, H, N, B}, box {64, 1, 128, 1}, 128-B swizzle
+    FwdArgs args;
+    int grid;              // persistent CTAs (<= SM count)
+    cudaStream_t stream;
+    bool causal;
+    bool bf16;
+};
+
+cudaError_t launch_fwd_d64(const FwdLaunch &L);
+cudaError_t launch_fwd_d128(const FwdLaunch &L);
+
+// Shared helper: set the dynamic shared-memory limit once per device, then
+// launch one instantiation.
+template <int D, bool kCausal, bool kBF16>
+cudaError_t launch_fwd_inst(const FwdLaunch &L) {
+    using Cfg = FwdCfg<D, kCausal, kBF16>;
+    auto kern = fa_fwd_kernel<D, kCausal, kBF16>;
+    static unsigned long long configured = 0ull;   // bit per device id (< 64)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(Cfg::SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured, bit, __ATOMIC_ACQ_REL);
+    }
+    kern<<<L.grid, Cfg::NTHREADS, Cfg::SMEM_BYTES, L.stream>>>(L.q, L.k, L.v, L.args);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_fwd_dispatch(const FwdLaunch &L) {
+    if (L.causal) {
+        return L.bf16 ? launch_fwd_inst<D, true, true>(L) : launch_fwd_inst<D, true, false>(L);
+    }
+    return L.bf16 ? launch_fwd_inst<D, false, true>(L) : launch_fwd_inst<D, false, false>(L);
+}
+
+}  // namespace fa

@@ -1,0 +1,105 @@
+/*
+ * fa.h -- C ABI of libfa: exact attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("FlashAttention-3 on Hopper", sec. 3.1 and 4.1-4.7; the
+ * Blackwell schedule in "FlashAttention v1-v4", FA4 sections):
+ *
+ *     S = alpha * Q K^T  (+ causal mask: key j hidden from query i when
+ *                          j > i, i.e. col > row + (Nk - Nq) with Nq = Nk)
+ *     O = softmax_rows(S) V
+ *     LSE_i = log sum_j exp(S_ij)                    (natural log)
+ *
+ * computed tile by tile with an online softmax, so the N x N score matrix
+ * never reaches device memory.  Rows with no visible key would give O = 0,
+ * LSE = -inf ("FlashAttention-3 on Hopper", sec. 4.6); with Nq = Nk every
+ * row sees at least one key.
+ *
+ * Layouts (all contiguous, row-major):
+ *     Q, K, V, O : [B][N][H][d]   (batch, sequence, head, head dim),
+ *                                 element (b,n,h,c) at ((b*N + n)*H + h)*d + c
+ *     LSE        : [B][H][N]      float32, element (b,h,n) at (b*H + h)*N + n
+ *     FP8 scales : [B][H][ceil(N/128)] float32, one per 128-row tile of a head
+ *
+ * Conventions for every entry point:
+ *   * Pointers named q, k, v, o, lse, x, x8, *_scale are DEVICE pointers
+ *     owned by the caller; the library never frees or keeps them.
+ *   * `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous: they validate, launch and return.
+ *   * Arguments are validated on the host before anything is launched; a
+ *     failed check returns an error code and launches nothing.
+ *   * The library allocates no device memory per call.  It owns one small
+ *     per-device status word in a static __device__ variable that kernels
+ *     set when a bounded wait gives up; fa_check_status reads it.
+ *   * Results are deterministic for fixed inputs: fixed reduction order, no
+ *     atomics on outputs.
+ *   * Thread safety: entry points may be called from several host threads;
+ *     the per-device caches inside are guarded by a mutex.
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad flag, non-finite alpha */
+    FA_ERR_UNSUPPORTED = 2,  /* head dim or dtype without a kernel, or not an sm_103 device */
+    FA_ERR_MISALIGNED = 3,   /* a tensor pointer is not 16-byte aligned (TMA rule) */
+    FA_ERR_TOO_LARGE = 4,    /* a size exceeds the TMA descriptor limits */
+    FA_ERR_CUDA = 5,         /* a CUDA runtime/driver call or the launch failed */
+    FA_ERR_TIMEOUT = 6       /* a kernel's bounded wait gave up (fa_check_status) */
+} fa_status;
+
+typedef enum {
+    FA_BF16 = 0,
+    FA_FP16 = 1
+} fa_dtype;
+
+/*
+ * fa_fwd -- exact attention forward, BF16 or FP16 in and out.
+ *   q, k, v : device, [B][N][H][d] in `dtype`, 16-byte aligned.
+ *   o       : device, [B][N][H][d] in `dtype`, 16-byte aligned (written).
+ *   lse     : device, float [B][H][N], 4-byte aligned, or NULL to skip.
+ *   B, H, N : >= 1.  d in {64, 128} (256 returns FA_ERR_UNSUPPORTED until
+ *             its kernel exists).
+ *   alpha   : the score scale (usually 1/sqrt(d)); must be finite.
+ *   causal  : 0 or 1.
+ * Accumulation is FP32; P is rounded to `dtype` before the P V product;
+ * O is rounded to `dtype` round-to-nearest-even.
+ */
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
+                 float *lse, int B, int H, int N, int d, float alpha,
+                 int causal, fa_dtype dtype, void *stream);
+
+/*
+ * fa_check_status -- synchronizes `stream`, then reports and clears the
+ * device status word of the current device.  Returns FA_ERR_TIMEOUT if a
+ * kernel launched since the last check gave up on a bounded wait (its
+ * outputs are then undefined), FA_ERR_CUDA if the synchronization failed,
+ * FA_OK otherwise.
+ */
+fa_status fa_check_status(void *stream);
+
+/*
+ * fa_status_detail -- the status word captured by the last fa_check_status
+ * that returned FA_ERR_TIMEOUT: out[0] code, out[1] role that gave up
+ * (1/2 softmax group L/H, 3 producer, 4 MMA issuer), out[2] wait site,
+ * out[3] block index.  Zeros if no timeout was ever reported.
+ */
+void fa_status_detail(uint32_t out[4]);
+
+/* fa_status_string -- a static, human-readable name for a status code. */
+const char *fa_status_string(fa_status s);
+
+/* fa_version -- library version as major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,111 @@
+"""Host-side checks of the C-ABI library (no GPU, no compute calls).
+
+* libfa.so builds for sm_103a here (nvcc cross-compiles) and loads;
+* it exports every function include/fa.h declares, and nothing in the
+  binding refers to a symbol the header does not declare;
+* argument validation returns the documented codes before touching CUDA;
+* the product package never imports the oracle.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import exact_attention_forward_fa_gb300 as fa
+from exact_attention_forward_fa_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return fa.load()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    assert _header_functions() == sorted(fa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(\S+)", out))
+    for name in _header_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_version_and_status_strings(lib):
+    assert fa.fa_version() == 100
+    names = [fa.status_string(c) for c in range(7)]
+    assert names == ["FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED",
+                     "FA_ERR_MISALIGNED", "FA_ERR_TOO_LARGE", "FA_ERR_CUDA",
+                     "FA_ERR_TIMEOUT"]
+    assert fa.status_string(99) == "FA_ERR_UNKNOWN"
+    assert fa.fa_status_detail() == [0, 0, 0, 0]
+
+
+A = 0x10000          # fake, 16-byte aligned device addresses (never dereferenced)
+
+
+def _call(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=1, N=128, d=64, alpha=0.125,
+          causal=0, dtype=0):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(k=None), fa.FA_ERR_INVALID_ARG),
+    (dict(v=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=None), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(alpha=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(alpha=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(B=1 << 20, H=1 << 10, N=1 << 20, d=128), fa.FA_ERR_TOO_LARGE),
+])
+def test_validation_codes(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the gpu tests")
+    assert _call(lib) in (fa.FA_ERR_CUDA, fa.FA_ERR_UNSUPPORTED)
+
+
+def test_product_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "exact_attention_forward_fa_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "fa_oracle" not in text and "liboracle" not in text, f
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import importlib
+    mod = importlib.import_module("exact_attention_forward_fa_gb300")
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(mod, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        mod.load()

@@ -1,0 +1,175 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle.
+
+Tolerances (stated for unit-variance inputs): O max-abs <= 1e-2, O RMSE
+<= 2e-3, LSE max-abs <= 1e-3.  Small and ragged shapes are compared element
+by element in full; the full-size workloads (B4 H16 N4096 d128 and the
+16k-token sequence sweep) are compared on sampled (b, h, row) outputs that
+the oracle computes one by one, in the same launch configuration the bench
+times.  Exact pins: causal row 0 reproduces V[0] bit for bit, a constant V
+gives that constant, and two launches give identical bits.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_forward_fa_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_RMSE, LSE_MAX = 1e-2, 2e-3, 1e-3
+THREADS = os.cpu_count() or 4
+DT = {"bf16": torch.bfloat16, "fp16": torch.float16}
+
+
+def _run(fa, q, k, v, causal, alpha, want_lse=True, stream=None):
+    dev = torch.device("cuda")
+    o, lse = fa.attention(q.to(dev), k.to(dev), v.to(dev), causal=causal,
+                          alpha=alpha, want_lse=want_lse, stream=stream)
+    assert fa.fa_check_status() == fa.FA_OK
+    return o, lse
+
+
+def _check(o_gpu, lse_gpu, o_ref, lse_ref):
+    o = o_gpu.astype(np.float64)
+    err = np.abs(o - o_ref)
+    rmse = float(np.sqrt(np.mean(err ** 2)))
+    assert np.all(np.isfinite(o))
+    assert err.max() <= O_MAX, f"O max-abs {err.max():.3e}"
+    assert rmse <= O_RMSE, f"O rmse {rmse:.3e}"
+    if lse_gpu is not None:
+        lerr = np.abs(lse_gpu.astype(np.float64) - lse_ref)
+        assert lerr.max() <= LSE_MAX, f"LSE max-abs {lerr.max():.3e}"
+    return float(err.max()), rmse
+
+
+FULL_CASES = [
+    # (B, H, N, d, causal, dtype)
+    (1, 1, 128, 64, False, "bf16"),        # the smallest workload (one tile)
+    (2, 8, 1024, 64, False, "bf16"),       # B2 H8 N1024 d64
+    (2, 8, 1024, 64, True, "bf16"),
+    (2, 8, 1000, 64, False, "bf16"),       # N not a tile multiple
+    (2, 8, 1000, 64, True, "bf16"),
+    (1, 1, 1, 64, False, "bf16"),
+    (1, 1, 1, 128, True, "bf16"),
+    (1, 2, 127, 128, True, "bf16"),
+    (2, 3, 129, 64, True, "bf16"),
+    (1, 2, 255, 64, False, "bf16"),
+    (1, 1, 257, 128, True, "bf16"),
+    (1, 2, 300, 128, False, "bf16"),
+    (3, 1, 384, 128, True, "bf16"),
+    (1, 2, 513, 128, False, "fp16"),
+    (1, 2, 513, 128, True, "fp16"),
+    (1, 1, 640, 64, True, "fp16"),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,dtype", FULL_CASES)
+def test_full_parity(gpu_lib, B, H, N, d, causal, dtype):
+    q, k, v = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + N, dtype=dtype)
+    alpha = synth.default_alpha(d)
+    o, lse = _run(gpu_lib, q, k, v, causal, alpha)
+    o_ref, lse_ref = oracle.attention(q, k, v, alpha, causal, n_threads=THREADS)
+    _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref)
+
+
+def _sampled(fa, B, H, N, d, causal, n_heads=3, n_rows=24, seed=0):
+    q, k, v = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + 7 * N + d)
+    alpha = synth.default_alpha(d)
+    o, lse = _run(fa, q, k, v, causal, alpha)
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    rng = np.random.default_rng(seed + N + d)
+    heads = {(0, 0), (B - 1, H - 1)}
+    while len(heads) < min(n_heads, B * H):
+        heads.add((int(rng.integers(B)), int(rng.integers(H))))
+    for b, h in sorted(heads):
+        rows = sorted(set([0, 1, 127, 128, N // 2, N - 1] +
+                          rng.integers(0, N, size=n_rows).tolist()))
+        o_ref, lse_ref = oracle.attention_rows(q, k, v, alpha, causal, b, h, rows)
+        _check(o[b, rows, h, :], lse[b, h, rows], o_ref, lse_ref)
+
+
+def test_sampled_b4_h16_n4096_d128(gpu_lib):
+    _sampled(gpu_lib, 4, 16, 4096, 128, False)
+
+
+SWEEP = [(n, d, h, c) for n in (512, 1024, 2048, 4096, 8192, 16384)
+         for (d, h) in ((64, 32), (128, 16)) for c in (False, True)]
+
+
+@pytest.mark.parametrize("N,d,H,causal", SWEEP)
+def test_sampled_sequence_sweep(gpu_lib, N, d, H, causal):
+    _sampled(gpu_lib, 16384 // N, H, N, d, causal, n_heads=2, n_rows=16)
+
+
+def test_head_dim_256_not_yet_supported(gpu_lib):
+    fa = gpu_lib
+    x = torch.zeros((1, 128, 1, 256), dtype=torch.bfloat16, device="cuda")
+    rc = fa.fa_fwd(x, x, x, x, None, 1, 1, 128, 256, 0.0625, 0, fa.FA_BF16)
+    assert rc == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_causal_row_zero_is_v0_exactly(gpu_lib, d):
+    B, H, N = 2, 3, 700
+    q, k, v = synth.qkv(B, H, N, d, seed=11)
+    o, lse = _run(gpu_lib, q, k, v, True, synth.default_alpha(d))
+    assert torch.equal(o[:, 0].cpu(), v[:, 0])
+    s0 = synth.default_alpha(d) * (q[:, 0].double() * k[:, 0].double()).sum(-1)
+    assert torch.allclose(lse[:, :, 0].cpu().double(), s0, atol=1e-5, rtol=0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_values_give_the_constant(gpu_lib, causal):
+    B, H, N, d = 1, 2, 1000, 128
+    q, k, _ = synth.qkv(B, H, N, d, seed=5)
+    v = torch.full((B, N, H, d), 0.71875, dtype=torch.bfloat16)   # exact in bf16
+    o, _ = _run(gpu_lib, q, k, v, causal, synth.default_alpha(d))
+    of = o.float().cpu()
+    # sum_j p_j c / sum_j p_j = c up to FP32 rounding, then one bf16 rounding
+    assert (of - 0.71875).abs().max().item() <= 2.0 ** -8
+
+
+def test_deterministic_bits_lse_optional_and_side_stream(gpu_lib):
+    fa = gpu_lib
+    B, H, N, d = 2, 4, 1536, 128
+    q, k, v = synth.qkv(B, H, N, d, seed=3)
+    a = synth.default_alpha(d)
+    o1, l1 = _run(fa, q, k, v, False, a)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o2, l2 = _run(fa, q, k, v, False, a, stream=s)
+    s.synchronize()
+    o3, l3 = _run(fa, q, k, v, False, a, want_lse=False)
+    assert l3 is None
+    assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
+
+
+@pytest.mark.parametrize("alpha", [0.03, 0.5])
+def test_other_scales_and_wide_scores(gpu_lib, alpha):
+    # Scores with a wide spread move the reference point often (tau = 8).
+    B, H, N, d = 1, 2, 777, 64
+    q, k, v = synth.qkv(B, H, N, d, seed=21)
+    q = (q.float() * 3).to(torch.bfloat16)
+    for causal in (False, True):
+        o, lse = _run(gpu_lib, q, k, v, causal, alpha)
+        o_ref, lse_ref = oracle.attention(q, k, v, alpha, causal, n_threads=THREADS)
+        _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref)
+
+
+def test_outputs_beyond_n_untouched(gpu_lib):
+    # Rows >= N of the last tile are computed but never stored.
+    fa = gpu_lib
+    B, H, N, d = 1, 1, 200, 128
+    q, k, v = synth.qkv(B, H, N, d, seed=9)
+    big = torch.full((B, N + 64, H, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    o = big[:, :N]                                  # contiguous prefix view
+    lse = torch.full((B, H, N + 64), 9.0, dtype=torch.float32, device="cuda")
+    rc = fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), o, lse, B, H, N, d,
+                   synth.default_alpha(d), 0, fa.FA_BF16)
+    assert rc == fa.FA_OK and fa.fa_check_status() == fa.FA_OK
+    assert torch.all(big[:, N:] == 7.0)
+    assert torch.all(lse[:, :, N:] == 9.0)
