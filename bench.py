@@ -1,0 +1,374 @@
+"""Throughput of the exact attention forward (fa_fwd) on GB300.
+
+One step = one fa_fwd launch over the whole workload: B=4, H=16, N=4096,
+d=128, BF16, non-causal (hidden 2048, 16k tokens), Q/K/V iid N(0,1) from
+fixed seeds.  Metric: attention forward TFLOP/s = 4*B*H*N^2*d / time
+(halved for causal) and its percentage of the 2250 TFLOP/s dense BF16 peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--causal]
+                  [--impl ours|reference] [--skip-cpu]
+
+The device-resident number times K back-to-back launches with CUDA events
+on the launching stream (inputs of 192 MiB exceed the 126 MB L2, so no
+flush is needed between steps).  ``e2e`` times the same steps through the
+C ABI with pinned host buffers: host->device copies of Q/K/V, the launch and
+the device->host copy of O and LSE, every step.  ``cpu_baseline`` is the
+FP64 CPU oracle on a bounded sample of the same workload.
+``--impl reference`` times that oracle alone, as the reference arm.
+Under torchrun every rank runs the full workload on its own GPU (independent
+replicas, weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+PEAK_SPEC = 2250.0          # TFLOP/s dense BF16, the metric's denominator
+METRIC = "attention fwd TFLOP/s (BF16, d=128) and % of 2250 TFLOP/s dense peak"
+WORKLOAD = dict(B=4, H=16, N=4096, d=128)
+
+
+def flops(B, H, N, d, causal):
+    f = 4.0 * B * H * N * N * d
+    return f / 2 if causal else f
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), float(m.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_forward_fa_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            t = json.load(f)
+        e = t[workload_key]
+        if e.get("source_hash") == source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample_rate(B, H, N, d, causal, rows_per_head, n_heads, threads):
+    """Times the FP64 oracle on `n_heads` heads x `rows_per_head` query rows
+    of the workload (full key range per row).  Returns (TFLOP/s, seconds,
+    description)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from exact_attention_forward_fa_gb300 import synth
+    alpha = synth.default_alpha(d)
+    heads = [(i // H % B, i % H) for i in range(n_heads)]
+    nb = max(b for b, _ in heads) + 1
+    q, k, v = synth.qkv(nb, H, N, d, seed=synth.BASE_SEED)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(N, size=min(rows_per_head, N), replace=False))
+    hq = [(oracle._f64(q[b, :, h]), oracle._f64(k[b, :, h]), oracle._f64(v[b, :, h]))
+          for b, h in heads]
+
+    def one(t):
+        qq, kk, vv = t
+        oracle.attention_head(qq, kk, vv, alpha, causal, rows=rows)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, hq))
+    dt = time.perf_counter() - t0
+    # FLOPs of the sampled rows: 4*d per visible (row, key) pair
+    vis = (rows + 1).sum() if causal else len(rows) * N
+    fl = 4.0 * d * float(vis) * n_heads
+    desc = (f"{n_heads} heads x {len(rows)} query rows (all keys) of B{B} H{H} N{N} d{d}"
+            f"{' causal' if causal else ''}, FP64 C oracle")
+    return fl / dt / 1e12, dt, desc
+
+
+def cpu_baseline(args, B, H, N, d):
+    """The oracle on the host cores: the whole workload when that takes under
+    ~30 s, else as many heads (all rows) as fit in ~20 s."""
+    threads = os.cpu_count() or 1
+    n0 = min(threads, B * H)
+    rate, dt, _ = oracle_sample_rate(B, H, N, d, args.causal, N, n0, threads)
+    per_head = dt * threads / n0                 # seconds for one head per thread
+    if per_head * (B * H) / threads <= 30.0:
+        heads = B * H
+    else:
+        heads = int(max(n0, min(B * H, 20.0 * threads / per_head)))
+    rate, dt, desc = oracle_sample_rate(B, H, N, d, args.causal, N, heads, threads)
+    return {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": desc, "seconds": round(dt, 2)}
+
+
+def run_reference(args, B, H, N, d, rank, world):
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    rate0, dt0, _ = oracle_sample_rate(B, H, N, d, args.causal, 16, threads, threads)
+    per_row = dt0 / 16.0
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(N, budget / per_row)))
+    for _ in range(args.warmup):
+        oracle_sample_rate(B, H, N, d, args.causal, rows, threads, threads)
+    rates, secs, desc = [], 0.0, ""
+    for _ in range(args.steps):
+        r, dt, desc = oracle_sample_rate(B, H, N, d, args.causal, rows, threads, threads)
+        rates.append(r)
+        secs += dt
+    value = float(np.median(rates))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": config_name(B, H, N, d, args.causal), "B": B, "H": H,
+                   "N": N, "d": d, "causal": args.causal},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "pct_of_2250": 100.0 * value / PEAK_SPEC,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_name(B, H, N, d, causal):
+    return (f"attention fwd B{B} H{H} N{N} d{d} bf16 {'causal' if causal else 'non-causal'}"
+            f" (hidden {H * d}, {B * N} tokens)")
+
+
+def run_ours(args, B, H, N, d, rank, world):
+    import torch
+    import torch.distributed as dist
+    import exact_attention_forward_fa_gb300 as fa
+    from exact_attention_forward_fa_gb300 import synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.load()
+    alpha = synth.default_alpha(d)
+    causal = int(args.causal)
+    qh, kh, vh = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + rank)
+    q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    def launch():
+        rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
+        if rc != fa.FA_OK:
+            raise fa.FaError(rc, "fa_fwd")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            launch()
+    stream.synchronize()
+    if fa.fa_check_status(sp) != fa.FA_OK:
+        raise RuntimeError("device status after warm-up: " + str(fa.fa_status_detail()))
+
+    # ---- device-resident timing ----
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(args.steps):
+                launch()
+            stop.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_total = start.elapsed_time(stop)
+    if fa.fa_check_status(sp) != fa.FA_OK:
+        raise RuntimeError("device status after timing: " + str(fa.fa_status_detail()))
+    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    fl = flops(B, H, N, d, args.causal)
+    value = world * fl * args.steps / (ms_max * 1e-3) / 1e12
+
+    # ---- end to end through the C ABI with pinned host buffers ----
+    qp, kp, vp = (x.pin_memory() for x in (qh, kh, vh))
+    op = torch.empty(qh.shape, dtype=qh.dtype).pin_memory()
+    lp = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        launch()
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    stream.synchronize()
+    barrier()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        stop.record(stream)
+    stream.synchronize()
+    barrier()
+    t2 = torch.tensor([start.elapsed_time(stop)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
+    e2e_value = world * fl * e2e_steps / (float(t2.item()) * 1e-3) / 1e12
+    h2d = 3 * qh.numel() * qh.element_size()
+    d2h = op.numel() * op.element_size() + lp.numel() * 4
+
+    if rank != 0:
+        return
+    burst, sustained, src = measured_peaks()
+    achieved = fl / (ms_step * 1e-3) / 1e12
+    wkey = config_name(B, H, N, d, args.causal)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs)",
+        "config": {"workload": wkey, "B": B, "H": H, "N": N, "d": d,
+                   "causal": bool(args.causal),
+                   "l2": "no flush: 192 MiB of inputs exceed the 126 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_2250": 100.0 * value / world / PEAK_SPEC,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": burst,
+                     "unit": "TFLOP/s", "frac": achieved / burst,
+                     "peak_source": f"{src} bf16 burst (cuBLAS 8192^3)",
+                     "traffic": profiled_traffic(wkey)},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.skip_cpu:
+        line["cpu_baseline"] = cpu_baseline(args, B, H, N, d)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true",
+                    help="omit the cpu_baseline leg (profiling runs)")
+    ap.add_argument("--B", type=int, default=WORKLOAD["B"])
+    ap.add_argument("--H", type=int, default=WORKLOAD["H"])
+    ap.add_argument("--N", type=int, default=WORKLOAD["N"])
+    ap.add_argument("--d", type=int, default=WORKLOAD["d"])
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    try:
+        if args.impl == "reference":
+            run_reference(args, args.B, args.H, args.N, args.d, rank, world)
+        else:
+            run_ours(args, args.B, args.H, args.N, args.d, rank, world)
+    finally:
+        if world > 1 and args.impl == "ours":
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -76,12 +76,14 @@ struct WaitCtx {
     uint32_t role;
 };
 
-static __device__ __noinline__ void report_timeout(const WaitCtx &w, uint32_t where) {
-    *w.abort_flag = 1u;
-    if (atomicCAS(&w.status[0], kStatusOk, kStatusTimeout) == kStatusOk) {
-        w.status[1] = w.role;
-        w.status[2] = where;
-        w.status[3] = blockIdx.x;
+static __device__ __noinline__ void report_timeout(volatile uint32_t *abort_flag,
+                                                   uint32_t *status, uint32_t role,
+                                                   uint32_t where) {
+    *abort_flag = 1u;
+    if (atomicCAS(&status[0], kStatusOk, kStatusTimeout) == kStatusOk) {
+        status[1] = role;
+        status[2] = where;
+        status[3] = blockIdx.x;
     }
     __threadfence();
 }
@@ -98,7 +100,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
         if ((it & 31u) == 0u) {
             if (*w.abort_flag) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                report_timeout(w, where);
+                report_timeout(w.abort_flag, w.status, w.role, where);
                 return false;
             }
         }
@@ -292,6 +294,19 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     }
     return r;
+}
+
+// Inverse of pack2: the two 16-bit floats of a packed pair, widened exactly.
+template <bool kBF16>
+__device__ __forceinline__ void unpack2(uint32_t pk, float &lo, float &hi) {
+    if constexpr (kBF16) {
+        lo = __uint_as_float(pk << 16);
+        hi = __uint_as_float(pk & 0xffff0000u);
+    } else {
+        asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+            "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+            : "=f"(lo), "=f"(hi) : "r"(pk));
+    }
 }
 
 }  // namespace fa

@@ -24,8 +24,9 @@
 //   * Warps 0-3 / 4-7 are the softmax groups for tiles L / H: thread t owns
 //     row t (TMEM lane t), reads its 128 scores with tcgen05.ld, masks,
 //     takes the row max, applies the conditional-rescale rule with threshold
-//     tau = 8 (log2 units), evaluates exp2 on MUFU, accumulates the row sum
-//     in FP32, writes P (bf16/fp16) back over its S columns with tcgen05.st,
+//     tau = 8 (log2 units), evaluates exp2 on MUFU, rounds P to bf16/fp16,
+//     accumulates the row sum of those rounded values in FP32, writes P back
+//     over its S columns with tcgen05.st,
 //     and rescales its O row in TMEM when the reference point moved.  After
 //     the last tile it normalises O by 1/l and stores O and LSE.
 //   * TMEM (512 columns): S_L [0,128), S_H [128,256), O_L [256,256+D),
@@ -167,24 +168,25 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            int qn[2] = {0, 0};
+            int qn0 = 0, qn1 = 0;                   // Q loads issued per tile slot
             uint32_t slot = 0, phase = 0;
             uint32_t armed = 0, armed_par = 0;      // per-slot: ever armed / parity
-            bool q_armed[2] = {false, false};
             bool ok = true;
+            auto load_q = [&](const int x, const Unit &U, int &qn)
+                              __attribute__((always_inline)) -> bool {
+                if (!mbar_wait(bar(C::B_QEMPTY + x), (qn & 1) ^ 1, w, 1)) return false;
+                mbar_arrive_expect_tx(bar(C::B_QFULL + x), C::TILE_BYTES);
+#pragma unroll
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_4d(&tm_q, base + C::Q_OFF + x * C::TILE_BYTES + c * C::CHUNK_BYTES,
+                                bar(C::B_QFULL + x), c * 64, U.h, U.m[x] * 128, U.b);
+                ++qn;
+                return true;
+            };
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
                 const Unit U = make_unit<kCausal>(u, a);
-                for (int x = 0; x < 2 && ok; ++x) {
-                    if (!U.act[x]) continue;
-                    ok = mbar_wait(bar(C::B_QEMPTY + x), (qn[x] & 1) ^ 1, w, 1);
-                    if (!ok) break;
-                    mbar_arrive_expect_tx(bar(C::B_QFULL + x), C::TILE_BYTES);
-                    for (int c = 0; c < C::NCH; ++c)
-                        tma_load_4d(&tm_q, base + C::Q_OFF + x * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                    bar(C::B_QFULL + x), c * 64, U.h, U.m[x] * 128, U.b);
-                    q_armed[x] = true;
-                    ++qn[x];
-                }
+                if (U.act[0]) ok = ok && load_q(0, U, qn0);
+                if (U.act[1]) ok = ok && load_q(1, U, qn1);
                 for (int t = 0; t < U.T && ok; ++t) {
                     const int j = U.T - 1 - t;
                     for (int kv = 0; kv < 2; ++kv) {
@@ -205,17 +207,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             for (int s = 0; s < C::NSTAGE; ++s)
                 if (armed & (1u << s))
                     mbar_wait_quiet(bar(C::B_KVFULL + s), (armed_par >> s) & 1u, 500000000ull);
-            for (int x = 0; x < 2; ++x)
-                if (q_armed[x])
-                    mbar_wait_quiet(bar(C::B_QFULL + x), (qn[x] - 1) & 1, 500000000ull);
+            if (qn0 > 0) mbar_wait_quiet(bar(C::B_QFULL + 0), (qn0 - 1) & 1, 500000000ull);
+            if (qn1 > 0) mbar_wait_quiet(bar(C::B_QFULL + 1), (qn1 - 1) & 1, 500000000ull);
         }
         __syncwarp();
     } else if (warp == 9) {
         // =================== MMA issuer (one lane) ===================
         if (lane == 0) {
             WaitCtx w{abort_flag, a.status, kRoleMma};
-            int qn[2] = {0, 0}, un[2] = {0, 0};
-            uint32_t pph[2] = {0, 0};
+            int qn0 = 0, qn1 = 0, un0 = 0, un1 = 0;
+            uint32_t pph0 = 0, pph1 = 0;
             uint32_t slot = 0, phase = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
@@ -226,33 +227,41 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     if (has_v) { vslot = slot; vph = phase; if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; } }
                     if (has_k) { kslot = slot; kph = phase; if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; } }
                     bool v_ready = false, k_ready = false;
-                    for (int x = 0; x < 2 && ok; ++x) {
+                    // One Q tile's two GEMMs of this step; x is a literal at
+                    // each call site, so every per-tile counter is a register.
+                    auto step_x = [&](const int x, const int t0x, int &qn, int &un,
+                                      uint32_t &pph) __attribute__((always_inline)) -> bool {
                         // ---- O_x += P_x V_(t-1) ----
-                        if (has_v && t - 1 >= U.t0[x]) {
-                            if (!v_ready) { ok = mbar_wait(bar(C::B_KVFULL + vslot), vph, w, 10); v_ready = true; }
-                            if (ok && t - 1 == U.t0[x])
-                                ok = mbar_wait(bar(C::B_OEMPTY + x), (un[x] & 1) ^ 1, w, 11);
-                            if (ok) ok = mbar_wait(bar(C::B_PFULL + x), pph[x], w, 12);
-                            if (!ok) break;
-                            pph[x] ^= 1;
+                        if (has_v && t - 1 >= t0x) {
+                            if (!v_ready) {
+                                if (!mbar_wait(bar(C::B_KVFULL + vslot), vph, w, 10)) return false;
+                                v_ready = true;
+                            }
+                            if (t - 1 == t0x &&
+                                !mbar_wait(bar(C::B_OEMPTY + x), (un & 1) ^ 1, w, 11)) return false;
+                            if (!mbar_wait(bar(C::B_PFULL + x), pph, w, 12)) return false;
+                            pph ^= 1;
                             tc_fence_after();
                             const uint32_t vbase = base + C::KV_OFF + vslot * C::TILE_BYTES;
+                            const uint32_t acc = (t - 1 > t0x) ? 1u : 0u;
 #pragma unroll
                             for (int kk = 0; kk < C::BN / 16; ++kk) {
                                 const uint64_t bd = smem_desc_sw128(vbase + kk * 2048u, C::CHUNK_BYTES, 1024u);
                                 mma_ts_f16(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u, bd,
-                                           C::IDESC_PV, (t - 1 > U.t0[x] || kk > 0) ? 1u : 0u);
+                                           C::IDESC_PV, (acc | kk) ? 1u : 0u);
                             }
                             if (t == U.T) mma_commit(bar(C::B_OFULL + x));
                         }
                         // ---- S_x = Q_x K_t^T ----
-                        if (has_k && t >= U.t0[x]) {
-                            if (!k_ready) { ok = mbar_wait(bar(C::B_KVFULL + kslot), kph, w, 13); k_ready = true; }
-                            if (ok && t == U.t0[x]) {
-                                ok = mbar_wait(bar(C::B_QFULL + x), qn[x] & 1, w, 14);
-                                ++qn[x];
+                        if (has_k && t >= t0x) {
+                            if (!k_ready) {
+                                if (!mbar_wait(bar(C::B_KVFULL + kslot), kph, w, 13)) return false;
+                                k_ready = true;
                             }
-                            if (!ok) break;
+                            if (t == t0x) {
+                                if (!mbar_wait(bar(C::B_QFULL + x), qn & 1, w, 14)) return false;
+                                ++qn;
+                            }
                             tc_fence_after();
                             const uint32_t qb = base + C::Q_OFF + x * C::TILE_BYTES;
                             const uint32_t kb = base + C::KV_OFF + kslot * C::TILE_BYTES;
@@ -266,12 +275,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                             mma_commit(bar(C::B_SFULL + x));
                             if (t == U.T - 1) mma_commit(bar(C::B_QEMPTY + x));
                         }
-                    }
+                        return true;
+                    };
+                    ok = step_x(0, U.t0[0], qn0, un0, pph0) && step_x(1, U.t0[1], qn1, un1, pph1);
                     if (!ok) break;
                     if (has_k) mma_commit(bar(C::B_KVEMPTY + kslot));
                     if (has_v) mma_commit(bar(C::B_KVEMPTY + vslot));
                 }
-                for (int x = 0; x < 2; ++x) if (U.act[x]) ++un[x];
+                un0 += U.act[0] ? 1 : 0;
+                un1 += U.act[1] ? 1 : 0;
             }
             // Drain: every issued MMA completes before TMEM is released.
             mma_commit(bar(C::B_MMADONE));
@@ -287,13 +299,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t tO = tbase + lane_off + C::col_o(x);
         WaitCtx w{abort_flag, a.status, x ? kRoleSoftmax1 : kRoleSoftmax0};
         const float sl2 = a.scale_log2;
+        const float2 c2 = make_float2(sl2, sl2);
         uint32_t sph = 0, oph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
             const Unit U = make_unit<kCausal>(u, a);
-            if (!U.act[x]) continue;
-            float r = -INFINITY, l = 0.f;
-            for (int t = U.t0[x]; t < U.T; ++t) {
+            const bool act = x ? U.act[1] : U.act[0];
+            if (!act) continue;
+            const int mt = x ? U.m[1] : U.m[0];
+            const int t0 = x ? U.t0[1] : U.t0[0];
+            // r: reference point (scaled log2 units); le: row sum of the FP32
+            // exponentials (for LSE); lr: row sum of the same values rounded
+            // as the P V product sees them (normalises O).
+            float r = -INFINITY, le = 0.f, lr = 0.f;
+            for (int t = t0; t < U.T; ++t) {
                 const int j = U.T - 1 - t;
                 ok = mbar_wait(bar(C::B_SFULL + x), sph, w, 20);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
@@ -309,7 +328,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // ---- masks: sequence tail and causal diagonal ----
                 int lim = 128;
                 if (j == a.n_kv - 1) lim = min(lim, a.N - j * 128);
-                if (kCausal && j == U.m[x]) lim = min(lim, row + 1);
+                if (kCausal && j == mt) lim = min(lim, row + 1);
                 if (lim < 128) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c) if (c >= lim) sf[c] = -INFINITY;
@@ -331,32 +350,47 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 else { rn = (bnew > r + C::TAU) ? bnew : r; corr = ex2_approx(r - rn); }
                 const bool need = (r != -INFINITY) && (rn != r);
                 const float rs = (rn == -INFINITY) ? 0.f : rn;
-                // ---- exponentials, row sum, P ----
-                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+                const float2 nr2 = make_float2(-rs, -rs);
+                // ---- exponentials, P, both row sums ----
+                float2 e_a = make_float2(0.f, 0.f), e_b = e_a, r_a = e_a, r_b = e_a;
                 uint32_t p[64];
 #pragma unroll
                 for (int c = 0; c < 128; c += 4) {
-                    const float e0 = ex2_approx(fmaf(sf[c + 0], sl2, -rs));
-                    const float e1 = ex2_approx(fmaf(sf[c + 1], sl2, -rs));
-                    const float e2 = ex2_approx(fmaf(sf[c + 2], sl2, -rs));
-                    const float e3 = ex2_approx(fmaf(sf[c + 3], sl2, -rs));
-                    l0 += e0; l1 += e1; l2 += e2; l3 += e3;
-                    p[c / 2] = pack2<kBF16>(e0, e1);
-                    p[c / 2 + 1] = pack2<kBF16>(e2, e3);
+                    const float2 x01 = __ffma2_rn(make_float2(sf[c + 0], sf[c + 1]), c2, nr2);
+                    const float2 x23 = __ffma2_rn(make_float2(sf[c + 2], sf[c + 3]), c2, nr2);
+                    const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+                    const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+                    const uint32_t pk0 = pack2<kBF16>(e01.x, e01.y);
+                    const uint32_t pk1 = pack2<kBF16>(e23.x, e23.y);
+                    p[c / 2] = pk0;
+                    p[c / 2 + 1] = pk1;
+                    float2 q01, q23;
+                    unpack2<kBF16>(pk0, q01.x, q01.y);
+                    unpack2<kBF16>(pk1, q23.x, q23.y);
+                    e_a = __fadd2_rn(e_a, e01);
+                    e_b = __fadd2_rn(e_b, e23);
+                    r_a = __fadd2_rn(r_a, q01);
+                    r_b = __fadd2_rn(r_b, q23);
                 }
-                l = l * corr + ((l0 + l1) + (l2 + l3));
+                le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y));
+                lr = lr * corr + ((r_a.x + r_a.y) + (r_b.x + r_b.y));
                 tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
                 tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
                 // ---- correction of O (its previous PV completed before S_FULL) ----
                 if (__any_sync(0xffffffffu, need)) {
+                    const float2 cc = make_float2(corr, corr);
 #pragma unroll 1
                     for (int ch = 0; ch < D / 32; ++ch) {
                         uint32_t ov[32];
                         tmem_ld32(tO + ch * 32, ov);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
+                        for (int i = 0; i < 32; i += 2) {
+                            const float2 v2 = __fmul2_rn(
+                                make_float2(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])), cc);
+                            ov[i] = __float_as_uint(v2.x);
+                            ov[i + 1] = __float_as_uint(v2.y);
+                        }
                         tmem_st32(tO + ch * 32, ov);
                     }
                 }
@@ -372,12 +406,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
             oph ^= 1;
             tc_fence_after();
-            const bool live = (l > 0.f) && (l == l);
-            const float inv = live ? 1.f / l : 0.f;
-            const int grow = U.m[x] * 128 + row;
-            using elem_t = uint16_t;
-            elem_t *orow = reinterpret_cast<elem_t *>(a.o) +
-                           ((static_cast<size_t>(U.b) * a.N + grow) * a.H + U.h) * D;
+            const bool live = (le > 0.f) && (lr > 0.f);
+            const float inv = live ? 1.f / lr : 0.f;
+            const int grow = mt * 128 + row;
+            uint16_t *orow = reinterpret_cast<uint16_t *>(a.o) +
+                             ((static_cast<size_t>(U.b) * a.N + grow) * a.H + U.h) * D;
 #pragma unroll 1
             for (int ch = 0; ch < D / 32; ++ch) {
                 uint32_t ov[32];
@@ -399,7 +432,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + x));
             if (a.lse != nullptr && grow < a.N) {
-                const float lse = live ? (r + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+                const float lse = live ? (r + log2f(le)) * 0.69314718055994530942f : -INFINITY;
                 a.lse[(static_cast<size_t>(U.b) * a.H + U.h) * a.N + grow] = lse;
             }
         }

@@ -68,8 +68,9 @@ typedef enum {
  *             its kernel exists).
  *   alpha   : the score scale (usually 1/sqrt(d)); must be finite.
  *   causal  : 0 or 1.
- * Accumulation is FP32; P is rounded to `dtype` before the P V product;
- * O is rounded to `dtype` round-to-nearest-even.
+ * Accumulation is FP32; P is rounded to `dtype` before the P V product and
+ * the softmax denominator sums those same rounded values; O is rounded to
+ * `dtype` round-to-nearest-even.
  */
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
                  float *lse, int B, int H, int N, int d, float alpha,

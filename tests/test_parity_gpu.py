@@ -32,12 +32,19 @@ def _run(fa, q, k, v, causal, alpha, want_lse=True, stream=None):
     return o, lse
 
 
-def _check(o_gpu, lse_gpu, o_ref, lse_ref):
+def _check(o_gpu, lse_gpu, o_ref, lse_ref, scale_aware=False):
     o = o_gpu.astype(np.float64)
     err = np.abs(o - o_ref)
     rmse = float(np.sqrt(np.mean(err ** 2)))
     assert np.all(np.isfinite(o))
-    assert err.max() <= O_MAX, f"O max-abs {err.max():.3e}"
+    if scale_aware:
+        # Inputs far from unit variance make |O| reach several units, where
+        # the spacing of BF16 values alone exceeds 1e-2: allow one BF16 ulp
+        # of the value (2^-8 |O|) on top of the unit-scale bound.
+        bound = O_MAX + 2.0 ** -8 * np.abs(o_ref)
+        assert np.all(err <= bound), f"O err/bound {(err / bound).max():.3f}"
+    else:
+        assert err.max() <= O_MAX, f"O max-abs {err.max():.3e}"
     assert rmse <= O_RMSE, f"O rmse {rmse:.3e}"
     if lse_gpu is not None:
         lerr = np.abs(lse_gpu.astype(np.float64) - lse_ref)
@@ -157,7 +164,8 @@ def test_other_scales_and_wide_scores(gpu_lib, alpha):
     for causal in (False, True):
         o, lse = _run(gpu_lib, q, k, v, causal, alpha)
         o_ref, lse_ref = oracle.attention(q, k, v, alpha, causal, n_threads=THREADS)
-        _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref)
+        _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref,
+               scale_aware=True)
 
 
 def test_outputs_beyond_n_untouched(gpu_lib):
