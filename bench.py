@@ -313,6 +313,13 @@ def run_ours(args, B, H, N, d, rank, world):
         return
     burst, sustained, src = measured_peaks()
     achieved = fl / (ms_step * 1e-3) / 1e12
+    # A timed region of back-to-back launches longer than a second runs
+    # under the power cap like the sustained cuBLAS loop; a short one is
+    # compared with the burst figure.
+    if ms_max >= 1000.0 and sustained > 0:
+        peak, peak_kind = sustained, "sustained"
+    else:
+        peak, peak_kind = burst, "burst"
     wkey = config_name(B, H, N, d, args.causal)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -324,9 +331,10 @@ def run_ours(args, B, H, N, d, rank, world):
                    "l2": "no flush: 192 MiB of inputs exceed the 126 MB L2",
                    "parallelism": f"replicas x{world}"},
         "pct_of_2250": 100.0 * value / world / PEAK_SPEC,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": burst,
-                     "unit": "TFLOP/s", "frac": achieved / burst,
-                     "peak_source": f"{src} bf16 burst (cuBLAS 8192^3)",
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{src} bf16 {peak_kind} (cuBLAS 8192^3)",
+                     "timed_region_ms": ms_max,
                      "traffic": profiled_traffic(wkey)},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},

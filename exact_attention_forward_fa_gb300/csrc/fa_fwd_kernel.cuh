@@ -212,8 +212,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         __syncwarp();
     } else if (warp == 9) {
-        // =================== MMA issuer (one lane) ===================
-        if (lane == 0) {
+        // =================== MMA issuer (whole warp, one elected lane issues) ===================
+        {
             WaitCtx w{abort_flag, a.status, kRoleMma};
             int qn0 = 0, qn1 = 0, un0 = 0, un1 = 0;
             uint32_t pph0 = 0, pph1 = 0;
@@ -234,59 +234,58 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         // ---- O_x += P_x V_(t-1) ----
                         if (has_v && t - 1 >= t0x) {
                             if (!v_ready) {
-                                if (!mbar_wait(bar(C::B_KVFULL + vslot), vph, w, 10)) return false;
+                                if (!mbar_wait_warp(bar(C::B_KVFULL + vslot), vph, w, 10)) return false;
                                 v_ready = true;
                             }
                             if (t - 1 == t0x &&
-                                !mbar_wait(bar(C::B_OEMPTY + x), (un & 1) ^ 1, w, 11)) return false;
-                            if (!mbar_wait(bar(C::B_PFULL + x), pph, w, 12)) return false;
+                                !mbar_wait_warp(bar(C::B_OEMPTY + x), (un & 1) ^ 1, w, 11)) return false;
+                            if (!mbar_wait_warp(bar(C::B_PFULL + x), pph, w, 12)) return false;
                             pph ^= 1;
                             tc_fence_after();
-                            const uint32_t vbase = base + C::KV_OFF + vslot * C::TILE_BYTES;
+                            const uint64_t vd = smem_desc_sw128(base + C::KV_OFF + vslot * C::TILE_BYTES,
+                                                                C::CHUNK_BYTES, 1024u);
                             const uint32_t acc = (t - 1 > t0x) ? 1u : 0u;
 #pragma unroll
-                            for (int kk = 0; kk < C::BN / 16; ++kk) {
-                                const uint64_t bd = smem_desc_sw128(vbase + kk * 2048u, C::CHUNK_BYTES, 1024u);
-                                mma_ts_f16(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u, bd,
-                                           C::IDESC_PV, (acc | kk) ? 1u : 0u);
-                            }
-                            if (t == U.T) mma_commit(bar(C::B_OFULL + x));
+                            for (int kk = 0; kk < C::BN / 16; ++kk)
+                                mma_ts_f16_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
+                                                 vd + ((kk * 2048u) >> 4), C::IDESC_PV,
+                                                 (acc | kk) ? 1u : 0u);
+                            if (t == U.T) mma_commit_elect(bar(C::B_OFULL + x));
                         }
                         // ---- S_x = Q_x K_t^T ----
                         if (has_k && t >= t0x) {
                             if (!k_ready) {
-                                if (!mbar_wait(bar(C::B_KVFULL + kslot), kph, w, 13)) return false;
+                                if (!mbar_wait_warp(bar(C::B_KVFULL + kslot), kph, w, 13)) return false;
                                 k_ready = true;
                             }
                             if (t == t0x) {
-                                if (!mbar_wait(bar(C::B_QFULL + x), qn & 1, w, 14)) return false;
+                                if (!mbar_wait_warp(bar(C::B_QFULL + x), qn & 1, w, 14)) return false;
                                 ++qn;
                             }
                             tc_fence_after();
-                            const uint32_t qb = base + C::Q_OFF + x * C::TILE_BYTES;
-                            const uint32_t kb = base + C::KV_OFF + kslot * C::TILE_BYTES;
+                            const uint64_t qd = smem_desc_sw128(base + C::Q_OFF + x * C::TILE_BYTES, 16u, 1024u);
+                            const uint64_t kd = smem_desc_sw128(base + C::KV_OFF + kslot * C::TILE_BYTES, 16u, 1024u);
 #pragma unroll
                             for (int kk = 0; kk < D / 16; ++kk) {
-                                const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32u;
-                                mma_ss_f16(tbase + C::col_s(x), smem_desc_sw128(qb + off, 16u, 1024u),
-                                           smem_desc_sw128(kb + off, 16u, 1024u), C::IDESC_QK,
-                                           kk > 0 ? 1u : 0u);
+                                const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32u) >> 4;
+                                mma_ss_f16_elect(tbase + C::col_s(x), qd + off, kd + off, C::IDESC_QK,
+                                                 kk > 0 ? 1u : 0u);
                             }
-                            mma_commit(bar(C::B_SFULL + x));
-                            if (t == U.T - 1) mma_commit(bar(C::B_QEMPTY + x));
+                            mma_commit_elect(bar(C::B_SFULL + x));
+                            if (t == U.T - 1) mma_commit_elect(bar(C::B_QEMPTY + x));
                         }
                         return true;
                     };
                     ok = step_x(0, U.t0[0], qn0, un0, pph0) && step_x(1, U.t0[1], qn1, un1, pph1);
                     if (!ok) break;
-                    if (has_k) mma_commit(bar(C::B_KVEMPTY + kslot));
-                    if (has_v) mma_commit(bar(C::B_KVEMPTY + vslot));
+                    if (has_k) mma_commit_elect(bar(C::B_KVEMPTY + kslot));
+                    if (has_v) mma_commit_elect(bar(C::B_KVEMPTY + vslot));
                 }
                 un0 += U.act[0] ? 1 : 0;
                 un1 += U.act[1] ? 1 : 0;
             }
             // Drain: every issued MMA completes before TMEM is released.
-            mma_commit(bar(C::B_MMADONE));
+            mma_commit_elect(bar(C::B_MMADONE));
             mbar_wait_quiet(bar(C::B_MMADONE), 0, 500000000ull);
         }
         __syncwarp();
