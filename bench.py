@@ -26,7 +26,6 @@ import json
 import os
 import subprocess
 import sys
-import threading
 import time
 
 import numpy as np
@@ -37,6 +36,23 @@ sys.path.insert(0, ROOT)
 PEAK_SPEC = 2250.0          # TFLOP/s dense BF16, the metric's denominator
 METRIC = "attention fwd TFLOP/s (BF16, d=128) and % of 2250 TFLOP/s dense peak"
 WORKLOAD = dict(B=4, H=16, N=4096, d=128)
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Maximum of a per-rank scalar over all ranks (identity on one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(flops_per_step: float, steps: int, ms_max: float, world: int) -> float:
+    """Whole-job TFLOP/s: every rank ran `steps` steps of the same workload
+    (replicas), and the job took the slowest rank's time."""
+    return world * flops_per_step * steps / (ms_max * 1e-3) / 1e12
 
 
 def flops(B, H, N, d, causal):
@@ -268,13 +284,10 @@ def run_ours(args, B, H, N, d, rank, world):
     ms_total = start.elapsed_time(stop)
     if fa.fa_check_status(sp) != fa.FA_OK:
         raise RuntimeError("device status after timing: " + str(fa.fa_status_detail()))
-    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = reduce_max(ms_total, world, dev)
     ms_step = ms_max / args.steps
     fl = flops(B, H, N, d, args.causal)
-    value = world * fl * args.steps / (ms_max * 1e-3) / 1e12
+    value = aggregate_value(fl, args.steps, ms_max, world)
 
     # ---- end to end through the C ABI with pinned host buffers ----
     qp, kp, vp = (x.pin_memory() for x in (qh, kh, vh))
@@ -302,10 +315,8 @@ def run_ours(args, B, H, N, d, rank, world):
         stop.record(stream)
     stream.synchronize()
     barrier()
-    t2 = torch.tensor([start.elapsed_time(stop)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t2, op=dist.ReduceOp.MAX)
-    e2e_value = world * fl * e2e_steps / (float(t2.item()) * 1e-3) / 1e12
+    e2e_ms = reduce_max(start.elapsed_time(stop), world, dev)
+    e2e_value = aggregate_value(fl, e2e_steps, e2e_ms, world)
     h2d = 3 * qh.numel() * qh.element_size()
     d2h = op.numel() * op.element_size() + lp.numel() * 4
 
