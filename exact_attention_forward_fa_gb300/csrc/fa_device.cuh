@@ -311,6 +311,20 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef FA_W8
 
 // ---------------------------------------------------------------------------
+// Register reallocation between warpgroups (all four warps of a warpgroup
+// execute the same instruction).  The sum over warpgroups must not exceed the
+// registers the block was launched with.
+// ---------------------------------------------------------------------------
+template <uint32_t N>
+__device__ __forceinline__ void regs_grow() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_shrink() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N));
+}
+
+// ---------------------------------------------------------------------------
 // Arithmetic helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -335,6 +349,21 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
         asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
     }
     return r;
+}
+
+// acc += lo + hi of a packed pair of 16-bit floats, each widened exactly,
+// with mixed-precision adds (no separate unpacking).
+template <bool kBF16>
+__device__ __forceinline__ void add_pair(float &acc0, float &acc1, uint32_t pk) {
+    if constexpr (kBF16) {
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+            : "+f"(acc0), "+f"(acc1) : "r"(pk));
+    } else {
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+            "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+            : "+f"(acc0), "+f"(acc1) : "r"(pk));
+    }
 }
 
 // Inverse of pack2: the two 16-bit floats of a packed pair, widened exactly.

@@ -14,6 +14,8 @@
 //     stream of 128-key K/V tiles, visited in descending order so that the
 //     masked tiles (sequence tail, causal diagonal) come first
 //     ("FlashAttention-3 on Hopper", sec. 4.7).
+//   * 384 threads; warpgroup 2 (warps 8-11) gives registers to the two
+//     softmax warpgroups with setmaxnreg.  Warps 10-11 are spare.
 //   * Warp 8 (one lane) is the TMA producer: Q_L/Q_H once per unit, then
 //     K_j and V_j into a ring of shared-memory stages guarded by full/empty
 //     mbarriers ("FlashAttention-3 on Hopper", sec. 4.3.1).
@@ -59,18 +61,32 @@ struct FwdCfg {
     static constexpr uint32_t CHUNK_BYTES = 128u * 128u;  // 128 rows x 128 B
     static constexpr uint32_t TILE_BYTES = NCH * CHUNK_BYTES;
     static constexpr int NSTAGE = (D == 64) ? 8 : 5;
-    static constexpr int NTHREADS = 320;
+    // 12 warps: 0-7 softmax groups, 8 TMA producer, 9 MMA issuer, 10-11
+    // spare.  Launch budget 384 x 168 registers; warpgroup 2 shrinks to
+    // REGS_LOW so the two softmax warpgroups can grow to REGS_HIGH:
+    // 128*REGS_LOW + 256*REGS_HIGH <= 384*168.
+    static constexpr int NTHREADS = 384;
+    static constexpr uint32_t REGS_LOW = 96, REGS_HIGH = 200;
+    static_assert(128 * REGS_LOW + 256 * REGS_HIGH <= 384 * 168, "register budget");
 
     // shared memory map (offsets from a 1024-B aligned base)
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t KV_OFF = 2 * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
     // barrier indices
+    // P is published in two parts: keys [0, 96) on B_PFULL (PV k-steps 0-5)
+    // and keys [96, 128) on B_PFULL2 (k-steps 6-7), so the P V product of a
+    // tile starts while its last quarter of exponentials is computed.
     static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4,
                          B_KVEMPTY = 4 + NSTAGE, B_SFULL = 4 + 2 * NSTAGE,
-                         B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
+                         B_PFULL = B_SFULL + 2, B_PFULL2 = B_PFULL + 2,
+                         B_OFULL = B_PFULL2 + 2,
                          B_OEMPTY = B_OFULL + 2, B_MMADONE = B_OEMPTY + 2,
                          NBAR = B_MMADONE + 1;
+    // The split pays off where the softmax dominates (d = 64); at d = 128
+    // the extra store wait costs more than the earlier PV start gains.
+    static constexpr bool SPLIT_P = (D == 64);
+    static constexpr int PV_SPLIT = SPLIT_P ? 6 : 8;   // PV k-steps covered by B_PFULL
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;   // + align slack
 
@@ -119,7 +135,7 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
 }
 
 template <int D, bool kCausal, bool kBF16>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -146,6 +162,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_init(bar(C::B_QEMPTY + x), 1);
             mbar_init(bar(C::B_SFULL + x), 1);
             mbar_init(bar(C::B_PFULL + x), 4);
+            mbar_init(bar(C::B_PFULL2 + x), 4);
             mbar_init(bar(C::B_OFULL + x), 1);
             mbar_init(bar(C::B_OEMPTY + x), 4);
         }
@@ -161,7 +178,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
-    if (warp == 8) {
+    if (warp >= 8) {
+      // Warpgroup 2 gives up registers first; each branch below starts with
+      // its warpgroup's setmaxnreg so the register budget of every role is
+      // known on every path into it.
+      regs_shrink<C::REGS_LOW>();
+      if (warp == 8) {
         // =================== TMA producer (one lane) ===================
         if (lane == 0) {
             WaitCtx w{abort_flag, a.status, kRoleProducer};
@@ -240,16 +262,24 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                             if (t - 1 == t0x &&
                                 !mbar_wait_warp(bar(C::B_OEMPTY + x), (un & 1) ^ 1, w, 11)) return false;
                             if (!mbar_wait_warp(bar(C::B_PFULL + x), pph, w, 12)) return false;
-                            pph ^= 1;
                             tc_fence_after();
                             const uint64_t vd = smem_desc_sw128(base + C::KV_OFF + vslot * C::TILE_BYTES,
                                                                 C::CHUNK_BYTES, 1024u);
                             const uint32_t acc = (t - 1 > t0x) ? 1u : 0u;
 #pragma unroll
-                            for (int kk = 0; kk < C::BN / 16; ++kk)
+                            for (int kk = 0; kk < C::PV_SPLIT; ++kk)
                                 mma_ts_f16_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
                                                  vd + ((kk * 2048u) >> 4), C::IDESC_PV,
                                                  (acc | kk) ? 1u : 0u);
+                            if constexpr (C::SPLIT_P) {
+                                if (!mbar_wait_warp(bar(C::B_PFULL2 + x), pph, w, 15)) return false;
+                                tc_fence_after();
+#pragma unroll
+                                for (int kk = C::PV_SPLIT; kk < C::BN / 16; ++kk)
+                                    mma_ts_f16_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
+                                                     vd + ((kk * 2048u) >> 4), C::IDESC_PV, 1u);
+                            }
+                            pph ^= 1;
                             if (t == U.T) mma_commit_elect(bar(C::B_OFULL + x));
                         }
                         // ---- S_x = Q_x K_t^T ----
@@ -289,7 +319,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_wait_quiet(bar(C::B_MMADONE), 0, 500000000ull);
         }
         __syncwarp();
+      }
     } else {
+        regs_grow<C::REGS_HIGH>();
         // =================== softmax group x (warps 4x .. 4x+3) ===================
         const int x = warp >> 2;
         const int row = tid & 127;                       // TMEM lane == tile row
@@ -353,29 +385,33 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // ---- exponentials, P, both row sums ----
                 float2 e_a = make_float2(0.f, 0.f), e_b = e_a, r_a = e_a, r_b = e_a;
                 uint32_t p[64];
+#define FA_EXP4(c)                                                                     \
+    {                                                                                  \
+        const float2 x01 = __ffma2_rn(make_float2(sf[(c) + 0], sf[(c) + 1]), c2, nr2);  \
+        const float2 x23 = __ffma2_rn(make_float2(sf[(c) + 2], sf[(c) + 3]), c2, nr2);  \
+        const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));          \
+        const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));          \
+        const uint32_t pk0 = pack2<kBF16>(e01.x, e01.y);                               \
+        const uint32_t pk1 = pack2<kBF16>(e23.x, e23.y);                               \
+        p[(c) / 2] = pk0;                                                              \
+        p[(c) / 2 + 1] = pk1;                                                          \
+        e_a = __fadd2_rn(e_a, e01);                                                    \
+        e_b = __fadd2_rn(e_b, e23);                                                    \
+        add_pair<kBF16>(r_a.x, r_a.y, pk0);                                            \
+        add_pair<kBF16>(r_b.x, r_b.y, pk1);                                            \
+    }
+                constexpr int CA = C::SPLIT_P ? 96 : 128;   // columns of part A
 #pragma unroll
-                for (int c = 0; c < 128; c += 4) {
-                    const float2 x01 = __ffma2_rn(make_float2(sf[c + 0], sf[c + 1]), c2, nr2);
-                    const float2 x23 = __ffma2_rn(make_float2(sf[c + 2], sf[c + 3]), c2, nr2);
-                    const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
-                    const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
-                    const uint32_t pk0 = pack2<kBF16>(e01.x, e01.y);
-                    const uint32_t pk1 = pack2<kBF16>(e23.x, e23.y);
-                    p[c / 2] = pk0;
-                    p[c / 2 + 1] = pk1;
-                    float2 q01, q23;
-                    unpack2<kBF16>(pk0, q01.x, q01.y);
-                    unpack2<kBF16>(pk1, q23.x, q23.y);
-                    e_a = __fadd2_rn(e_a, e01);
-                    e_b = __fadd2_rn(e_b, e23);
-                    r_a = __fadd2_rn(r_a, q01);
-                    r_b = __fadd2_rn(r_b, q23);
+                for (int c = 0; c < CA; c += 4) FA_EXP4(c)
+                if constexpr (!C::SPLIT_P) {
+                    le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y));
+                    lr = lr * corr + ((r_a.x + r_a.y) + (r_b.x + r_b.y));
                 }
-                le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y));
-                lr = lr * corr + ((r_a.x + r_a.y) + (r_b.x + r_b.y));
                 tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-                tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
-                // ---- correction of O (its previous PV completed before S_FULL) ----
+                if constexpr (C::SPLIT_P) tmem_st16(tS + 32, &p[32]);
+                else tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                // ---- correction of O (its previous PV completed before S_FULL),
+                //      before the first part of P is published ----
                 if (__any_sync(0xffffffffu, need)) {
                     const float2 cc = make_float2(corr, corr);
 #pragma unroll 1
@@ -397,6 +433,18 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_PFULL + x));
+                if constexpr (C::SPLIT_P) {
+#pragma unroll
+                    for (int c = 96; c < 128; c += 4) FA_EXP4(c)
+                    tmem_st16(tS + 48, &p[48]);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_PFULL2 + x));
+                    le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y));
+                    lr = lr * corr + ((r_a.x + r_a.y) + (r_b.x + r_b.y));
+                }
+#undef FA_EXP4
                 r = rn;
             }
             if (!ok) break;
