@@ -72,15 +72,15 @@ fa_status get_device(DeviceInfo **out) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 4-D map over a [B][N][H][d] tensor of 2-byte elements: dims {d, H, N, B},
-// box {64, 1, 128, 1} (a 128-row x 128-byte tile), 128-byte swizzle, rows
+// box {64, 1, rows, 1} (a rows x 128-byte tile), 128-byte swizzle, rows
 // beyond N read as zero.
 fa_status encode_bshd(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int B,
-                      int H, int N, int d) {
+                      int H, int N, int d, cuuint32_t rows) {
     const cuuint64_t esz = 2;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
     cuuint64_t strides[3] = {esz * d, esz * d * H, esz * d * H * static_cast<cuuint64_t>(N)};
-    cuuint32_t box[4] = {64, 1, 128, 1};
+    cuuint32_t box[4] = {64, 1, rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, dt, 4, const_cast<void *>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -117,15 +117,17 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_MISALIGNED;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_MISALIGNED;
     // TMA: every global stride < 2^40 bytes; kernel indexing uses 64-bit
     // offsets, the unit counter is a 32-bit int.
     const uint64_t batch_stride = 2ull * d * H * static_cast<uint64_t>(N);
     if (batch_stride >= (1ull << 40)) return FA_ERR_TOO_LARGE;
+    // Work units: pairs of 128-row Q tiles for d <= 128, single Q tiles
+    // for d = 256 (whose O accumulator alone fills half of TMEM).
     const uint64_t n_qt = (static_cast<uint64_t>(N) + 127) / 128;
-    const uint64_t units = static_cast<uint64_t>(B) * H * ((n_qt + 1) / 2);
+    const uint64_t units = static_cast<uint64_t>(B) * H * (d == 256 ? n_qt : (n_qt + 1) / 2);
     if (units > 0x7fffffffull || static_cast<uint64_t>(B) * H * N > 0x7fffffffffffull)
         return FA_ERR_TOO_LARGE;
 
@@ -137,16 +139,17 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
     std::memset(&L, 0, sizeof(L));
     const CUtensorMapDataType dt =
         dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    if ((st = encode_bshd(&L.q, q, dt, B, H, N, d)) != FA_OK) return st;
-    if ((st = encode_bshd(&L.k, k, dt, B, H, N, d)) != FA_OK) return st;
-    if ((st = encode_bshd(&L.v, v, dt, B, H, N, d)) != FA_OK) return st;
+    const cuuint32_t kv_rows = d == 256 ? 64 : 128;     // key tile height
+    if ((st = encode_bshd(&L.q, q, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.k, k, dt, B, H, N, d, kv_rows)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.v, v, dt, B, H, N, d, kv_rows)) != FA_OK) return st;
     L.args.o = o;
     L.args.lse = lse;
     L.args.status = dev->status;
     L.args.B = B;
     L.args.H = H;
     L.args.N = N;
-    L.args.n_kv = static_cast<int>(n_qt);
+    L.args.n_kv = static_cast<int>(d == 256 ? (static_cast<uint64_t>(N) + 63) / 64 : n_qt);
     L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
     L.args.n_units = static_cast<int>(units);
     L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
@@ -155,7 +158,8 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
     L.causal = causal != 0;
     L.bf16 = dtype == FA_BF16;
 
-    cudaError_t e = (d == 64) ? fa::launch_fwd_d64(L) : fa::launch_fwd_d128(L);
+    cudaError_t e = (d == 64) ? fa::launch_fwd_d64(L)
+                    : (d == 128) ? fa::launch_fwd_d128(L) : fa::launch_fwd_d256(L);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa_fwd_1q_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -20,6 +21,7 @@ struct FwdLaunch {
 
 cudaError_t launch_fwd_d64(const FwdLaunch &L);
 cudaError_t launch_fwd_d128(const FwdLaunch &L);
+cudaError_t launch_fwd_d256(const FwdLaunch &L);   // K/V maps with 64-row boxes
 
 // Shared helper: set the dynamic shared-memory limit once per device, then
 // launch one instantiation.
@@ -28,6 +30,26 @@ cudaError_t launch_fwd_inst(const FwdLaunch &L) {
     using Cfg = FwdCfg<D, kCausal, kBF16>;
     auto kern = fa_fwd_kernel<D, kCausal, kBF16>;
     static unsigned long long configured = 0ull;   // bit per device id (< 64)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(Cfg::SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured, bit, __ATOMIC_ACQ_REL);
+    }
+    kern<<<L.grid, Cfg::NTHREADS, Cfg::SMEM_BYTES, L.stream>>>(L.q, L.k, L.v, L.args);
+    return cudaGetLastError();
+}
+
+// Same, for the one-Q-tile schedule used at head dim 256.
+template <int D, bool kCausal, bool kBF16>
+cudaError_t launch_fwd_1q_inst(const FwdLaunch &L) {
+    using Cfg = Fwd1qCfg<D, kCausal, kBF16>;
+    auto kern = fa_fwd_1q_kernel<D, kCausal, kBF16>;
+    static unsigned long long configured = 0ull;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

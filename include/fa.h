@@ -64,8 +64,8 @@ typedef enum {
  *   q, k, v : device, [B][N][H][d] in `dtype`, 16-byte aligned.
  *   o       : device, [B][N][H][d] in `dtype`, 16-byte aligned (written).
  *   lse     : device, float [B][H][N], 4-byte aligned, or NULL to skip.
- *   B, H, N : >= 1.  d in {64, 128} (256 returns FA_ERR_UNSUPPORTED until
- *             its kernel exists).
+ *   B, H, N : >= 1.  d in {64, 128, 256}; other head dims return
+ *             FA_ERR_UNSUPPORTED.
  *   alpha   : the score scale (usually 1/sqrt(d)); must be finite.
  *   causal  : 0 or 1.
  * Accumulation is FP32; P is rounded to `dtype` before the P V product and

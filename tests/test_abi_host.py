@@ -76,6 +76,7 @@ def _call(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=1, N=128, d=64, alpha=0.125,
     (dict(dtype=7), fa.FA_ERR_INVALID_ARG),
     (dict(d=32), fa.FA_ERR_UNSUPPORTED),
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
     (dict(q=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(o=A + 2), fa.FA_ERR_MISALIGNED),
     (dict(lse=A + 2), fa.FA_ERR_MISALIGNED),

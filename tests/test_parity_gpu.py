@@ -70,6 +70,13 @@ FULL_CASES = [
     (1, 2, 513, 128, False, "fp16"),
     (1, 2, 513, 128, True, "fp16"),
     (1, 1, 640, 64, True, "fp16"),
+    (1, 1, 1, 256, True, "bf16"),          # head dim 256: one Q tile per unit
+    (1, 1, 64, 256, False, "bf16"),
+    (2, 1, 129, 256, True, "bf16"),
+    (1, 2, 300, 256, False, "bf16"),
+    (1, 2, 300, 256, True, "bf16"),
+    (1, 2, 513, 256, False, "fp16"),
+    (2, 2, 1000, 256, True, "bf16"),
 ]
 
 
@@ -104,7 +111,7 @@ def test_sampled_b4_h16_n4096_d128(gpu_lib):
 
 
 SWEEP = [(n, d, h, c) for n in (512, 1024, 2048, 4096, 8192, 16384)
-         for (d, h) in ((64, 32), (128, 16)) for c in (False, True)]
+         for (d, h) in ((64, 32), (128, 16), (256, 8)) for c in (False, True)]
 
 
 @pytest.mark.parametrize("N,d,H,causal", SWEEP)
@@ -112,14 +119,14 @@ def test_sampled_sequence_sweep(gpu_lib, N, d, H, causal):
     _sampled(gpu_lib, 16384 // N, H, N, d, causal, n_heads=2, n_rows=16)
 
 
-def test_head_dim_256_not_yet_supported(gpu_lib):
+def test_unsupported_head_dim_is_rejected(gpu_lib):
     fa = gpu_lib
-    x = torch.zeros((1, 128, 1, 256), dtype=torch.bfloat16, device="cuda")
-    rc = fa.fa_fwd(x, x, x, x, None, 1, 1, 128, 256, 0.0625, 0, fa.FA_BF16)
+    x = torch.zeros((1, 128, 1, 96), dtype=torch.bfloat16, device="cuda")
+    rc = fa.fa_fwd(x, x, x, x, None, 1, 1, 128, 96, 0.1, 0, fa.FA_BF16)
     assert rc == fa.FA_ERR_UNSUPPORTED
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_causal_row_zero_is_v0_exactly(gpu_lib, d):
     B, H, N = 2, 3, 700
     q, k, v = synth.qkv(B, H, N, d, seed=11)
