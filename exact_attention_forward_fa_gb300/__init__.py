@@ -29,8 +29,8 @@ FA_BF16 = 0
 FA_FP16 = 1
 
 # Every symbol include/fa.h declares (checked by the tests).
-EXPORTS = ("fa_fwd", "fa_check_status", "fa_status_detail", "fa_status_string",
-           "fa_version")
+EXPORTS = ("fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_check_status",
+           "fa_status_detail", "fa_status_string", "fa_version")
 
 _lib = None
 
@@ -54,6 +54,10 @@ def load():
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_quantize_fp8.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
+    lib.fa_quantize_fp8.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+    lib.fa_fwd_fp8.restype = i
     lib.fa_check_status.argtypes = [vp]
     lib.fa_check_status.restype = i
     lib.fa_status_detail.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -97,6 +101,52 @@ def fa_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, alpha: float,
     return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                          int(B), int(H), int(N), int(d), float(alpha),
                          int(causal), int(dtype), _stream(stream))
+
+
+def fa_quantize_fp8(x, x8, scales, hadamard_signs, B: int, H: int, N: int,
+                    d: int, stream=None) -> int:
+    """Direct call of the C entry point (see include/fa.h)."""
+    return load().fa_quantize_fp8(_ptr(x), _ptr(x8), _ptr(scales), _ptr(hadamard_signs),
+                                  int(B), int(H), int(N), int(d), _stream(stream))
+
+
+def fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B: int, H: int,
+               N: int, d: int, alpha: float, causal: int, stream=None) -> int:
+    """Direct call of the C entry point (see include/fa.h)."""
+    return load().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale),
+                             _ptr(v_scale), _ptr(o), _ptr(lse), int(B), int(H), int(N),
+                             int(d), float(alpha), int(causal), _stream(stream))
+
+
+def quantize_fp8(x, hadamard_signs=None, stream=None):
+    """bf16 [B,N,H,d] on the GPU -> (uint8 e4m3 codes, float scales [B,H,ceil(N/128)])."""
+    import torch
+    B, N, H, d = x.shape
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    sc = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=x.device)
+    rc = fa_quantize_fp8(x, x8, sc, hadamard_signs, B, H, N, d, stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_quantize_fp8")
+    return x8, sc
+
+
+def attention_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False,
+                  alpha: float | None = None, out=None, lse=None, want_lse: bool = True,
+                  stream=None):
+    """FP8 forward on quantized inputs; returns (O bf16, LSE or None)."""
+    import torch
+    B, N, H, d = q8.shape
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
+    rc = fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, out, lse, B, H, N, d, alpha,
+                    int(bool(causal)), stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_fp8")
+    return out, lse
 
 
 def fa_check_status(stream=None) -> int:

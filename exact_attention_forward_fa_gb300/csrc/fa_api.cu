@@ -71,16 +71,16 @@ fa_status get_device(DeviceInfo **out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 4-D map over a [B][N][H][d] tensor of 2-byte elements: dims {d, H, N, B},
-// box {64, 1, rows, 1} (a rows x 128-byte tile), 128-byte swizzle, rows
-// beyond N read as zero.
+// 4-D map over a [B][N][H][d] tensor: dims {d, H, N, B}, box {128 B of the
+// row, 1, rows, 1}, 128-byte swizzle, rows beyond N read as zero.  2-byte
+// elements (bf16/fp16) or 1-byte e4m3 codes.
 fa_status encode_bshd(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int B,
                       int H, int N, int d, cuuint32_t rows) {
-    const cuuint64_t esz = 2;
+    const cuuint64_t esz = dt == CU_TENSOR_MAP_DATA_TYPE_UINT8 ? 1 : 2;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
     cuuint64_t strides[3] = {esz * d, esz * d * H, esz * d * H * static_cast<cuuint64_t>(N)};
-    cuuint32_t box[4] = {64, 1, rows, 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / esz), 1, rows, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(m, dt, 4, const_cast<void *>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -160,6 +160,78 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
 
     cudaError_t e = (d == 64) ? fa::launch_fwd_d64(L)
                     : (d == 128) ? fa::launch_fwd_d128(L) : fa::launch_fwd_d256(L);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
+                          const float *hadamard_signs, int B, int H, int N, int d,
+                          void *stream) {
+    if (!x || !x8 || !scales) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(x8)) return FA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(scales) & 3u) ||
+        (reinterpret_cast<uintptr_t>(hadamard_signs) & 3u))
+        return FA_ERR_MISALIGNED;
+    const uint64_t n_tiles = (static_cast<uint64_t>(N) + 127) / 128;
+    if (static_cast<uint64_t>(B) * H * n_tiles > 0x7fffffffull ||
+        static_cast<uint64_t>(B) * H * N > 0x7fffffffffffull)
+        return FA_ERR_TOO_LARGE;
+    DeviceInfo *dev = nullptr;
+    fa_status st = get_device(&dev);
+    if (st != FA_OK) return st;
+    cudaError_t e = fa::launch_quantize(x, x8, scales, hadamard_signs, B, H, N, d,
+                                        static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                     const float *q_scale, const float *k_scale, const float *v_scale,
+                     void *o, float *lse, int B, int H, int N, int d, float alpha,
+                     int causal, void *stream) {
+    if (!q8 || !k8 || !v8 || !q_scale || !k_scale || !v_scale || !o) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
+    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o)) return FA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(q_scale) & 3u) || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
+        (reinterpret_cast<uintptr_t>(v_scale) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+        return FA_ERR_MISALIGNED;
+    const uint64_t batch_stride = 1ull * d * H * static_cast<uint64_t>(N);
+    if (batch_stride >= (1ull << 40)) return FA_ERR_TOO_LARGE;
+    const uint64_t n_qt = (static_cast<uint64_t>(N) + 127) / 128;
+    const uint64_t units = static_cast<uint64_t>(B) * H * ((n_qt + 1) / 2);
+    if (units > 0x7fffffffull || static_cast<uint64_t>(B) * H * N > 0x7fffffffffffull)
+        return FA_ERR_TOO_LARGE;
+    DeviceInfo *dev = nullptr;
+    fa_status st = get_device(&dev);
+    if (st != FA_OK) return st;
+
+    fa::FwdLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if ((st = encode_bshd(&L.q, q8, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.k, k8, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.v, v8, dt, B, H, N, d, 128)) != FA_OK) return st;
+    L.args.o = o;
+    L.args.lse = lse;
+    L.args.status = dev->status;
+    L.args.B = B;
+    L.args.H = H;
+    L.args.N = N;
+    L.args.n_kv = static_cast<int>(n_qt);
+    L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
+    L.args.n_units = static_cast<int>(units);
+    L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
+    L.args.q_scale = q_scale;
+    L.args.k_scale = k_scale;
+    L.args.v_scale = v_scale;
+    L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.causal = causal != 0;
+    L.bf16 = true;
+    cudaError_t e = fa::launch_fwd_fp8(L);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -1,14 +1,17 @@
-// fa_fwd_1q_kernel.cuh -- exact attention forward for head dim 256 on sm_103a.
+// fa_fwd_1q_kernel.cuh -- exact attention forward, one Q tile per work unit
+// (used for head dim 256) on sm_103a.
 //
 // Same operation as fa_fwd_kernel.cuh ("FlashAttention-3 on Hopper",
 // sec. 4.1-4.7: online softmax over key tiles, LSE in natural-log units,
 // bottom-right causal predicate), scheduled for d = 256 where the output
 // accumulator alone is 256 TMEM columns per 128-row Q tile:
-//   * one 128-row Q tile per work unit, 64-key K/V tiles;
-//   * TMEM (512 columns): S0 [0,64), S1 [64,128) double-buffered scores (P
-//     overlays the first 32 columns of its S buffer), Q [128,256) as the A
-//     operand of S = Q K^T (TS form, so Q is not re-read from shared memory
-//     for every key tile), O [256,512);
+//   * one 128-row Q tile per work unit, BN-key K/V tiles (BN = 64 at d = 256,
+//     128 otherwise; measured slower than the two-tile kernel at d <= 128,
+//     where one softmax warpgroup cannot keep up with the tensor core);
+//   * TMEM (512 columns): S0 [0,BN), S1 [BN,2BN) double-buffered scores (P
+//     overlays the first BN/2 columns of its S buffer), Q [2BN, 2BN+d/2) as
+//     the A operand of S = Q K^T (TS form, so Q is not re-read from shared
+//     memory for every key tile), O after it (at d = 256: [256,512));
 //   * shared memory: a 64 KB Q staging tile (TMA, 128-byte swizzle) that the
 //     softmax threads copy into TMEM, and a 5-stage ring of 32 KB K/V tiles;
 //   * MMA order QK(t), PV(t-1): the score tile of step t+1 is computed while
@@ -28,14 +31,15 @@ namespace fa {
 
 template <int D, bool kCausal, bool kBF16>
 struct Fwd1qCfg {
-    static_assert(D == 256, "this schedule is for head dim 256");
-    static constexpr int BM = 128, BN = 64;
+    static_assert(D == 64 || D == 128 || D == 256, "head dim");
+    static constexpr int BM = 128;
+    static constexpr int BN = (D == 256) ? 64 : 128;           // keys per tile
     static constexpr int NCH = D / 64;                          // 128-B column chunks
     static constexpr uint32_t Q_CHUNK = 128u * 128u;            // 128 rows x 128 B
-    static constexpr uint32_t KV_CHUNK = 64u * 128u;            // 64 rows x 128 B
-    static constexpr uint32_t Q_BYTES = NCH * Q_CHUNK;          // 64 KB
-    static constexpr uint32_t KV_BYTES = NCH * KV_CHUNK;        // 32 KB
-    static constexpr int NSTAGE = 5;
+    static constexpr uint32_t KV_CHUNK = BN * 128u;             // BN rows x 128 B
+    static constexpr uint32_t Q_BYTES = NCH * Q_CHUNK;
+    static constexpr uint32_t KV_BYTES = NCH * KV_CHUNK;
+    static constexpr int NSTAGE = (D == 256) ? 5 : (D == 128) ? 6 : 8;
     static constexpr int NTHREADS = 192;
 
     static constexpr uint32_t QS_OFF = 0;
@@ -49,22 +53,24 @@ struct Fwd1qCfg {
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;
 
+    // TMEM: S0 [0,BN), S1 [BN,2BN), Q [2BN, 2BN + D/2), O [.., + D)
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_Q = 128, COL_O = 256;
-    __host__ __device__ static constexpr uint32_t col_s(int b) { return b ? 64u : 0u; }
+    static constexpr uint32_t COL_Q = 2 * BN, COL_O = 2 * BN + D / 2;
+    static_assert(COL_O + D <= TMEM_COLS, "TMEM budget");
+    __host__ __device__ static constexpr uint32_t col_s(int b) { return b ? BN : 0u; }
 
     static constexpr uint32_t IDESC_QK = idesc_f16(128, BN, kBF16, false, false);
     static constexpr uint32_t IDESC_PV = idesc_f16(128, D, kBF16, false, true);
     static constexpr float TAU = 8.0f;
 };
 
-// Work unit: one 128-row Q tile of one (b, h); keys in 64-wide tiles visited
+// Work unit: one 128-row Q tile of one (b, h); keys in BN-wide tiles visited
 // in descending order from T-1 to 0.
 struct Unit1q {
     int b, h, m, T;
 };
 
-template <bool kCausal>
+template <bool kCausal, int BN>
 __device__ __forceinline__ Unit1q make_unit_1q(int u, const FwdArgs &a) {
     Unit1q U;
     const int BH = a.B * a.H;
@@ -79,8 +85,8 @@ __device__ __forceinline__ Unit1q make_unit_1q(int u, const FwdArgs &a) {
     }
     U.b = bh / a.H;
     U.h = bh % a.H;
-    // a.n_kv counts 64-key tiles here
-    U.T = kCausal ? min(a.n_kv, 2 * U.m + 2) : a.n_kv;
+    // a.n_kv counts BN-key tiles; the diagonal tile holds key m*128 + 127
+    U.T = kCausal ? min(a.n_kv, (U.m * 128 + 127) / BN + 1) : a.n_kv;
     return U;
 }
 
@@ -143,14 +149,14 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
                     tma_load_4d(tm, base + C::KV_OFF + slot * C::KV_BYTES + c * C::KV_CHUNK,
-                                bar(C::B_KVFULL + slot), c * 64, U.h, j * 64, U.b);
+                                bar(C::B_KVFULL + slot), c * 64, U.h, j * C::BN, U.b);
                 armed |= 1u << slot;
                 armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
                 if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
                 return true;
             };
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-                const Unit1q U = make_unit_1q<kCausal>(u, a);
+                const Unit1q U = make_unit_1q<kCausal, C::BN>(u, a);
                 ok = mbar_wait(bar(C::B_QSEMPTY), (qn & 1) ^ 1, w, 1);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(C::B_QSFULL), C::Q_BYTES);
@@ -186,7 +192,7 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
         };
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-            const Unit1q U = make_unit_1q<kCausal>(u, a);
+            const Unit1q U = make_unit_1q<kCausal, C::BN>(u, a);
             ok = mbar_wait_warp(bar(C::B_QTFULL), qtph, w, 30);
             if (!ok) break;
             qtph ^= 1;
@@ -289,7 +295,7 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
         };
 
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-            const Unit1q U = make_unit_1q<kCausal>(u, a);
+            const Unit1q U = make_unit_1q<kCausal, C::BN>(u, a);
             // ---- copy Q (staged by TMA, 128-B swizzle) into TMEM; the last
             //      QK of the previous unit completed before its S_FULL ----
             ok = mbar_wait(bar(C::B_QSFULL), qsph, w, 40);
@@ -332,22 +338,24 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (sb) sph1 ^= 1; else sph0 ^= 1;
                 tc_fence_after();
                 const uint32_t tS = tbase + lane_off + C::col_s(sb);
-                uint32_t s[64];
-                tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-                tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                constexpr int BN = C::BN;
+                uint32_t s[BN];
+#pragma unroll
+                for (int c = 0; c < BN; c += 32)
+                    tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&s[c]));
                 tmem_ld_wait();
                 float *sf = reinterpret_cast<float *>(s);
-                // ---- masks: sequence tail and causal diagonal (64-key tiles) ----
-                int lim = 64;
-                if (j == a.n_kv - 1) lim = min(lim, a.N - j * 64);
-                if (kCausal) lim = min(lim, U.m * 128 + row - j * 64 + 1);
-                if (lim < 64) {
+                // ---- masks: sequence tail and causal diagonal ----
+                int lim = BN;
+                if (j == a.n_kv - 1) lim = min(lim, a.N - j * BN);
+                if (kCausal) lim = min(lim, U.m * 128 + row - j * BN + 1);
+                if (lim < BN) {
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) if (c >= lim) sf[c] = -INFINITY;
+                    for (int c = 0; c < BN; ++c) if (c >= lim) sf[c] = -INFINITY;
                 }
                 float m0 = sf[0], m1 = sf[1], m2 = sf[2], m3 = sf[3];
 #pragma unroll
-                for (int c = 4; c < 64; c += 8) {
+                for (int c = 4; c < BN; c += 8) {
                     m0 = max3(m0, sf[c + 0], sf[c + 4]);
                     m1 = max3(m1, sf[c + 1], sf[c + 5]);
                     m2 = max3(m2, sf[c + 2], sf[c + 6]);
@@ -362,9 +370,9 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const float rs = (rn == -INFINITY) ? 0.f : rn;
                 const float2 nr2 = make_float2(-rs, -rs);
                 float2 e_a = make_float2(0.f, 0.f), e_b = e_a, r_a = e_a, r_b = e_a;
-                uint32_t p[32];
+                uint32_t p[BN / 2];
 #pragma unroll
-                for (int c = 0; c < 64; c += 4) {
+                for (int c = 0; c < BN; c += 4) {
                     const float2 x01 = __ffma2_rn(make_float2(sf[c + 0], sf[c + 1]), c2, nr2);
                     const float2 x23 = __ffma2_rn(make_float2(sf[c + 2], sf[c + 3]), c2, nr2);
                     const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
@@ -380,7 +388,9 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
                 le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y));
                 lr = lr * corr + ((r_a.x + r_a.y) + (r_b.x + r_b.y));
-                tmem_st32(tS + 0, p);
+#pragma unroll
+                for (int c = 0; c < BN / 2; c += 32)
+                    tmem_st32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&p[c]));
                 // ---- the previous PV must be complete before O is rescaled
                 //      and before this tile's P is published (one wait per PV) ----
                 if (t > 0) {

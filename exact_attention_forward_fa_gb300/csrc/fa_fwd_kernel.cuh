@@ -50,17 +50,27 @@ struct FwdArgs {
     int n_pairs;         // ceil(ceil(N / 128) / 2) Q-tile pairs per head
     int n_units;         // B * H * n_pairs
     float scale_log2;    // alpha * log2(e)
+    // FP8 only: one FP32 scale per 128-row tile of each head, [B][H][n_kv]
+    const float *q_scale, *k_scale, *v_scale;
 };
 
-template <int D, bool kCausal, bool kBF16>
+// kFP8: Q/K/V are e4m3 codes with per-tile scales (kind::f8f6f4 MMAs), O is
+// bf16.  Otherwise Q/K/V/O are bf16 (kBF16) or fp16.
+template <int D, bool kCausal, bool kBF16, bool kFP8 = false>
 struct FwdCfg {
     static_assert(D == 64 || D == 128, "head dim");
+    static_assert(!kFP8 || (D == 128 && kBF16), "FP8 path: d = 128, bf16 output");
+    static constexpr int ESZ = kFP8 ? 1 : 2;            // bytes per Q/K/V element
     static constexpr int BM = 128;                      // query rows per tile
     static constexpr int BN = 128;                      // keys per tile
-    static constexpr int NCH = D / 64;                  // 128-byte column chunks
+    static constexpr int NCH = D * ESZ / 128;           // 128-byte column chunks
     static constexpr uint32_t CHUNK_BYTES = 128u * 128u;  // 128 rows x 128 B
     static constexpr uint32_t TILE_BYTES = NCH * CHUNK_BYTES;
-    static constexpr int NSTAGE = (D == 64) ? 8 : 5;
+    static constexpr int NSTAGE = (kFP8 || D == 64) ? 8 : 5;
+    static constexpr int QK_STEPS = D * ESZ / 32;       // 32 bytes of K per MMA
+    static constexpr int PV_KEYS = 32 / ESZ;            // keys per PV MMA
+    static constexpr int PV_STEPS = BN / PV_KEYS;
+    static constexpr int P_COLS = BN * ESZ / 4;         // TMEM columns of P
     // 12 warps: 0-7 softmax groups, 8 TMA producer, 9 MMA issuer, 10-11
     // spare.  Launch budget 384 x 168 registers; warpgroup 2 shrinks to
     // REGS_LOW so the two softmax warpgroups can grow to REGS_HIGH:
@@ -85,8 +95,8 @@ struct FwdCfg {
                          NBAR = B_MMADONE + 1;
     // The split pays off where the softmax dominates (d = 64); at d = 128
     // the extra store wait costs more than the earlier PV start gains.
-    static constexpr bool SPLIT_P = (D == 64);
-    static constexpr int PV_SPLIT = SPLIT_P ? 6 : 8;   // PV k-steps covered by B_PFULL
+    static constexpr bool SPLIT_P = (D == 64) && !kFP8;
+    static constexpr int PV_SPLIT = SPLIT_P ? 6 : PV_STEPS;   // PV k-steps covered by B_PFULL
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;   // + align slack
 
@@ -95,9 +105,16 @@ struct FwdCfg {
     __host__ __device__ static constexpr uint32_t col_s(int x) { return x ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t col_o(int x) { return 256u + (x ? D : 0u); }
 
-    static constexpr uint32_t IDESC_QK = idesc_f16(128, 128, kBF16, false, false);
-    static constexpr uint32_t IDESC_PV = idesc_f16(128, D, kBF16, false, true);
-    static constexpr float TAU = 8.0f;
+    static constexpr uint32_t IDESC_QK =
+        kFP8 ? idesc_e4m3(128, 128, false, false) : idesc_f16(128, 128, kBF16, false, false);
+    static constexpr uint32_t IDESC_PV =
+        kFP8 ? idesc_e4m3(128, D, false, true) : idesc_f16(128, D, kBF16, false, true);
+    // Conditional-rescale threshold (log2 units).  16-bit P: tau = 8, so
+    // P <= 2^8.  FP8 P ("03 FA3", sec. 4, Max_offset = 8): the exponent is
+    // shifted by +8 to use the e4m3 range and tau = 0.8 keeps
+    // P <= 2^8.8 < 448, the largest e4m3 value.
+    static constexpr float TAU = kFP8 ? 0.8f : 8.0f;
+    static constexpr float P_OFFSET = kFP8 ? 8.0f : 0.0f;
 };
 
 // The geometry of one work unit, identical in every role.
@@ -134,12 +151,12 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     return U;
 }
 
-template <int D, bool kCausal, bool kBF16>
+template <int D, bool kCausal, bool kBF16, bool kFP8 = false>
 __global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
-    using C = FwdCfg<D, kCausal, kBF16>;
+    using C = FwdCfg<D, kCausal, kBF16, kFP8>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -201,7 +218,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
                     tma_load_4d(&tm_q, base + C::Q_OFF + x * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                bar(C::B_QFULL + x), c * 64, U.h, U.m[x] * 128, U.b);
+                                bar(C::B_QFULL + x), c * (128 / C::ESZ), U.h, U.m[x] * 128, U.b);
                 ++qn;
                 return true;
             };
@@ -218,7 +235,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const CUtensorMap *tm = kv ? &tm_v : &tm_k;
                         for (int c = 0; c < C::NCH; ++c)
                             tma_load_4d(tm, base + C::KV_OFF + slot * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                        bar(C::B_KVFULL + slot), c * 64, U.h, j * 128, U.b);
+                                        bar(C::B_KVFULL + slot), c * (128 / C::ESZ), U.h, j * 128, U.b);
                         armed |= 1u << slot;
                         armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
                         if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
@@ -267,17 +284,22 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                 C::CHUNK_BYTES, 1024u);
                             const uint32_t acc = (t - 1 > t0x) ? 1u : 0u;
 #pragma unroll
-                            for (int kk = 0; kk < C::PV_SPLIT; ++kk)
-                                mma_ts_f16_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
-                                                 vd + ((kk * 2048u) >> 4), C::IDESC_PV,
-                                                 (acc | kk) ? 1u : 0u);
+                            for (int kk = 0; kk < C::PV_SPLIT; ++kk) {
+                                const uint64_t bd = vd + ((kk * C::PV_KEYS * 128u) >> 4);
+                                if constexpr (kFP8)
+                                    mma_ts_f8_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
+                                                    bd, C::IDESC_PV, (acc | kk) ? 1u : 0u);
+                                else
+                                    mma_ts_f16_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
+                                                     bd, C::IDESC_PV, (acc | kk) ? 1u : 0u);
+                            }
                             if constexpr (C::SPLIT_P) {
                                 if (!mbar_wait_warp(bar(C::B_PFULL2 + x), pph, w, 15)) return false;
                                 tc_fence_after();
 #pragma unroll
-                                for (int kk = C::PV_SPLIT; kk < C::BN / 16; ++kk)
+                                for (int kk = C::PV_SPLIT; kk < C::PV_STEPS; ++kk)
                                     mma_ts_f16_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
-                                                     vd + ((kk * 2048u) >> 4), C::IDESC_PV, 1u);
+                                                     vd + ((kk * C::PV_KEYS * 128u) >> 4), C::IDESC_PV, 1u);
                             }
                             pph ^= 1;
                             if (t == U.T) mma_commit_elect(bar(C::B_OFULL + x));
@@ -296,10 +318,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const uint64_t qd = smem_desc_sw128(base + C::Q_OFF + x * C::TILE_BYTES, 16u, 1024u);
                             const uint64_t kd = smem_desc_sw128(base + C::KV_OFF + kslot * C::TILE_BYTES, 16u, 1024u);
 #pragma unroll
-                            for (int kk = 0; kk < D / 16; ++kk) {
+                            for (int kk = 0; kk < C::QK_STEPS; ++kk) {
                                 const uint32_t off = ((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32u) >> 4;
-                                mma_ss_f16_elect(tbase + C::col_s(x), qd + off, kd + off, C::IDESC_QK,
-                                                 kk > 0 ? 1u : 0u);
+                                if constexpr (kFP8)
+                                    mma_ss_f8_elect(tbase + C::col_s(x), qd + off, kd + off,
+                                                    C::IDESC_QK, kk > 0 ? 1u : 0u);
+                                else
+                                    mma_ss_f16_elect(tbase + C::col_s(x), qd + off, kd + off,
+                                                     C::IDESC_QK, kk > 0 ? 1u : 0u);
                             }
                             mma_commit_elect(bar(C::B_SFULL + x));
                             if (t == U.T - 1) mma_commit_elect(bar(C::B_QEMPTY + x));
@@ -339,9 +365,21 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (!act) continue;
             const int mt = x ? U.m[1] : U.m[0];
             const int t0 = x ? U.t0[1] : U.t0[0];
+            // FP8: the Q tile's scale and the largest V scale of the head
+            // (the per-tile V scales are folded into P relative to it).
+            const size_t sbase = (static_cast<size_t>(U.b) * a.H + U.h) * a.n_kv;
+            float qs = 1.f, vmax = 1.f;
+            if constexpr (kFP8) {
+                qs = a.q_scale[sbase + mt];
+                float vm = 0.f;
+                for (int jj = lane; jj < a.n_kv; jj += 32) vm = fmaxf(vm, a.v_scale[sbase + jj]);
+#pragma unroll
+                for (int m = 16; m > 0; m >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, m));
+                vmax = vm;
+            }
             // r: reference point (scaled log2 units); le: row sum of the FP32
             // exponentials (for LSE); lr: row sum of the same values rounded
-            // as the P V product sees them (normalises O).
+            // as the P V product sees them (normalises O; 16-bit P only).
             float r = -INFINITY, le = 0.f, lr = 0.f;
             for (int t = t0; t < U.T; ++t) {
                 const int j = U.T - 1 - t;
@@ -374,17 +412,43 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     m3 = max3(m3, sf[c + 3], sf[c + 7]);
                 }
                 const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-                const float bnew = mx * sl2;                    // -inf stays -inf
+                // Score scale to log2 units; FP8 adds the q and k tile scales
+                // ("FlashAttention-3 on Hopper", sec. 6.3) and the exponent
+                // offset 8 + log2(v_j / v_max) (P carries the V tile scale).
+                float sc = sl2, voff = 0.f, vratio = 1.f;
+                if constexpr (kFP8) {
+                    sc = sl2 * qs * a.k_scale[sbase + j];
+                    vratio = a.v_scale[sbase + j] / vmax;
+                    voff = C::P_OFFSET + log2f(vratio);
+                }
+                const float bnew = mx * sc;                     // -inf stays -inf
                 // ---- conditional rescale: move r only if the max grew by > tau ----
                 float rn, corr;
                 if (r == -INFINITY) { rn = bnew; corr = 1.f; }
                 else { rn = (bnew > r + C::TAU) ? bnew : r; corr = ex2_approx(r - rn); }
                 const bool need = (r != -INFINITY) && (rn != r);
                 const float rs = (rn == -INFINITY) ? 0.f : rn;
-                const float2 nr2 = make_float2(-rs, -rs);
-                // ---- exponentials, P, both row sums ----
+                const float2 c2 = make_float2(sc, sc);
+                const float2 nr2 = make_float2(voff - rs, voff - rs);
                 float2 e_a = make_float2(0.f, 0.f), e_b = e_a, r_a = e_a, r_b = e_a;
-                uint32_t p[64];
+                uint32_t p[kFP8 ? 32 : 64];
+                if constexpr (kFP8) {
+                    // ---- FP8: P' = 2^(x - r + 8) (v_j / v_max) as e4m3 ----
+#pragma unroll
+                    for (int c = 0; c < 128; c += 4) {
+                        const float2 x01 = __ffma2_rn(make_float2(sf[c + 0], sf[c + 1]), c2, nr2);
+                        const float2 x23 = __ffma2_rn(make_float2(sf[c + 2], sf[c + 3]), c2, nr2);
+                        const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+                        const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+                        p[c / 4] = pack4_e4m3(e01.x, e01.y, e23.x, e23.y);
+                        e_a = __fadd2_rn(e_a, e01);
+                        e_b = __fadd2_rn(e_b, e23);
+                    }
+                    // the row sum counts 2^(x - r + 8) without the V factor
+                    le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y)) / vratio;
+                    tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+                } else {
+                // ---- 16-bit P: exponentials, P, both row sums ----
 #define FA_EXP4(c)                                                                     \
     {                                                                                  \
         const float2 x01 = __ffma2_rn(make_float2(sf[(c) + 0], sf[(c) + 1]), c2, nr2);  \
@@ -410,6 +474,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
                 if constexpr (C::SPLIT_P) tmem_st16(tS + 32, &p[32]);
                 else tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
+                }
                 // ---- correction of O (its previous PV completed before S_FULL),
                 //      before the first part of P is published ----
                 if (__any_sync(0xffffffffu, need)) {
@@ -453,8 +518,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
             oph ^= 1;
             tc_fence_after();
-            const bool live = (le > 0.f) && (lr > 0.f);
-            const float inv = live ? 1.f / lr : 0.f;
+            // 16-bit P: O / l_r.  FP8: O v_max / l (O accumulated P' = P v_j/v_max).
+            const bool live = (le > 0.f) && (kFP8 || lr > 0.f);
+            const float inv = live ? (kFP8 ? vmax / le : 1.f / lr) : 0.f;
             const int grow = mt * 128 + row;
             uint16_t *orow = reinterpret_cast<uint16_t *>(a.o) +
                              ((static_cast<size_t>(U.b) * a.N + grow) * a.H + U.h) * D;
@@ -479,7 +545,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + x));
             if (a.lse != nullptr && grow < a.N) {
-                const float lse = live ? (r + log2f(le)) * 0.69314718055994530942f : -INFINITY;
+                const float lse = live ? (r - C::P_OFFSET + log2f(le)) * 0.69314718055994530942f
+                                       : -INFINITY;
                 a.lse[(static_cast<size_t>(U.b) * a.H + U.h) * a.N + grow] = lse;
             }
         }

@@ -22,13 +22,16 @@ struct FwdLaunch {
 cudaError_t launch_fwd_d64(const FwdLaunch &L);
 cudaError_t launch_fwd_d128(const FwdLaunch &L);
 cudaError_t launch_fwd_d256(const FwdLaunch &L);   // K/V maps with 64-row boxes
+cudaError_t launch_fwd_fp8(const FwdLaunch &L);    // e4m3 maps, 128-byte boxes
+cudaError_t launch_quantize(const void *x, void *x8, float *scales, const float *signs,
+                            int B, int H, int N, int d, cudaStream_t stream);
 
 // Shared helper: set the dynamic shared-memory limit once per device, then
 // launch one instantiation.
-template <int D, bool kCausal, bool kBF16>
+template <int D, bool kCausal, bool kBF16, bool kFP8 = false>
 cudaError_t launch_fwd_inst(const FwdLaunch &L) {
-    using Cfg = FwdCfg<D, kCausal, kBF16>;
-    auto kern = fa_fwd_kernel<D, kCausal, kBF16>;
+    using Cfg = FwdCfg<D, kCausal, kBF16, kFP8>;
+    auto kern = fa_fwd_kernel<D, kCausal, kBF16, kFP8>;
     static unsigned long long configured = 0ull;   // bit per device id (< 64)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

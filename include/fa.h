@@ -77,6 +77,43 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
                  int causal, fa_dtype dtype, void *stream);
 
 /*
+ * fa_quantize_fp8 -- FP8 pre-pass: block quantization with optional
+ * incoherent processing ("FlashAttention-3 on Hopper", sec. 6.3 and 6.4).
+ *   x      : device, bf16 [B][N][H][d], 16-byte aligned.
+ *   x8     : device, uint8 e4m3 codes [B][N][H][d], 16-byte aligned (written).
+ *   scales : device, float [B][H][ceil(N/128)] (written): one scale per
+ *            128-row tile of a head, scale = amax / 448 over the (rotated)
+ *            tile, 1 for an all-zero tile.
+ *   hadamard_signs : device, float[d] of +-1, or NULL for no rotation.  With
+ *            it, each row is replaced by y = x (1/sqrt d) H D before
+ *            quantization (H: d x d Sylvester Hadamard matrix, D = diag of
+ *            the signs).  Use the same signs for Q and K, none for V: the
+ *            product (QM)(KM)^T equals Q K^T because M is orthogonal.
+ *   d in {64, 128, 256}.
+ * codes = e4m3(y / scale), round to nearest even, saturating at +-448.
+ */
+fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
+                          const float *hadamard_signs, int B, int H, int N, int d,
+                          void *stream);
+
+/*
+ * fa_fwd_fp8 -- attention forward on e4m3 Q/K/V with per-tile scales
+ * (as written by fa_quantize_fp8), bf16 output ("FlashAttention-3 on
+ * Hopper", sec. 6.3: descales folded into the softmax scale per tile
+ * pair; "03 FA3", sec. 4: exponent offset 8 for the FP8 probabilities).
+ *   q8, k8, v8 : device, uint8 e4m3 [B][N][H][d], 16-byte aligned.
+ *   q_scale, k_scale, v_scale : device, float [B][H][ceil(N/128)].
+ *   o   : device, bf16 [B][N][H][d] (written).  lse : as for fa_fwd.
+ *   d = 128 (others return FA_ERR_UNSUPPORTED).  alpha, causal as fa_fwd.
+ * P is rounded to e4m3 before the P V product with the V tile scale
+ * folded in; accumulation is FP32.
+ */
+fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                     const float *q_scale, const float *k_scale, const float *v_scale,
+                     void *o, float *lse, int B, int H, int N, int d, float alpha,
+                     int causal, void *stream);
+
+/*
  * fa_check_status -- synchronizes `stream`, then reports and clears the
  * device status word of the current device.  Returns FA_ERR_TIMEOUT if a
  * kernel launched since the last check gave up on a bounded wait (its

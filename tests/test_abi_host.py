@@ -86,6 +86,43 @@ def test_validation_codes(lib, kw, code):
     assert _call(lib, **kw) == code
 
 
+def _qcall(lib, x=A, x8=A, sc=A, signs=None, B=1, H=1, N=128, d=128):
+    return lib.fa_quantize_fp8(x, x8, sc, signs, B, H, N, d, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), fa.FA_ERR_INVALID_ARG),
+    (dict(x8=None), fa.FA_ERR_INVALID_ARG),
+    (dict(sc=None), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(x=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(sc=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(signs=A + 1), fa.FA_ERR_MISALIGNED),
+])
+def test_quantize_validation_codes(lib, kw, code):
+    assert _qcall(lib, **kw) == code
+
+
+def _f8call(lib, q=A, k=A, v=A, qs=A, ks=A, vs=A, o=A, lse=None, B=1, H=1, N=128, d=128,
+            alpha=0.088, causal=0):
+    return lib.fa_fwd_fp8(q, k, v, qs, ks, vs, o, lse, B, H, N, d, alpha, causal, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(vs=None), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=3), fa.FA_ERR_INVALID_ARG),
+    (dict(alpha=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(d=64), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(k=A + 4), fa.FA_ERR_MISALIGNED),
+    (dict(qs=A + 2), fa.FA_ERR_MISALIGNED),
+])
+def test_fp8_validation_codes(lib, kw, code):
+    assert _f8call(lib, **kw) == code
+
+
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     import torch
     if torch.cuda.is_available():

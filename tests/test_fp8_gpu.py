@@ -1,0 +1,164 @@
+"""GPU checks of the FP8 path: the quantization pre-pass against the
+oracle's block quantization, and the FP8 forward against FP64 attention.
+
+* Quantization ("FlashAttention-3 on Hopper", sec. 6.3-6.4): scales equal
+  amax/448 of the (rotated) tile -- exactly without rotation, to 2^-20
+  relative with it (the kernel's FP32 Walsh-Hadamard butterflies round);
+  codes equal the round-to-nearest e4m3 code of y/scale, except where y/scale
+  lies within 2^-18 of a rounding boundary, where either neighbour is valid.
+* FP8 forward on the outlier distribution (N(0,1) + 0.1% N(0,100)), the
+  metric of the FA3 numerical-error experiment: O RMSE against the FP64
+  oracle on the unquantized inputs <= 1.5e-2 with block scales and the
+  Hadamard rotation; the rotation lowers the error.
+* A bound derived from the arithmetic, against FP64 attention on the
+  dequantized (rotated) inputs, i.e. the operands the tensor core sees: the
+  kernel differs only by the e4m3 rounding of P (relative 2^-4 for normal
+  values, absolute 2^-10 below 2^-6, in units where the largest P of a row
+  is at most 448) and FP32 accumulation, so
+      |O_gpu - O_deq| <= (2^-4 + n_keys 2^-10 / (ratio_min 256)) max_j |v_j - O_deq|
+                        + 2^-8 |O_deq| + 1e-3.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_forward_fa_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+THREADS = os.cpu_count() or 4
+
+
+def _quant(fa, x, signs):
+    dev = torch.device("cuda")
+    s = None if signs is None else torch.from_numpy(signs).to(dev)
+    x8, sc = fa.quantize_fp8(x.to(dev), s)
+    assert fa.fa_check_status() == fa.FA_OK
+    return x8.cpu().numpy(), sc.cpu().numpy()
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("rotate", [False, True])
+def test_quantize_matches_oracle(gpu_lib, d, rotate):
+    B, H, N = 2, 3, 300
+    x = torch.from_numpy(synth.normal((B, N, H, d), seed=77 + d, outliers=True)).to(torch.bfloat16)
+    signs = synth.hadamard_signs(d, seed=5) if rotate else None
+    x8, sc = _quant(gpu_lib, x, signs)
+    for b in range(B):
+        for h in range(H):
+            xh = x[b, :, h, :].double().numpy()
+            y = oracle.hadamard_rotate(xh, signs) if rotate else xh
+            codes_ref, sc_ref = oracle.quantize_e4m3_tiles(y, 128)
+            rel = np.abs(sc[b, h] - sc_ref) / sc_ref
+            assert np.all(rel <= (2.0 ** -20 if rotate else 0.0)), rel.max()
+            got = x8[b, :, h, :]
+            scale_rows = np.repeat(sc[b, h], 128)[:N, None]          # float32
+            if not rotate:
+                # Same decision in the kernel's precision: the FP32 quotient
+                # x / scale, then round-to-nearest-even to e4m3 -> bit exact.
+                q32 = (xh.astype(np.float32) / scale_rows).astype(np.float64)
+                assert np.array_equal(got, oracle.e4m3_encode(q32))
+            else:
+                # The rotated values carry FP32 butterfly rounding: the code
+                # is the RNE code of y/scale, or a neighbour where y/scale
+                # lies within 2^-18 of a rounding boundary.
+                v = y / scale_rows.astype(np.float64)
+                lo = oracle.e4m3_encode(v * (1 - 2.0 ** -18) - 2.0 ** -40)
+                hi = oracle.e4m3_encode(v * (1 + 2.0 ** -18) + 2.0 ** -40)
+                mid = oracle.e4m3_encode(v)
+                ok = (got == mid) | (got == lo) | (got == hi)
+                assert np.all(ok), np.argwhere(~ok)[:5]
+
+
+def test_quantize_e4m3_ties_round_to_even(gpu_lib):
+    # A tile with amax 448 has scale 1, so its codes are e4m3(x) directly:
+    # every exact midpoint between e4m3 neighbours must go to the even code.
+    vals = oracle.e4m3_decode(np.arange(0x7e))
+    mids = (vals[:-1] + vals[1:]) / 2
+    bf = torch.tensor(mids).to(torch.bfloat16).double().numpy()
+    ties = bf[bf == mids]
+    x = np.zeros((1, 128, 1, 64), dtype=np.float32)
+    x.reshape(-1)[:len(ties)] = ties
+    x.reshape(-1)[-1] = 448.0
+    x8, sc = _quant(gpu_lib, torch.from_numpy(x).to(torch.bfloat16), None)
+    assert sc.item() == 1.0
+    assert np.array_equal(x8.reshape(-1)[:len(ties)], oracle.e4m3_encode(ties))
+
+
+def _fp8_run(fa, q, k, v, causal, signs):
+    dev = torch.device("cuda")
+    s = None if signs is None else torch.from_numpy(signs).to(dev)
+    q8, qs = fa.quantize_fp8(q.to(dev), s)
+    k8, ks = fa.quantize_fp8(k.to(dev), s)
+    v8, vs = fa.quantize_fp8(v.to(dev), None)
+    d = q.shape[-1]
+    o, lse = fa.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, alpha=synth.default_alpha(d))
+    assert fa.fa_check_status() == fa.FA_OK
+    return (o.float().cpu().numpy(), lse.cpu().numpy(),
+            (q8.cpu().numpy(), qs.cpu().numpy(), k8.cpu().numpy(), ks.cpu().numpy(),
+             v8.cpu().numpy(), vs.cpu().numpy()))
+
+
+def _dequant(codes, scales):
+    B, N, H, d = codes.shape
+    vals = oracle.e4m3_decode(codes)
+    rows = np.repeat(scales, 128, axis=2)[:, :, :N]          # [B, H, N]
+    return vals * np.transpose(rows, (0, 2, 1))[:, :, :, None]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_rmse_gate_and_rotation_helps(gpu_lib, causal):
+    B, H, N, d = 1, 4, 1024, 128
+    q, k, v = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + 5, outliers=True)
+    a = synth.default_alpha(d)
+    o_ref, lse_ref = oracle.attention(q, k, v, a, causal, n_threads=THREADS)
+    o_rot, lse_rot, _ = _fp8_run(gpu_lib, q, k, v, causal, synth.hadamard_signs(d))
+    o_plain, _, _ = _fp8_run(gpu_lib, q, k, v, causal, None)
+    rmse_rot = float(np.sqrt(np.mean((o_rot - o_ref) ** 2)))
+    rmse_plain = float(np.sqrt(np.mean((o_plain - o_ref) ** 2)))
+    print(f"FP8 RMSE causal={causal}: rotated {rmse_rot:.3e}, unrotated {rmse_plain:.3e}")
+    assert np.all(np.isfinite(o_rot))
+    assert rmse_rot <= 1.5e-2
+    assert rmse_rot < rmse_plain
+
+
+@pytest.mark.parametrize("B,H,N,causal", [(1, 2, 300, False), (1, 2, 300, True),
+                                           (2, 3, 1000, True), (1, 1, 129, False)])
+def test_fp8_kernel_against_dequantized_inputs(gpu_lib, B, H, N, causal):
+    d = 128
+    q, k, v = synth.qkv(B, H, N, d, seed=N + 3, outliers=True)
+    signs = synth.hadamard_signs(d, seed=N)
+    o, lse, (q8, qs, k8, ks, v8, vs) = _fp8_run(gpu_lib, q, k, v, causal, signs)
+    qd, kd, vd = _dequant(q8, qs), _dequant(k8, ks), _dequant(v8, vs)
+    a = synth.default_alpha(d)
+    o_deq, lse_deq = oracle.attention(qd, kd, vd, a, causal, n_threads=THREADS)
+    ratio_min = (vs / vs.max(axis=2, keepdims=True)).min()
+    for b in range(B):
+        for h in range(H):
+            vv = vd[b, :, h, :]
+            od = o_deq[b, :, h, :]
+            spread = np.max(np.abs(vv[None, :, :] - od[:, None, :]), axis=1)   # [N, d]
+            w = 2.0 ** -4 + N * 2.0 ** -10 / (ratio_min * 256.0)
+            bound = w * spread + 2.0 ** -8 * np.abs(od) + 1e-3
+            err = np.abs(o[b, :, h, :] - od)
+            assert np.all(err <= bound), (err / bound).max()
+    assert np.abs(lse - lse_deq).max() < 5e-2
+
+
+def test_fp8_full_size_sampled_rmse(gpu_lib):
+    # B4 H16 N4096 d128 with outliers, in the bench's launch configuration.
+    B, H, N, d = 4, 16, 4096, 128
+    q, k, v = synth.qkv(B, H, N, d, seed=synth.BASE_SEED, outliers=True)
+    o, _, _ = _fp8_run(gpu_lib, q, k, v, False, synth.hadamard_signs(d))
+    a = synth.default_alpha(d)
+    rng = np.random.default_rng(9)
+    sq = []
+    for b, h in [(0, 0), (3, 15), (1, 7), (2, 3)]:
+        rows = sorted(rng.choice(N, 48, replace=False).tolist())
+        o_ref, _ = oracle.attention_rows(q, k, v, a, False, b, h, rows)
+        sq.append((o[b, rows, h, :] - o_ref) ** 2)
+    rmse = float(np.sqrt(np.mean(np.concatenate(sq))))
+    print(f"FP8 sampled RMSE B4 H16 N4096 d128: {rmse:.3e}")
+    assert rmse <= 1.5e-2
