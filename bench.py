@@ -35,6 +35,8 @@ sys.path.insert(0, ROOT)
 
 PEAK_SPEC = 2250.0          # TFLOP/s dense BF16, the metric's denominator
 METRIC = "attention fwd TFLOP/s (BF16, d=128) and % of 2250 TFLOP/s dense peak"
+METRIC_FP8 = "attention fwd TFLOP/s (FP8 e4m3, d=128) and % of 4500 TFLOP/s dense FP8 peak"
+PEAK_SPEC_FP8 = 4500.0
 WORKLOAD = dict(B=4, H=16, N=4096, d=128)
 
 
@@ -227,8 +229,9 @@ def run_reference(args, B, H, N, d, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def config_name(B, H, N, d, causal):
-    return (f"attention fwd B{B} H{H} N{N} d{d} bf16 {'causal' if causal else 'non-causal'}"
+def config_name(B, H, N, d, causal, fp8=False):
+    kind = "fp8 e4m3 (outliers, Hadamard)" if fp8 else "bf16"
+    return (f"attention fwd B{B} H{H} N{N} d{d} {kind} {'causal' if causal else 'non-causal'}"
             f" (hidden {H * d}, {B * N} tokens)")
 
 
@@ -244,15 +247,29 @@ def run_ours(args, B, H, N, d, rank, world):
     fa.load()
     alpha = synth.default_alpha(d)
     causal = int(args.causal)
-    qh, kh, vh = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + rank)
+    qh, kh, vh = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + rank, outliers=args.fp8)
     q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
+    if args.fp8:
+        signs = torch.from_numpy(synth.hadamard_signs(d)).to(dev)
+        nt = (N + 127) // 128
+        q8, k8, v8 = (torch.empty(q.shape, dtype=torch.uint8, device=dev) for _ in range(3))
+        qs, ks, vs = (torch.empty((B, H, nt), dtype=torch.float32, device=dev) for _ in range(3))
+
+    def quantize():
+        for x, x8, sc, sg in ((q, q8, qs, signs), (k, k8, ks, signs), (v, v8, vs, None)):
+            rc = fa.fa_quantize_fp8(x, x8, sc, sg, B, H, N, d, sp)
+            if rc != fa.FA_OK:
+                raise fa.FaError(rc, "fa_quantize_fp8")
 
     def launch():
-        rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
+        if args.fp8:
+            rc = fa.fa_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, B, H, N, d, alpha, causal, sp)
+        else:
+            rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
         if rc != fa.FA_OK:
             raise fa.FaError(rc, "fa_fwd")
 
@@ -261,11 +278,23 @@ def run_ours(args, B, H, N, d, rank, world):
             dist.barrier()
 
     with torch.cuda.stream(stream):
+        if args.fp8:
+            quantize()
         for _ in range(args.warmup):
             launch()
     stream.synchronize()
     if fa.fa_check_status(sp) != fa.FA_OK:
         raise RuntimeError("device status after warm-up: " + str(fa.fa_status_detail()))
+    prepass_ms = None
+    if args.fp8:            # the pre-pass, timed on its own (3 tensors)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(20):
+                quantize()
+            ev1.record(stream)
+        stream.synchronize()
+        prepass_ms = ev0.elapsed_time(ev1) / 20
 
     # ---- device-resident timing ----
     start = torch.cuda.Event(enable_timing=True)
@@ -299,6 +328,8 @@ def run_ours(args, B, H, N, d, rank, world):
         q.copy_(qp, non_blocking=True)
         k.copy_(kp, non_blocking=True)
         v.copy_(vp, non_blocking=True)
+        if args.fp8:
+            quantize()
         launch()
         op.copy_(o, non_blocking=True)
         lp.copy_(lse, non_blocking=True)
@@ -323,6 +354,8 @@ def run_ours(args, B, H, N, d, rank, world):
     if rank != 0:
         return
     burst, sustained, src = measured_peaks()
+    if args.fp8:            # FP8 dense peak: the BF16 measurement x the nominal 2x ratio
+        burst, sustained = 2 * burst, 2 * sustained
     achieved = fl / (ms_step * 1e-3) / 1e12
     # A timed region of back-to-back launches longer than a second runs
     # under the power cap like the sustained cuBLAS loop; a short one is
@@ -331,20 +364,26 @@ def run_ours(args, B, H, N, d, rank, world):
         peak, peak_kind = sustained, "sustained"
     else:
         peak, peak_kind = burst, "burst"
-    wkey = config_name(B, H, N, d, args.causal)
+    wkey = config_name(B, H, N, d, args.causal, args.fp8)
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC_FP8 if args.fp8 else METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs)",
+        "dtype": "e4m3" if args.fp8 else "bf16",
+        "data": ("synthetic (seeded N(0,1) + 0.1% N(0,100) outliers)" if args.fp8
+                 else "synthetic (seeded N(0,1) inputs)"),
         "config": {"workload": wkey, "B": B, "H": H, "N": N, "d": d,
                    "causal": bool(args.causal),
                    "l2": "no flush: 192 MiB of inputs exceed the 126 MB L2",
                    "parallelism": f"replicas x{world}"},
         "pct_of_2250": 100.0 * value / world / PEAK_SPEC,
+        **({"pct_of_4500_fp8": 100.0 * value / world / PEAK_SPEC_FP8,
+            "prepass_ms": prepass_ms} if args.fp8 else {}),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
-                     "peak_source": f"{src} bf16 {peak_kind} (cuBLAS 8192^3)",
+                     "peak_source": (f"{src} bf16 {peak_kind} (cuBLAS 8192^3)"
+                                     + (" x 2 (nominal FP8/BF16 ratio)" if args.fp8 else "")),
                      "timed_region_ms": ms_max,
                      "traffic": profiled_traffic(wkey)},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -364,6 +403,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--causal", action="store_true")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 e4m3 path (outlier inputs, Hadamard rotation); times "
+                         "fa_fwd_fp8, reports the quantization pre-pass separately")
     ap.add_argument("--skip-cpu", action="store_true",
                     help="omit the cpu_baseline leg (profiling runs)")
     ap.add_argument("--B", type=int, default=WORKLOAD["B"])
