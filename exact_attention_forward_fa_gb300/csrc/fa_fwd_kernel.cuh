@@ -84,19 +84,11 @@ struct FwdCfg {
     static constexpr uint32_t KV_OFF = 2 * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
     // barrier indices
-    // P is published in two parts: keys [0, 96) on B_PFULL (PV k-steps 0-5)
-    // and keys [96, 128) on B_PFULL2 (k-steps 6-7), so the P V product of a
-    // tile starts while its last quarter of exponentials is computed.
     static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4,
                          B_KVEMPTY = 4 + NSTAGE, B_SFULL = 4 + 2 * NSTAGE,
-                         B_PFULL = B_SFULL + 2, B_PFULL2 = B_PFULL + 2,
-                         B_OFULL = B_PFULL2 + 2,
+                         B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
                          B_OEMPTY = B_OFULL + 2, B_MMADONE = B_OEMPTY + 2,
                          NBAR = B_MMADONE + 1;
-    // The split pays off where the softmax dominates (d = 64); at d = 128
-    // the extra store wait costs more than the earlier PV start gains.
-    static constexpr bool SPLIT_P = (D == 64) && !kFP8;
-    static constexpr int PV_SPLIT = SPLIT_P ? 6 : PV_STEPS;   // PV k-steps covered by B_PFULL
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;   // + align slack
 
@@ -115,6 +107,11 @@ struct FwdCfg {
     // P <= 2^8.8 < 448, the largest e4m3 value.
     static constexpr float TAU = kFP8 ? 0.8f : 8.0f;
     static constexpr float P_OFFSET = kFP8 ? 8.0f : 0.0f;
+    // 16-bit P is first formed against the current reference r and kept
+    // when the tile's FP32 row sum is <= 2^16.  The sum bounds every term,
+    // so a kept tile has P <= 2^16; a tile that fails has a term > 2^16/128
+    // = 2^9 > 2^tau, so its row max grew by more than tau and r moves.
+    static constexpr float KEEP_SUM = 65536.0f;
 };
 
 // The geometry of one work unit, identical in every role.
@@ -179,7 +176,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_init(bar(C::B_QEMPTY + x), 1);
             mbar_init(bar(C::B_SFULL + x), 1);
             mbar_init(bar(C::B_PFULL + x), 4);
-            mbar_init(bar(C::B_PFULL2 + x), 4);
             mbar_init(bar(C::B_OFULL + x), 1);
             mbar_init(bar(C::B_OEMPTY + x), 4);
         }
@@ -284,7 +280,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                 C::CHUNK_BYTES, 1024u);
                             const uint32_t acc = (t - 1 > t0x) ? 1u : 0u;
 #pragma unroll
-                            for (int kk = 0; kk < C::PV_SPLIT; ++kk) {
+                            for (int kk = 0; kk < C::PV_STEPS; ++kk) {
                                 const uint64_t bd = vd + ((kk * C::PV_KEYS * 128u) >> 4);
                                 if constexpr (kFP8)
                                     mma_ts_f8_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
@@ -292,14 +288,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                 else
                                     mma_ts_f16_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
                                                      bd, C::IDESC_PV, (acc | kk) ? 1u : 0u);
-                            }
-                            if constexpr (C::SPLIT_P) {
-                                if (!mbar_wait_warp(bar(C::B_PFULL2 + x), pph, w, 15)) return false;
-                                tc_fence_after();
-#pragma unroll
-                                for (int kk = C::PV_SPLIT; kk < C::PV_STEPS; ++kk)
-                                    mma_ts_f16_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
-                                                     vd + ((kk * C::PV_KEYS * 128u) >> 4), C::IDESC_PV, 1u);
                             }
                             pph ^= 1;
                             if (t == U.T) mma_commit_elect(bar(C::B_OFULL + x));
@@ -356,7 +344,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t tO = tbase + lane_off + C::col_o(x);
         WaitCtx w{abort_flag, a.status, x ? kRoleSoftmax1 : kRoleSoftmax0};
         const float sl2 = a.scale_log2;
-        const float2 c2 = make_float2(sl2, sl2);
         uint32_t sph = 0, oph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
@@ -388,52 +375,58 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 sph ^= 1;
                 tc_fence_after();
                 uint32_t s[128];
-                tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-                tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-                tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
-                tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
-                tmem_ld_wait();
                 float *sf = reinterpret_cast<float *>(s);
-                // ---- masks: sequence tail and causal diagonal ----
+                // ---- S -> registers, masks: sequence tail and causal diagonal ----
                 int lim = 128;
                 if (j == a.n_kv - 1) lim = min(lim, a.N - j * 128);
                 if (kCausal && j == mt) lim = min(lim, row + 1);
-                if (lim < 128) {
+                auto load_s = [&]() __attribute__((always_inline)) {
+                    tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+                    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+                    tmem_ld_wait();
+                    if (lim < 128) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) if (c >= lim) sf[c] = -INFINITY;
-                }
-                // ---- row max ----
-                float m0 = sf[0], m1 = sf[1], m2 = sf[2], m3 = sf[3];
+                        for (int c = 0; c < 128; ++c) if (c >= lim) sf[c] = -INFINITY;
+                    }
+                };
+                load_s();
+                auto row_max = [&]() __attribute__((always_inline)) -> float {
+                    float m0 = sf[0], m1 = sf[1], m2 = sf[2], m3 = sf[3];
 #pragma unroll
-                for (int c = 4; c < 128; c += 8) {
-                    m0 = max3(m0, sf[c + 0], sf[c + 4]);
-                    m1 = max3(m1, sf[c + 1], sf[c + 5]);
-                    m2 = max3(m2, sf[c + 2], sf[c + 6]);
-                    m3 = max3(m3, sf[c + 3], sf[c + 7]);
-                }
-                const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-                // Score scale to log2 units; FP8 adds the q and k tile scales
-                // ("FlashAttention-3 on Hopper", sec. 6.3) and the exponent
-                // offset 8 + log2(v_j / v_max) (P carries the V tile scale).
-                float sc = sl2, voff = 0.f, vratio = 1.f;
-                if constexpr (kFP8) {
-                    sc = sl2 * qs * a.k_scale[sbase + j];
-                    vratio = a.v_scale[sbase + j] / vmax;
-                    voff = C::P_OFFSET + log2f(vratio);
-                }
-                const float bnew = mx * sc;                     // -inf stays -inf
-                // ---- conditional rescale: move r only if the max grew by > tau ----
-                float rn, corr;
-                if (r == -INFINITY) { rn = bnew; corr = 1.f; }
-                else { rn = (bnew > r + C::TAU) ? bnew : r; corr = ex2_approx(r - rn); }
-                const bool need = (r != -INFINITY) && (rn != r);
-                const float rs = (rn == -INFINITY) ? 0.f : rn;
-                const float2 c2 = make_float2(sc, sc);
-                const float2 nr2 = make_float2(voff - rs, voff - rs);
-                float2 e_a = make_float2(0.f, 0.f), e_b = e_a, r_a = e_a, r_b = e_a;
+                    for (int c = 4; c < 128; c += 8) {
+                        m0 = max3(m0, sf[c + 0], sf[c + 4]);
+                        m1 = max3(m1, sf[c + 1], sf[c + 5]);
+                        m2 = max3(m2, sf[c + 2], sf[c + 6]);
+                        m3 = max3(m3, sf[c + 3], sf[c + 7]);
+                    }
+                    return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+                };
+                // r: reference of this tile's P; corr = 2^(r_old - r) rescales O
+                // and the row sums when r moves.
+                float rn = r, corr = 1.f, vr = 1.f;
+                bool need = false;
+                float2 e_a, e_b;
                 uint32_t p[kFP8 ? 32 : 64];
                 if constexpr (kFP8) {
-                    // ---- FP8: P' = 2^(x - r + 8) (v_j / v_max) as e4m3 ----
+                    // Score scale to log2 units with the q and k tile scales
+                    // ("FlashAttention-3 on Hopper", sec. 6.3); the exponent
+                    // offset 8 + log2(v_j / v_max) carries the V tile scale.
+                    const float sc = sl2 * qs * a.k_scale[sbase + j];
+                    vr = a.v_scale[sbase + j] / vmax;
+                    const float voff = C::P_OFFSET + log2f(vr);
+                    // e4m3 saturates above 448, so the row max comes first.
+                    const float bnew = row_max() * sc;             // -inf stays -inf
+                    if (r == -INFINITY) rn = bnew;
+                    else { rn = (bnew > r + C::TAU) ? bnew : r; corr = ex2_approx(r - rn); }
+                    need = (r != -INFINITY) && (rn != r);
+                    const float rs = (rn == -INFINITY) ? 0.f : rn;
+                    const float2 c2 = make_float2(sc, sc);
+                    const float2 nr2 = make_float2(voff - rs, voff - rs);
+                    e_a = make_float2(0.f, 0.f);
+                    e_b = e_a;
+                    // ---- P' = 2^(x - r + 8) (v_j / v_max) as e4m3 ----
 #pragma unroll
                     for (int c = 0; c < 128; c += 4) {
                         const float2 x01 = __ffma2_rn(make_float2(sf[c + 0], sf[c + 1]), c2, nr2);
@@ -444,39 +437,46 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         e_a = __fadd2_rn(e_a, e01);
                         e_b = __fadd2_rn(e_b, e23);
                     }
-                    // the row sum counts 2^(x - r + 8) without the V factor
-                    le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y)) / vratio;
                     tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
                 } else {
-                // ---- 16-bit P: exponentials, P, both row sums ----
-#define FA_EXP4(c)                                                                     \
-    {                                                                                  \
-        const float2 x01 = __ffma2_rn(make_float2(sf[(c) + 0], sf[(c) + 1]), c2, nr2);  \
-        const float2 x23 = __ffma2_rn(make_float2(sf[(c) + 2], sf[(c) + 3]), c2, nr2);  \
-        const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));          \
-        const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));          \
-        const uint32_t pk0 = pack2<kBF16>(e01.x, e01.y);                               \
-        const uint32_t pk1 = pack2<kBF16>(e23.x, e23.y);                               \
-        p[(c) / 2] = pk0;                                                              \
-        p[(c) / 2 + 1] = pk1;                                                          \
-        e_a = __fadd2_rn(e_a, e01);                                                    \
-        e_b = __fadd2_rn(e_b, e23);                                                    \
-        add_pair<kBF16>(r_a.x, r_a.y, pk0);                                            \
-        add_pair<kBF16>(r_b.x, r_b.y, pk1);                                            \
-    }
-                constexpr int CA = C::SPLIT_P ? 96 : 128;   // columns of part A
+                    // ---- 16-bit P = 2^(x - r): first against the current r;
+                    //      the max is formed only on the first tile or when
+                    //      the tile's sum exceeds KEEP_SUM ----
+                    const float2 c2 = make_float2(sl2, sl2);
+                    auto exps = [&](const float rs) __attribute__((always_inline)) {
+                        const float2 nr2 = make_float2(-rs, -rs);
+                        e_a = make_float2(0.f, 0.f);
+                        e_b = e_a;
 #pragma unroll
-                for (int c = 0; c < CA; c += 4) FA_EXP4(c)
-                if constexpr (!C::SPLIT_P) {
-                    le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y));
-                    lr = lr * corr + ((r_a.x + r_a.y) + (r_b.x + r_b.y));
+                        for (int c = 0; c < 128; c += 4) {
+                            const float2 x01 = __ffma2_rn(make_float2(sf[c + 0], sf[c + 1]), c2, nr2);
+                            const float2 x23 = __ffma2_rn(make_float2(sf[c + 2], sf[c + 3]), c2, nr2);
+                            const float2 e01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
+                            const float2 e23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
+                            p[c / 2] = pack2<kBF16>(e01.x, e01.y);
+                            p[c / 2 + 1] = pack2<kBF16>(e23.x, e23.y);
+                            e_a = __fadd2_rn(e_a, e01);
+                            e_b = __fadd2_rn(e_b, e23);
+                        }
+                    };
+                    bool keep = __all_sync(0xffffffffu, r != -INFINITY);
+                    if (keep) {
+                        exps(r);
+                        const float ts = (e_a.x + e_a.y) + (e_b.x + e_b.y);
+                        keep = __all_sync(0xffffffffu, ts <= C::KEEP_SUM);   // NaN: redo
+                        if (!keep) load_s();
+                    }
+                    if (!keep) {
+                        const float bnew = row_max() * sl2;
+                        if (r == -INFINITY) rn = bnew;
+                        else { rn = (bnew > r + C::TAU) ? bnew : r; corr = ex2_approx(r - rn); }
+                        need = (r != -INFINITY) && (rn != r);
+                        exps((rn == -INFINITY) ? 0.f : rn);
+                    }
+                    tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
+                    tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
                 }
-                tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-                if constexpr (C::SPLIT_P) tmem_st16(tS + 32, &p[32]);
-                else tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&p[32]));
-                }
-                // ---- correction of O (its previous PV completed before S_FULL),
-                //      before the first part of P is published ----
+                // ---- correction of O (its previous PV completed before S_FULL) ----
                 if (__any_sync(0xffffffffu, need)) {
                     const float2 cc = make_float2(corr, corr);
 #pragma unroll 1
@@ -498,18 +498,18 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_PFULL + x));
-                if constexpr (C::SPLIT_P) {
+                // ---- row sums, after P is published ----
+                // (FP8: the row sum counts 2^(x - r + 8) without the V factor)
+                le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y)) / vr;
+                if constexpr (!kFP8) {
+                    float2 r_a = make_float2(0.f, 0.f), r_b = r_a;
 #pragma unroll
-                    for (int c = 96; c < 128; c += 4) FA_EXP4(c)
-                    tmem_st16(tS + 48, &p[48]);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::B_PFULL2 + x));
-                    le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y));
+                    for (int i = 0; i < 64; i += 2) {
+                        add_pair<kBF16>(r_a.x, r_a.y, p[i]);
+                        add_pair<kBF16>(r_b.x, r_b.y, p[i + 1]);
+                    }
                     lr = lr * corr + ((r_a.x + r_a.y) + (r_b.x + r_b.y));
                 }
-#undef FA_EXP4
                 r = rn;
             }
             if (!ok) break;

@@ -175,6 +175,27 @@ def test_other_scales_and_wide_scores(gpu_lib, alpha):
                scale_aware=True)
 
 
+@pytest.mark.parametrize("lift", [2.0, 5.0])
+@pytest.mark.parametrize("d", [64, 128])
+def test_late_spike_moves_the_reference(gpu_lib, d, lift):
+    # Key 0 scores far above every other key for most rows.  Key tiles are
+    # visited from the last to the first, so the spike arrives on the final
+    # tile: depending on the row the reference point either stays (P up to
+    # 2^16) or moves late, rescaling everything accumulated before it.
+    B, H, N = 1, 2, 700
+    q, k, v = synth.qkv(B, H, N, d, seed=33)
+    u = torch.ones(d) / d ** 0.5
+    q = (q.float() + lift * u).to(torch.bfloat16)
+    k = k.clone()
+    k[:, 0] = (5.0 * d ** 0.5 * u).to(torch.bfloat16)
+    a = synth.default_alpha(d)
+    for causal in (False, True):
+        o, lse = _run(gpu_lib, q, k, v, causal, a)
+        o_ref, lse_ref = oracle.attention(q, k, v, a, causal, n_threads=THREADS)
+        _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref,
+               scale_aware=True)
+
+
 def test_outputs_beyond_n_untouched(gpu_lib):
     # Rows >= N of the last tile are computed but never stored.
     fa = gpu_lib
