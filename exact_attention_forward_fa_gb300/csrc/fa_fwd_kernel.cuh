@@ -524,26 +524,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int grow = mt * 128 + row;
             uint16_t *orow = reinterpret_cast<uint16_t *>(a.o) +
                              ((static_cast<size_t>(U.b) * a.N + grow) * a.H + U.h) * D;
-#pragma unroll 1
-            for (int ch = 0; ch < D / 32; ++ch) {
-                uint32_t ov[32];
-                tmem_ld32(tO + ch * 32, ov);
-                tmem_ld_wait();
-                uint32_t pk[16];
+            // The whole O row comes into registers first, so the accumulator
+            // is handed back to the next unit's P V before the stores.
+            uint32_t ov[D];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack2<kBF16>(__uint_as_float(ov[2 * i]) * inv,
-                                         __uint_as_float(ov[2 * i + 1]) * inv);
-                if (grow < a.N) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
-            }
+            for (int ch = 0; ch < D / 32; ++ch)
+                tmem_ld32(tO + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[ch * 32]));
+            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + x));
+            if (grow < a.N) {
+#pragma unroll
+                for (int ch = 0; ch < D / 8; ++ch) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        pk[i] = pack2<kBF16>(__uint_as_float(ov[8 * ch + 2 * i]) * inv,
+                                             __uint_as_float(ov[8 * ch + 2 * i + 1]) * inv);
+                    reinterpret_cast<uint4 *>(orow)[ch] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
             if (a.lse != nullptr && grow < a.N) {
                 const float lse = live ? (r - C::P_OFFSET + log2f(le)) * 0.69314718055994530942f
                                        : -INFINITY;
