@@ -180,8 +180,31 @@ fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
     DeviceInfo *dev = nullptr;
     fa_status st = get_device(&dev);
     if (st != FA_OK) return st;
-    cudaError_t e = fa::launch_quantize(x, x8, scales, hadamard_signs, B, H, N, d,
-                                        static_cast<cudaStream_t>(stream));
+    fa::QuantLaunch L;
+    // one TMA box is a whole 128-row tile: {d, 1, 128, 1}, no swizzle
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {2ull * d, 2ull * d * H, 2ull * d * H * static_cast<cuuint64_t>(N)};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (g_encode(&L.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides,
+                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return FA_ERR_CUDA;
+    L.args.x8 = x8;
+    L.args.scales = scales;
+    L.args.signs = hadamard_signs;
+    L.args.status = dev->status;
+    L.args.B = B;
+    L.args.H = H;
+    L.args.N = N;
+    L.args.n_tiles = static_cast<int>(n_tiles);
+    L.args.total = static_cast<int>(static_cast<uint64_t>(B) * H * n_tiles);
+    L.d = d;
+    L.sm_count = dev->sm_count;
+    L.stream = static_cast<cudaStream_t>(stream);
+    cudaError_t e = fa::launch_quantize(L);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -23,8 +23,23 @@ cudaError_t launch_fwd_d64(const FwdLaunch &L);
 cudaError_t launch_fwd_d128(const FwdLaunch &L);
 cudaError_t launch_fwd_d256(const FwdLaunch &L);   // K/V maps with 64-row boxes
 cudaError_t launch_fwd_fp8(const FwdLaunch &L);    // e4m3 maps, 128-byte boxes
-cudaError_t launch_quantize(const void *x, void *x8, float *scales, const float *signs,
-                            int B, int H, int N, int d, cudaStream_t stream);
+// FP8 pre-pass: persistent CTAs over (b, h, 128-row tile); x arrives by
+// TMA (map {d, H, N, B}, box {d, 1, 128, 1}, no swizzle, rows >= N zero).
+struct QuantArgs {
+    uint8_t *x8;            // e4m3 codes, [B][N][H][d]
+    float *scales;          // [B][H][n_tiles]
+    const float *signs;     // +-1 diagonal of the rotation, or null
+    uint32_t *status;       // device status word
+    int B, H, N, n_tiles, total;   // total = B * H * n_tiles
+};
+struct QuantLaunch {
+    CUtensorMap x;
+    QuantArgs args;
+    int d;
+    int sm_count;
+    cudaStream_t stream;
+};
+cudaError_t launch_quantize(const QuantLaunch &L);
 
 // Shared helper: set the dynamic shared-memory limit once per device, then
 // launch one instantiation.

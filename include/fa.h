@@ -125,7 +125,8 @@ fa_status fa_check_status(void *stream);
 /*
  * fa_status_detail -- the status word captured by the last fa_check_status
  * that returned FA_ERR_TIMEOUT: out[0] code, out[1] role that gave up
- * (1/2 softmax group L/H, 3 producer, 4 MMA issuer), out[2] wait site,
+ * (1/2 softmax group L/H, 3 producer, 4 MMA issuer, 6 FP8 pre-pass),
+ * out[2] wait site,
  * out[3] block index.  Zeros if no timeout was ever reported.
  */
 void fa_status_detail(uint32_t out[4]);

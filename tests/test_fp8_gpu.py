@@ -4,8 +4,10 @@ oracle's block quantization, and the FP8 forward against FP64 attention.
 * Quantization ("FlashAttention-3 on Hopper", sec. 6.3-6.4): scales equal
   amax/448 of the (rotated) tile -- exactly without rotation, to 2^-20
   relative with it (the kernel's FP32 Walsh-Hadamard butterflies round);
-  codes equal the round-to-nearest e4m3 code of y/scale, except where y/scale
-  lies within 2^-18 of a rounding boundary, where either neighbour is valid.
+  codes equal the round-to-nearest e4m3 code of y/scale (the kernel forms
+  y * (1/scale) in FP32, within one rounding of the quotient), except where
+  y/scale lies within 2^-18 of a rounding boundary, where either neighbour
+  is valid.
 * FP8 forward on the outlier distribution (N(0,1) + 0.1% N(0,100)), the
   metric of the FA3 numerical-error experiment: O RMSE against the FP64
   oracle on the unquantized inputs <= 1.5e-2 with block scales and the
@@ -56,9 +58,10 @@ def test_quantize_matches_oracle(gpu_lib, d, rotate):
             got = x8[b, :, h, :]
             scale_rows = np.repeat(sc[b, h], 128)[:N, None]          # float32
             if not rotate:
-                # Same decision in the kernel's precision: the FP32 quotient
-                # x / scale, then round-to-nearest-even to e4m3 -> bit exact.
-                q32 = (xh.astype(np.float32) / scale_rows).astype(np.float64)
+                # Same decision in the kernel's precision: the FP32 product
+                # x * (1 / scale), then round-to-nearest-even to e4m3 -> bit exact.
+                inv = np.float32(1.0) / scale_rows
+                q32 = (xh.astype(np.float32) * inv).astype(np.float64)
                 assert np.array_equal(got, oracle.e4m3_encode(q32))
             else:
                 # The rotated values carry FP32 butterfly rounding: the code
