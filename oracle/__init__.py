@@ -1,4 +1,5 @@
-"""FP64 CPU oracle for exact attention forward -- TEST INFRASTRUCTURE ONLY.
+"""FP64 CPU oracle for exact attention (forward and gradients) -- TEST
+INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 ``--impl reference`` legs of ``bench.py`` may import this package.  The
@@ -15,6 +16,8 @@ computes, and the passage it follows, is stated in ``fa_oracle.c``:
 * ``attention_online``: the tiled online recurrence with the conditional
   rescale rule, "FlashAttention-3 on Hopper" sec. 4.2 and "FlashAttention
   v1-v4" (conditional rescale).
+* ``attention_bwd`` / ``attention_bwd_head``: the gradients dQ, dK, dV from
+  the definition, "FlashAttention-3 on Hopper" sec. 7.1.
 * ``hadamard_rotate``, ``e4m3_encode`` / ``e4m3_decode``,
   ``quantize_e4m3_tiles``: the FP8 pre-pass pieces, "FlashAttention-3 on
   Hopper" sec. 6.1, 6.3, 6.4.
@@ -64,6 +67,16 @@ def _load():
         _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int]
     lib.oracle_attention_fwd.restype = ctypes.c_int
+    lib.oracle_attention_bwd_head.argtypes = [
+        _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_long,
+        ctypes.c_double, ctypes.c_int, _dp, ctypes.c_long, _dp, ctypes.c_long,
+        _dp, ctypes.c_long]
+    lib.oracle_attention_bwd_head.restype = ctypes.c_int
+    lib.oracle_attention_bwd.argtypes = [
+        _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int]
+    lib.oracle_attention_bwd.restype = ctypes.c_int
     lib.oracle_attention_online_head.argtypes = [
         _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_double,
@@ -109,6 +122,37 @@ def attention(q, k, v, alpha: float, causal: bool, n_threads: int = 1):
     if rc:
         raise RuntimeError(f"oracle_attention_fwd failed ({rc})")
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, alpha: float, causal: bool, n_threads: int = 1):
+    """Gradients (dQ, dK, dV) [B,N,H,d] in float64 of attention with the
+    upstream gradient dO [B,N,H,d]."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, N, H, d = q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(q), np.zeros_like(q)
+    rc = _load().oracle_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                      _ptr(dq), _ptr(dk), _ptr(dv), B, H, N, d,
+                                      float(alpha), int(bool(causal)),
+                                      int(n_threads))
+    if rc:
+        raise RuntimeError(f"oracle_attention_bwd failed ({rc})")
+    return dq, dk, dv
+
+
+def attention_bwd_head(q, k, v, dout, alpha: float, causal: bool):
+    """One head: q/dout [Nq,d], k/v [Nk,d] -> (dQ [Nq,d], dK, dV [Nk,d])."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    Nq, d = q.shape
+    Nk = k.shape[0]
+    dq = np.zeros((Nq, d))
+    dk = np.zeros((Nk, d))
+    dv = np.zeros((Nk, d))
+    rc = _load().oracle_attention_bwd_head(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), Nq, Nk, d, d, d, d, d,
+        float(alpha), int(bool(causal)), _ptr(dq), d, _ptr(dk), d, _ptr(dv), d)
+    if rc:
+        raise RuntimeError(f"oracle_attention_bwd_head failed ({rc})")
+    return dq, dk, dv
 
 
 def attention_head(q, k, v, alpha: float, causal: bool, rows=None,

@@ -1,5 +1,6 @@
 /*
- * fa_oracle.c -- plain, slow, FP64 CPU oracle for exact attention forward.
+ * fa_oracle.c -- plain, slow, FP64 CPU oracle for exact attention (forward
+ * and its gradients).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
  * load this file: only the tests, the smoke check and the CPU-baseline leg
@@ -13,6 +14,8 @@
  *           sec. 3.2.1 block-combine, sec. 4.2 online-softmax invariant,
  *           sec. 4.6 finalize: empty rows give O = 0 and LSE = -inf,
  *           sec. 4.7 causal predicate col > row + (Nk - Nq),
+ *           sec. 7.1 gradient math (product rule through S = alpha Q K^T
+ *           and O = P V; softmax Jacobian contracted to D_i = <P_i, dP_i>),
  *           sec. 6.3 block quantization, sec. 6.4 incoherent processing
  *           M = (1/sqrt d) H D with H a Hadamard matrix, D = diag(+-1).
  *   [FAv4]  "FlashAttention v1-v4: from IO awareness to asynchronous
@@ -189,6 +192,136 @@ int oracle_attention_fwd(const double *q, const double *k, const double *v,
     for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
     return J.err;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Gradients, one head: [FA3H] sec. 7.1.  With S = alpha Q K^T (masked       */
+/* entries -inf), P = softmax(S) row-wise and O = P V, for an upstream       */
+/* gradient dO:                                                              */
+/*   dV  = P^T dO                                                            */
+/*   dP  = dO V^T                                                            */
+/*   D_i = sum_j P_ij dP_ij          (the softmax Jacobian, contracted)      */
+/*   dS  = P o (dP - D)              (o: elementwise; D broadcast per row)   */
+/*   dQ  = alpha dS K,   dK = alpha dS^T Q                                   */
+/* P is materialised row by row from the definition above; a row with no     */
+/* visible key contributes nothing.  dq rows: every query row; dk, dv rows:  */
+/* every key row (accumulated over the query rows).                          */
+/* ------------------------------------------------------------------------ */
+int oracle_attention_bwd_head(const double *q, const double *k, const double *v,
+                              const double *dout, int Nq, int Nk, int d,
+                              long ldq, long ldk, long ldv, long lddo,
+                              double alpha, int causal, double *dq, long lddq,
+                              double *dk, long lddk, double *dv, long lddv)
+{
+    if (Nq < 0 || Nk < 0 || d < 1 || !q || !k || !v || !dout || !dq || !dk || !dv)
+        return -1;
+    size_t nk1 = (size_t)(Nk > 0 ? Nk : 1);
+    double *s = (double *)malloc(sizeof(double) * nk1);
+    double *p = (double *)malloc(sizeof(double) * nk1);
+    double *pr = (double *)malloc(sizeof(double) * nk1);
+    double *dp = (double *)malloc(sizeof(double) * nk1);
+    double *orow = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!s || !p || !pr || !dp || !orow) {
+        free(s); free(p); free(pr); free(dp); free(orow);
+        return -1;
+    }
+    for (int j = 0; j < Nk; ++j)
+        for (int c = 0; c < d; ++c) {
+            dk[(long)j * lddk + c] = 0.0;
+            dv[(long)j * lddv + c] = 0.0;
+        }
+    for (int i = 0; i < Nq; ++i) {
+        const double *qi = q + (long)i * ldq;
+        const double *doi = dout + (long)i * lddo;
+        double *dqi = dq + (long)i * lddq;
+        double lse;
+        attention_row(qi, k, v, i, Nq, Nk, d, ldk, ldv, alpha, causal, s, p,
+                      orow, &lse, pr);
+        for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+        if (lse == -INFINITY) continue;          /* no visible key */
+        /* dP_ij = dO_i . v_j ; D_i = sum_j P_ij dP_ij */
+        double D = 0.0;
+        for (int j = 0; j < Nk; ++j) {
+            const double *vj = v + (long)j * ldv;
+            double t = 0.0;
+            for (int c = 0; c < d; ++c) t += doi[c] * vj[c];
+            dp[j] = t;
+            D += pr[j] * t;
+        }
+        for (int j = 0; j < Nk; ++j) {
+            if (pr[j] == 0.0) continue;
+            const double ds = pr[j] * (dp[j] - D);
+            const double *kj = k + (long)j * ldk;
+            double *dkj = dk + (long)j * lddk;
+            double *dvj = dv + (long)j * lddv;
+            for (int c = 0; c < d; ++c) {
+                dqi[c] += alpha * ds * kj[c];
+                dkj[c] += alpha * ds * qi[c];
+                dvj[c] += pr[j] * doi[c];
+            }
+        }
+    }
+    free(s); free(p); free(pr); free(dp); free(orow);
+    return 0;
+}
+
+typedef struct {
+    const double *q, *k, *v, *dout;
+    double *dq, *dk, *dv;
+    int B, H, N, d, causal;
+    double alpha;
+    int next;
+    int err;
+    pthread_mutex_t mu;
+} bwd_job;
+
+static void *bwd_worker(void *arg)
+{
+    bwd_job *J = (bwd_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int u = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (u >= J->B * J->H) break;
+        int b = u / J->H, h = u % J->H;
+        long ld = (long)J->H * J->d;
+        long off = ((long)b * J->N * J->H + h) * J->d;
+        int rc = oracle_attention_bwd_head(J->q + off, J->k + off, J->v + off,
+                                           J->dout + off, J->N, J->N, J->d, ld,
+                                           ld, ld, ld, J->alpha, J->causal,
+                                           J->dq + off, ld, J->dk + off, ld,
+                                           J->dv + off, ld);
+        if (rc) {
+            pthread_mutex_lock(&J->mu);
+            J->err = rc;
+            pthread_mutex_unlock(&J->mu);
+        }
+    }
+    return NULL;
+}
+
+/* Whole [B][N][H][d] tensors, threaded over (b, h): each head's gradients
+ * depend on that head alone. */
+int oracle_attention_bwd(const double *q, const double *k, const double *v,
+                         const double *dout, double *dq, double *dk, double *dv,
+                         int B, int H, int N, int d, double alpha, int causal,
+                         int n_threads)
+{
+    if (B < 1 || H < 1 || N < 0 || d < 1) return -1;
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 512) n_threads = 512;
+    bwd_job J = {q, k, v, dout, dq, dk, dv, B, H, N, d, causal, alpha, 0, 0,
+                 PTHREAD_MUTEX_INITIALIZER};
+    pthread_t th[512];
+    int started = 0;
+    for (int t = 0; t < n_threads; ++t) {
+        if (pthread_create(&th[t], NULL, bwd_worker, &J) != 0) break;
+        ++started;
+    }
+    if (started == 0) bwd_worker(&J);
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+    return J.err;
+}
+
 
 /* ------------------------------------------------------------------------ */
 /* The tiled online algorithm, FP64, one head: the method's own steps, kept  */

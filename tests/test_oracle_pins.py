@@ -13,7 +13,12 @@
 * block quantization: scale = amax / 448 and half-ulp reconstruction;
 * a stored golden case (tests/golden) written by oracle-only script;
 * planted mistakes (swapped or transposed operands, a wrong scale) fail the
-  brute-force pin, so the pins are sensitive to them.
+  brute-force pin, so the pins are sensitive to them;
+* gradients: central finite differences of L = sum(O * dO) through the
+  forward definition, fp64 torch autograd through plain ops, the invariants
+  sum_j dK_j = 0, D_i = dO_i . O_i and dV = P^T dO, and planted mistakes
+  (swapped operands, a dropped scale, an ignored mask) that the
+  finite-difference pin rejects.
 """
 import json
 import math
@@ -290,3 +295,102 @@ def test_planted_mistakes_are_caught():
     # sign error in the scores
     o, l = oracle.attention_head(-q, k, v, a, False)
     assert _brute_fails(q, k, v, a, False, o, l)
+
+
+# ---------------------------------------------------------------------------
+# Gradients ("FlashAttention-3 on Hopper", sec. 7.1)
+# ---------------------------------------------------------------------------
+
+def _loss(q, k, v, dout, a, causal):
+    """L = sum(O * dO), whose gradients are the ones the backward returns."""
+    o, _ = oracle.attention_head(q, k, v, a, causal)
+    return float(np.sum(o * dout))
+
+
+def _fd_grads(q, k, v, dout, a, causal, eps=1e-5):
+    """Central finite differences of L with respect to every input element."""
+    out = []
+    for which in range(3):
+        args = [q.copy(), k.copy(), v.copy()]
+        g = np.zeros_like(args[which])
+        for idx in np.ndindex(g.shape):
+            x0 = args[which][idx]
+            args[which][idx] = x0 + eps
+            lp = _loss(*args, dout, a, causal)
+            args[which][idx] = x0 - eps
+            lm = _loss(*args, dout, a, causal)
+            args[which][idx] = x0
+            g[idx] = (lp - lm) / (2 * eps)
+        out.append(g)
+    return out
+
+
+def _fd_agrees(grads, fd, tol=1e-7):
+    return all(np.allclose(g, f, rtol=tol, atol=tol) for g, f in zip(grads, fd))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nk,d", [(1, 1, 1), (3, 3, 2), (5, 5, 3), (4, 6, 2), (6, 3, 3)])
+def test_bwd_matches_finite_differences(nq, nk, d, causal):
+    q, k, v, dout = _rand(nq, d), _rand(nk, d), _rand(nk, d), _rand(nq, d)
+    a = 0.9
+    grads = oracle.attention_bwd_head(q, k, v, dout, a, causal)
+    assert _fd_agrees(grads, _fd_grads(q, k, v, dout, a, causal))
+
+
+def _torch_grads(q, k, v, dout, a, causal):
+    """The same gradients by fp64 autograd through plain torch ops."""
+    t = [torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v)]
+    s = a * t[0] @ t[1].T
+    if causal:
+        nq, nk = s.shape
+        i = torch.arange(nq)[:, None]
+        j = torch.arange(nk)[None, :]
+        s = s.masked_fill(j > i + (nk - nq), float("-inf"))
+    o = torch.softmax(s, dim=-1) @ t[2]
+    o.backward(torch.tensor(dout, dtype=torch.float64))
+    return [x.grad.numpy() for x in t]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_matches_torch_autograd(causal):
+    B, H, N, d = 1, 2, 37, 8
+    q, k, v, dout = (_rand(B, N, H, d) for _ in range(4))
+    a = 0.35
+    dq, dk, dv = oracle.attention_bwd(q, k, v, dout, a, causal, n_threads=2)
+    for h in range(H):
+        ref = _torch_grads(q[0, :, h], k[0, :, h], v[0, :, h], dout[0, :, h], a, causal)
+        for got, want in zip((dq[0, :, h], dk[0, :, h], dv[0, :, h]), ref):
+            assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_invariants(causal):
+    # Each row of dS sums to zero, so the key gradients sum to zero; and
+    # D_i = <P_i, dP_i> equals dO_i . O_i (sec. 7.1.2), which the GPU uses.
+    N, d = 29, 6
+    q, k, v, dout = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+    a = 0.6
+    dq, dk, dv = oracle.attention_bwd_head(q, k, v, dout, a, causal)
+    assert np.abs(dk.sum(axis=0)).max() <= 1e-12
+    o, _, p = oracle.attention_head(q, k, v, a, causal, want_probs=True)
+    d_from_p = np.sum(p * (dout @ v.T), axis=1)
+    assert np.allclose(np.sum(dout * o, axis=1), d_from_p, rtol=1e-12, atol=1e-12)
+    # dV is linear in dO with the probabilities as weights: dV = P^T dO
+    assert np.allclose(dv, p.T @ dout, rtol=1e-12, atol=1e-12)
+
+
+def test_bwd_planted_mistakes_are_caught():
+    N, d = 5, 3
+    q, k, v, dout = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+    a = 0.8
+    fd = _fd_grads(q, k, v, dout, a, True)
+    assert _fd_agrees(oracle.attention_bwd_head(q, k, v, dout, a, True), fd)
+    # swapped K and V
+    assert not _fd_agrees(oracle.attention_bwd_head(q, v, k, dout, a, True), fd)
+    # dO and V exchanged (dP built from the wrong operand)
+    assert not _fd_agrees(oracle.attention_bwd_head(q, k, dout, v, a, True), fd)
+    # scale dropped
+    assert not _fd_agrees(oracle.attention_bwd_head(q, k, v, dout, 1.0, True), fd)
+    # mask ignored
+    assert not _fd_agrees(oracle.attention_bwd_head(q, k, v, dout, a, False), fd)
