@@ -29,7 +29,7 @@ FA_BF16 = 0
 FA_FP16 = 1
 
 # Every symbol include/fa.h declares (checked by the tests).
-EXPORTS = ("fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_check_status",
+EXPORTS = ("fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_check_status",
            "fa_status_detail", "fa_status_string", "fa_version")
 
 _lib = None
@@ -58,6 +58,8 @@ def load():
     lib.fa_quantize_fp8.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd_fp8.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    lib.fa_bwd.restype = i
     lib.fa_check_status.argtypes = [vp]
     lib.fa_check_status.restype = i
     lib.fa_status_detail.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -147,6 +149,38 @@ def attention_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False,
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_fp8")
     return out, lse
+
+
+def fa_bwd(q, k, v, o, dout, lse, delta, dq, dk, dv, B: int, H: int, N: int, d: int,
+           alpha: float, causal: int, dtype: int, stream=None) -> int:
+    """Direct call of the C entry point (see include/fa.h)."""
+    return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                         _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N),
+                         int(d), float(alpha), int(causal), int(dtype), _stream(stream))
+
+
+def attention_backward(q, k, v, o, lse, dout, causal: bool = False,
+                       alpha: float | None = None, stream=None):
+    """Gradients (dQ, dK, dV) for torch tensors on the GPU; ``o`` and ``lse``
+    come from ``attention`` on the same inputs.  Allocates the outputs and
+    the D workspace with torch; raises FaError on a non-OK status."""
+    import torch
+    if q.dtype == torch.bfloat16:
+        dt = FA_BF16
+    elif q.dtype == torch.float16:
+        dt = FA_FP16
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    B, N, H, d = q.shape
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    delta = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = fa_bwd(q, k, v, o, dout, lse, delta, dq, dk, dv, B, H, N, d, alpha,
+                int(bool(causal)), dt, stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+    return dq, dk, dv
 
 
 def fa_check_status(stream=None) -> int:

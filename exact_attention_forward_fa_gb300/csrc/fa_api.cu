@@ -258,6 +258,70 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                 const float *lse, float *delta, void *dq, void *dk, void *dv, int B, int H,
+                 int N, int d, float alpha, int causal, fa_dtype dtype, void *stream) {
+    // ---- host-side validation: nothing is launched on failure ----
+    if (!q || !k || !v || !o || !dout || !lse || !delta || !dq || !dk || !dv)
+        return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return FA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(delta) & 3u))
+        return FA_ERR_MISALIGNED;
+    const uint64_t batch_stride = 2ull * d * H * static_cast<uint64_t>(N);
+    if (batch_stride >= (1ull << 40)) return FA_ERR_TOO_LARGE;
+    const uint64_t n_t = (static_cast<uint64_t>(N) + 127) / 128;
+    const uint64_t units = static_cast<uint64_t>(B) * H * n_t;
+    const uint64_t rows = static_cast<uint64_t>(B) * H * N;
+    if (units > 0x7fffffffull || rows > 0x7fffffffffffull) return FA_ERR_TOO_LARGE;
+
+    DeviceInfo *dev = nullptr;
+    fa_status st = get_device(&dev);
+    if (st != FA_OK) return st;
+
+    fa::BwdLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const CUtensorMapDataType dt =
+        dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if ((st = encode_bshd(&L.q, q, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.k, k, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.v, v, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.dout, dout, dt, B, H, N, d, 128)) != FA_OK) return st;
+    L.args.lse = lse;
+    L.args.delta = delta;
+    L.args.o = o;
+    L.args.dout = dout;
+    L.args.dq = dq;
+    L.args.dk = dk;
+    L.args.dv = dv;
+    L.args.status = dev->status;
+    L.args.B = B;
+    L.args.H = H;
+    L.args.N = N;
+    L.args.n_t = static_cast<int>(n_t);
+    L.args.n_units = static_cast<int>(units);
+    L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
+    L.args.alpha = alpha;
+    L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
+    // preprocess: 8 warps per CTA, each warp 4 passes of 32*8/d rows
+    const uint64_t rows_per_cta = 8ull * 4ull * (256ull / static_cast<uint64_t>(d));
+    const uint64_t gd = (rows + rows_per_cta - 1) / rows_per_cta;
+    const uint64_t gcap = 8ull * static_cast<uint64_t>(dev->sm_count);
+    L.grid_delta = static_cast<int>(gd < gcap ? gd : gcap);
+    L.d = d;
+    L.causal = causal != 0;
+    L.bf16 = dtype == FA_BF16;
+    L.stream = static_cast<cudaStream_t>(stream);
+    cudaError_t e = fa::launch_bwd(L);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 fa_status fa_check_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
     DeviceInfo *dev = nullptr;

@@ -1,0 +1,820 @@
+// fa_bwd_kernel.cuh -- gradients of exact attention (dQ, dK, dV) on sm_103a.
+//
+// "FlashAttention-3 on Hopper", ch. 7 (the backward pass):
+//   sec. 7.1   S = alpha Q K^T, P = softmax(S) recomputed from the forward's
+//              LSE as P = exp2(S alpha log2e - LSE log2e) (no running max:
+//              the exponent is log P <= 0); dV = P^T dO; dP = dO V^T;
+//              dS = P o (dP - D) with D_i = rowsum(dO_i o O_i);
+//              dQ = alpha dS K; dK = alpha dS^T Q.
+//   sec. 7.2   KV-parallel ownership for dK, dV (a CTA owns one key tile and
+//              visits the query tiles; causal: from the diagonal on).  Of
+//              the section's three ways to produce dQ across key tiles, this
+//              file takes the first: a second, query-parallel kernel that
+//              recomputes S and dP for its query tile and accumulates dQ in
+//              TMEM.  On GB300 the KV-parallel kernel's TMEM is full with
+//              S^T, dP^T, dV and dK at d = 128 (512 columns) and its shared
+//              memory with K, V and two Q/dO stages, so a dQ accumulator or
+//              an FP32 dQ staging tile has no room; the second kernel needs
+//              no atomics, no FP32 workspace and gives identical bits on
+//              every run.
+//   sec. 7.3   the preprocessing pass computes D.
+//
+// Both main kernels: 192 threads -- warps 0-3 the elementwise group (one
+// thread per TMEM lane = tile row), warp 4 the TMA producer, warp 5 the MMA
+// issuer (converged warp, elected lane).  All GEMMs are tcgen05.mma
+// kind::f16 with FP32 accumulation in TMEM; P and dS are rounded to the
+// input's 16-bit type for the GEMMs that consume them.  Every mbarrier wait
+// is bounded and reports through the device status word.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fa_device.cuh"
+
+namespace fa {
+
+struct BwdArgs {
+    const float *lse;      // [B][H][N], natural log, from the forward
+    float *delta;          // [B][H][N] D_i = rowsum(dO_i o O_i)
+    const void *o;         // [B][N][H][d] forward output (preprocess only)
+    const void *dout;      // [B][N][H][d] upstream gradient (preprocess only)
+    void *dq, *dk, *dv;    // [B][N][H][d] outputs, input dtype
+    uint32_t *status;
+    int B, H, N;
+    int n_t;               // 128-row tiles per sequence
+    int n_units;           // B * H * n_t
+    float scale_log2;      // alpha * log2(e)
+    float alpha;
+};
+
+template <int D, bool kBF16>
+struct BwdCfg {
+    static_assert(D == 64 || D == 128, "head dim");
+    static constexpr int NCH = D / 64;                   // 128-byte column chunks
+    static constexpr uint32_t CHUNK = 128u * 128u;       // 128 rows x 128 B
+    static constexpr uint32_t TILE = NCH * CHUNK;        // one 128 x D tile
+    static constexpr int NTHREADS = 192;
+    static constexpr uint32_t TMEM_COLS = 512;
+    // S = Q K^T style: both operands K-major, M = N = 128
+    static constexpr uint32_t IDESC_SS = idesc_f16(128, 128, kBF16, false, false);
+    // (.) x B with B MN-major, N = D (P V style)
+    static constexpr uint32_t IDESC_ACC = idesc_f16(128, D, kBF16, false, true);
+    static constexpr int QK_STEPS = D / 16;              // K = D in steps of 16
+    static constexpr int ACC_STEPS = 128 / 16;           // K = 128 rows in steps of 16
+
+    // ---- dQ kernel: Q, dO resident per unit; ring of K / V tiles ----
+    static constexpr int DQ_NSTAGE = D == 128 ? 5 : 10;
+    static constexpr uint32_t DQ_Q_OFF = 0, DQ_DO_OFF = TILE, DQ_KV_OFF = 2 * TILE;
+    static constexpr uint32_t DQ_BAR_OFF = DQ_KV_OFF + DQ_NSTAGE * TILE;
+    static constexpr int DQB_QFULL = 0, DQB_QEMPTY = 1, DQB_SFULL = 2, DQB_DPFULL = 3,
+                         DQB_SFREE = 4, DQB_DSFULL = 5 /* x2 */, DQB_DQFULL = 7,
+                         DQB_DQEMPTY = 8, DQB_MMADONE = 9, DQB_KVFULL = 10,
+                         DQB_KVEMPTY = 10 + DQ_NSTAGE, DQ_NBAR = 10 + 2 * DQ_NSTAGE;
+    static constexpr uint32_t DQ_MISC_OFF = DQ_BAR_OFF + DQ_NBAR * 8;
+    static constexpr uint32_t DQ_SMEM = DQ_MISC_OFF + 16 + 1024;
+    // TMEM: S [0,128), dP [128,256), dQ [256,256+D), dS0, dS1 (64 columns each)
+    static constexpr uint32_t DQ_COL_S = 0, DQ_COL_DP = 128, DQ_COL_DQ = 256,
+                              DQ_COL_DS = 256 + D;
+    static_assert(DQ_COL_DS + 128 <= TMEM_COLS, "dQ kernel TMEM budget");
+
+    // ---- dK/dV kernel: K, V resident per unit; ring of (Q, dO, LSE, D) ----
+    static constexpr int KV_NSTAGE = D == 128 ? 2 : 4;
+    static constexpr uint32_t VEC_BYTES = 2u * 128u * 4u;          // lse2[128], D[128]
+    static constexpr uint32_t STAGE = 2 * TILE + VEC_BYTES;        // Q, dO, vectors
+    static constexpr uint32_t KV_K_OFF = 0, KV_V_OFF = TILE, KV_RING_OFF = 2 * TILE;
+    static constexpr uint32_t KV_BAR_OFF = KV_RING_OFF + KV_NSTAGE * STAGE;
+    static constexpr int KVB_KVFULL = 0, KVB_KVEMPTY = 1, KVB_STFULL = 2, KVB_DPTFULL = 3,
+                         KVB_PFULL = 4, KVB_DSFULL = 5, KVB_ACCFULL = 6, KVB_ACCEMPTY = 7,
+                         KVB_MMADONE = 8, KVB_QFULL = 9, KVB_QEMPTY = 9 + KV_NSTAGE,
+                         KV_NBAR = 9 + 2 * KV_NSTAGE;
+    static constexpr uint32_t KV_MISC_OFF = KV_BAR_OFF + KV_NBAR * 8;
+    static constexpr uint32_t KV_SMEM = KV_MISC_OFF + 16 + 1024;
+    // TMEM: S^T [0,128) (P^T over its first 64), dP^T [128,256) (dS^T over
+    // its first 64), dV [256,256+D), dK [256+D,256+2D)
+    static constexpr uint32_t KV_COL_ST = 0, KV_COL_DPT = 128, KV_COL_DV = 256,
+                              KV_COL_DK = 256 + D;
+    static_assert(KV_COL_DK + D <= TMEM_COLS, "dK/dV kernel TMEM budget");
+    static_assert(DQ_SMEM <= 232448 && KV_SMEM <= 232448, "shared memory");
+};
+
+// Work unit: one 128-row tile (queries for dQ, keys for dK/dV) of one (b, h).
+// Causal: the longest units first (dQ: the last query tiles; dK/dV: the
+// first key tiles).
+struct BwdUnit {
+    int b, h, m;
+};
+
+template <bool kCausal, bool kKeyTiles>
+__device__ __forceinline__ BwdUnit make_bwd_unit(int u, const BwdArgs &a) {
+    BwdUnit U;
+    const int BH = a.B * a.H;
+    int bh;
+    if (kCausal) {
+        const int k = u / BH;
+        U.m = kKeyTiles ? k : a.n_t - 1 - k;
+        bh = u % BH;
+    } else {
+        U.m = u % a.n_t;
+        bh = u / a.n_t;
+    }
+    U.b = bh / a.H;
+    U.h = bh % a.H;
+    return U;
+}
+
+// ---------------------------------------------------------------------------
+// Preprocess: D[b][h][n] = sum_c dO[b][n][h][c] * O[b][n][h][c] in FP32
+// ("FlashAttention-3 on Hopper", sec. 7.1.2 and 7.3).  HBM-bound: reads
+// 2 x 2 B per element.  A row of D elements is read by D/8 threads with
+// 16-byte loads; each thread handles 4 rows per pass for memory parallelism.
+// ---------------------------------------------------------------------------
+template <int D, bool kBF16>
+__global__ void __launch_bounds__(256)
+fa_bwd_delta_kernel(const BwdArgs a) {
+    constexpr int TPR = D / 8;                       // threads per row
+    constexpr int RPW = 32 / TPR;                    // rows per warp pass
+    const long n_rows = static_cast<long>(a.B) * a.N * a.H;
+    const int lane = threadIdx.x & 31;
+    const long warp_g = (static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const long n_warps = (static_cast<long>(gridDim.x) * blockDim.x) >> 5;
+    const int sub = lane / TPR, part = lane % TPR;
+    const uint4 *o4 = reinterpret_cast<const uint4 *>(a.o);
+    const uint4 *d4 = reinterpret_cast<const uint4 *>(a.dout);
+    for (long base = warp_g * RPW * 4; base < n_rows; base += n_warps * RPW * 4) {
+        uint4 ov[4], dv[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const long row = base + r * RPW + sub;
+            ov[r] = make_uint4(0u, 0u, 0u, 0u);
+            dv[r] = ov[r];
+            if (row < n_rows) {
+                ov[r] = o4[row * TPR + part];
+                dv[r] = d4[row * TPR + part];
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t ow[4] = {ov[r].x, ov[r].y, ov[r].z, ov[r].w};
+            const uint32_t dw[4] = {dv[r].x, dv[r].y, dv[r].z, dv[r].w};
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float o0, o1, g0, g1;
+                unpack2<kBF16>(ow[i], o0, o1);
+                unpack2<kBF16>(dw[i], g0, g1);
+                acc = fmaf(o0, g0, acc);
+                acc = fmaf(o1, g1, acc);
+            }
+#pragma unroll
+            for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+            const long row = base + r * RPW + sub;
+            if (part == 0 && row < n_rows) {
+                // row = (b * N + n) * H + h
+                const long h = row % a.H;
+                const long bn = row / a.H;
+                const long n = bn % a.N, b = bn / a.N;
+                a.delta[(b * a.H + h) * a.N + n] = acc;
+            }
+        }
+    }
+}
+
+// Shared helpers of the two main kernels -----------------------------------
+
+// One TMA tile (128 rows x D, 128-byte swizzled chunks) of a [B][N][H][d] map.
+template <int NCH>
+__device__ __forceinline__ void load_tile(const CUtensorMap *m, uint32_t dst, uint32_t bar,
+                                          int h, int row0, int b) {
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+        tma_load_4d(m, dst + c * 128u * 128u, bar, c * 64, h, row0, b);
+}
+
+// 16-bit A x B^T over the full K = D: both tiles K-major (S = Q K^T style).
+template <int D>
+__device__ __forceinline__ void gemm_ss_kmajor(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+                                               uint32_t idesc) {
+    const uint64_t ad = smem_desc_sw128(a_smem, 16u, 1024u);
+    const uint64_t bd = smem_desc_sw128(b_smem, 16u, 1024u);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * 128u * 128u + (kk & 3) * 32u) >> 4;
+        mma_ss_f16_elect(d_tmem, ad + off, bd + off, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+// D += A B with A (128 x 128, 16-bit) in TMEM and B (128 rows x D) an
+// MN-major shared-memory tile (P V style).
+__device__ __forceinline__ void gemm_ts_mn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                           uint32_t idesc, bool accumulate) {
+    const uint64_t bd = smem_desc_sw128(b_smem, 128u * 128u, 1024u);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+        mma_ts_f16_elect(d_tmem, a_tmem + kk * 8u, bd + ((kk * 2048u) >> 4), idesc,
+                         (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Epilogue row store: v (D FP32 values of one row) * scale -> 16 bit.
+template <int D, bool kBF16>
+__device__ __forceinline__ void store_row(void *dst_base, const BwdArgs &a, int b, int h,
+                                          int row, const uint32_t (&v)[D], float scale) {
+    if (row >= a.N) return;
+    uint16_t *dst = reinterpret_cast<uint16_t *>(dst_base) +
+                    ((static_cast<size_t>(b) * a.N + row) * a.H + h) * D;
+#pragma unroll
+    for (int ch = 0; ch < D / 8; ++ch) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            pk[i] = pack2<kBF16>(__uint_as_float(v[8 * ch + 2 * i]) * scale,
+                                 __uint_as_float(v[8 * ch + 2 * i + 1]) * scale);
+        reinterpret_cast<uint4 *>(dst)[ch] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dQ kernel (query-parallel).  Per key tile t of the unit's query tile:
+//   S(t) = Q K_t^T, dP(t) = dO V_t^T          (TMEM S, dP)
+//   P = exp2(S c - LSE2), dS = P o (dP - D)   (elementwise group; P in
+//                                              registers, dS -> TMEM dS[t%2])
+//   dQ += dS(t) K_t                           (TMEM dQ; K_t MN-major)
+// MMA order: S(0), dP(0), then for each t: [S consumed] S(t+1);
+// [dS(t) ready] dP(t+1), dQ(t).  The exponentials of tile t+1 overlap dQ(t)
+// and dP(t+1); dS is double-buffered so dQ(t) reads dS(t) while dS(t+1) is
+// written.
+// ---------------------------------------------------------------------------
+template <int D, bool kCausal, bool kBF16>
+__global__ void __launch_bounds__(192, 1)
+fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                 const BwdArgs a) {
+    using C = BwdCfg<D, kBF16>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    auto bar = [&](int i) -> uint32_t { return base + C::DQ_BAR_OFF + 8u * i; };
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF + 4);
+    auto n_key_tiles = [&](const BwdUnit &U) { return kCausal ? U.m + 1 : a.n_t; };
+
+    if (warp == 5) tmem_alloc(base + C::DQ_MISC_OFF, C::TMEM_COLS);
+    if (tid == 0) {
+        *abort_flag = 0u;
+        mbar_init(bar(C::DQB_QFULL), 1);
+        mbar_init(bar(C::DQB_QEMPTY), 1);
+        mbar_init(bar(C::DQB_SFULL), 1);
+        mbar_init(bar(C::DQB_DPFULL), 1);
+        mbar_init(bar(C::DQB_SFREE), 4);
+        mbar_init(bar(C::DQB_DSFULL + 0), 4);
+        mbar_init(bar(C::DQB_DSFULL + 1), 4);
+        mbar_init(bar(C::DQB_DQFULL), 1);
+        mbar_init(bar(C::DQB_DQEMPTY), 4);
+        mbar_init(bar(C::DQB_MMADONE), 1);
+        for (int s = 0; s < C::DQ_NSTAGE; ++s) {
+            mbar_init(bar(C::DQB_KVFULL + s), 1);
+            mbar_init(bar(C::DQB_KVEMPTY + s), 1);
+        }
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 4) {
+        // =================== TMA producer (one lane) ===================
+        if (lane == 0) {
+            WaitCtx w{abort_flag, a.status, kRoleProducer};
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+            uint32_t slot = 0, phase = 0, armed = 0, armed_par = 0;
+            int qn = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+                const BwdUnit U = make_bwd_unit<kCausal, false>(u, a);
+                ok = mbar_wait(bar(C::DQB_QEMPTY), (qn & 1) ^ 1, w, 50);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar(C::DQB_QFULL), 2 * C::TILE);
+                load_tile<C::NCH>(&tm_q, base + C::DQ_Q_OFF, bar(C::DQB_QFULL), U.h, U.m * 128, U.b);
+                load_tile<C::NCH>(&tm_do, base + C::DQ_DO_OFF, bar(C::DQB_QFULL), U.h, U.m * 128, U.b);
+                ++qn;
+                const int T = n_key_tiles(U);
+                for (int t = 0; ok && t < T; ++t) {
+                    const int j = T - 1 - t;
+                    for (int kv = 0; kv < 2; ++kv) {      // K(t), then V(t)
+                        ok = mbar_wait(bar(C::DQB_KVEMPTY + slot), phase ^ 1, w, 51);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(bar(C::DQB_KVFULL + slot), C::TILE);
+                        load_tile<C::NCH>(kv ? &tm_v : &tm_k, base + C::DQ_KV_OFF + slot * C::TILE,
+                                          bar(C::DQB_KVFULL + slot), U.h, j * 128, U.b);
+                        armed |= 1u << slot;
+                        armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
+                        if (++slot == C::DQ_NSTAGE) { slot = 0; phase ^= 1; }
+                    }
+                }
+            }
+            for (int s = 0; s < C::DQ_NSTAGE; ++s)
+                if (armed & (1u << s))
+                    mbar_wait_quiet(bar(C::DQB_KVFULL + s), (armed_par >> s) & 1u, 500000000ull);
+            if (qn > 0) mbar_wait_quiet(bar(C::DQB_QFULL), (qn - 1) & 1, 500000000ull);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // =================== MMA issuer ===================
+        WaitCtx w{abort_flag, a.status, kRoleMma};
+        uint32_t kv_item = 0;               // ring items consumed so far
+        uint32_t qph = 0, sfree_ph = 0, ds_ph0 = 0, ds_ph1 = 0, dqe_ph = 0;
+        bool ok = true;
+        auto item = [&](uint32_t i, uint32_t &s, uint32_t &p) {
+            s = i % C::DQ_NSTAGE;
+            p = (i / C::DQ_NSTAGE) & 1u;
+        };
+        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            const BwdUnit U = make_bwd_unit<kCausal, false>(u, a);
+            const int T = n_key_tiles(U);
+            ok = mbar_wait_warp(bar(C::DQB_QFULL), qph, w, 60);
+            if (!ok) break;
+            qph ^= 1;
+            // S(0), dP(0)
+            uint32_t ks, kp, vs, vp;
+            item(kv_item + 0, ks, kp);
+            item(kv_item + 1, vs, vp);
+            ok = mbar_wait_warp(bar(C::DQB_KVFULL + ks), kp, w, 61) &&
+                 mbar_wait_warp(bar(C::DQB_KVFULL + vs), vp, w, 62);
+            if (!ok) break;
+            tc_fence_after();
+            gemm_ss_kmajor<D>(tbase + C::DQ_COL_S, base + C::DQ_Q_OFF,
+                              base + C::DQ_KV_OFF + ks * C::TILE, C::IDESC_SS);
+            mma_commit_elect(bar(C::DQB_SFULL));
+            gemm_ss_kmajor<D>(tbase + C::DQ_COL_DP, base + C::DQ_DO_OFF,
+                              base + C::DQ_KV_OFF + vs * C::TILE, C::IDESC_SS);
+            mma_commit_elect(bar(C::DQB_DPFULL));
+            mma_commit_elect(bar(C::DQB_KVEMPTY + vs));
+            if (T == 1) mma_commit_elect(bar(C::DQB_QEMPTY));
+            for (int t = 0; ok && t < T; ++t) {
+                uint32_t kts, ktp;
+                item(kv_item + 2 * t, kts, ktp);             // K(t) slot
+                // ---- S(t+1) once S(t) has been read ----
+                ok = mbar_wait_warp(bar(C::DQB_SFREE), sfree_ph, w, 63);
+                if (!ok) break;
+                sfree_ph ^= 1;
+                if (t + 1 < T) {
+                    item(kv_item + 2 * (t + 1), ks, kp);
+                    ok = mbar_wait_warp(bar(C::DQB_KVFULL + ks), kp, w, 64);
+                    if (!ok) break;
+                    tc_fence_after();
+                    gemm_ss_kmajor<D>(tbase + C::DQ_COL_S, base + C::DQ_Q_OFF,
+                                      base + C::DQ_KV_OFF + ks * C::TILE, C::IDESC_SS);
+                    mma_commit_elect(bar(C::DQB_SFULL));
+                }
+                // ---- dS(t) ready: dP(t+1), then dQ += dS(t) K(t) ----
+                const int b2 = t & 1;
+                ok = mbar_wait_warp(bar(C::DQB_DSFULL + b2), b2 ? ds_ph1 : ds_ph0, w, 65);
+                if (!ok) break;
+                if (b2) ds_ph1 ^= 1; else ds_ph0 ^= 1;
+                if (t + 1 < T) {
+                    item(kv_item + 2 * (t + 1) + 1, vs, vp);
+                    ok = mbar_wait_warp(bar(C::DQB_KVFULL + vs), vp, w, 66);
+                    if (!ok) break;
+                    tc_fence_after();
+                    gemm_ss_kmajor<D>(tbase + C::DQ_COL_DP, base + C::DQ_DO_OFF,
+                                      base + C::DQ_KV_OFF + vs * C::TILE, C::IDESC_SS);
+                    mma_commit_elect(bar(C::DQB_DPFULL));
+                    mma_commit_elect(bar(C::DQB_KVEMPTY + vs));
+                    if (t + 2 == T) mma_commit_elect(bar(C::DQB_QEMPTY));   // last use of Q, dO
+                }
+                if (t == 0) {
+                    ok = mbar_wait_warp(bar(C::DQB_DQEMPTY), dqe_ph ^ 1, w, 67);
+                    if (!ok) break;
+                    dqe_ph ^= 1;
+                }
+                tc_fence_after();
+                gemm_ts_mn(tbase + C::DQ_COL_DQ, tbase + C::DQ_COL_DS + b2 * 64u,
+                           base + C::DQ_KV_OFF + kts * C::TILE, C::IDESC_ACC, t > 0);
+                mma_commit_elect(bar(C::DQB_KVEMPTY + kts));
+            }
+            if (!ok) break;
+            mma_commit_elect(bar(C::DQB_DQFULL));
+            kv_item += 2 * T;
+        }
+        mma_commit_elect(bar(C::DQB_MMADONE));
+        mbar_wait_quiet(bar(C::DQB_MMADONE), 0, 500000000ull);
+        __syncwarp();
+    } else {
+        // =================== elementwise group (warps 0-3) ===================
+        const int row = tid;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        WaitCtx w{abort_flag, a.status, kRoleSoftmax0};
+        const float sl2 = a.scale_log2;
+        uint32_t sph = 0, dpph = 0, dqph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            const BwdUnit U = make_bwd_unit<kCausal, false>(u, a);
+            const int T = n_key_tiles(U);
+            const int grow = U.m * 128 + row;
+            // log2-domain LSE of this row (+inf hides rows beyond N and
+            // empty rows: their P is 0), and D of this row
+            float lse2 = INFINITY, drow = 0.f;
+            if (grow < a.N) {
+                const size_t idx = (static_cast<size_t>(U.b) * a.H + U.h) * a.N + grow;
+                const float l = a.lse[idx];
+                lse2 = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+                drow = a.delta[idx];
+            }
+            const float2 c2 = make_float2(sl2, sl2);
+            const float2 nl2 = make_float2(-lse2, -lse2);
+            for (int t = 0; t < T; ++t) {
+                const int j = T - 1 - t;
+                // ---- P(t) = exp2(S c - LSE2) from S(t) ----
+                ok = mbar_wait(bar(C::DQB_SFULL), sph, w, 70);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                sph ^= 1;
+                tc_fence_after();
+                uint32_t s[128];
+                const uint32_t tS = tbase + lane_off + C::DQ_COL_S;
+#pragma unroll
+                for (int c = 0; c < 128; c += 32)
+                    tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&s[c]));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::DQB_SFREE));
+                int lim = min(128, a.N - j * 128);              // keys beyond N
+                if (kCausal) lim = min(lim, grow - j * 128 + 1);
+                float *pf = reinterpret_cast<float *>(s);
+#pragma unroll
+                for (int c = 0; c < 128; c += 2) {
+                    const float2 x = __ffma2_rn(make_float2(pf[c], pf[c + 1]), c2, nl2);
+                    pf[c] = c < lim ? ex2_approx(x.x) : 0.f;
+                    pf[c + 1] = c + 1 < lim ? ex2_approx(x.y) : 0.f;
+                }
+                // ---- dS(t) = P o (dP - D) -> TMEM dS[t%2] ----
+                ok = mbar_wait(bar(C::DQB_DPFULL), dpph, w, 71);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                dpph ^= 1;
+                tc_fence_after();
+                const uint32_t tDP = tbase + lane_off + C::DQ_COL_DP;
+                const uint32_t tDS = tbase + lane_off + C::DQ_COL_DS + (t & 1) * 64u;
+                const float2 nd2 = make_float2(-drow, -drow);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t dp[32];
+                    tmem_ld32(tDP + ch * 32, dp);
+                    tmem_ld_wait();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 g = __fadd2_rn(
+                            make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), nd2);
+                        const float2 ds = __fmul2_rn(make_float2(pf[ch * 32 + i], pf[ch * 32 + i + 1]), g);
+                        pk[i / 2] = pack2<kBF16>(ds.x, ds.y);
+                    }
+                    tmem_st16(tDS + ch * 16, pk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::DQB_DSFULL + (t & 1)));
+            }
+            if (!ok) break;
+            // ---- epilogue: dQ * alpha -> global ----
+            ok = mbar_wait(bar(C::DQB_DQFULL), dqph, w, 72);
+            if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+            dqph ^= 1;
+            tc_fence_after();
+            uint32_t dq[D];
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch)
+                tmem_ld32(tbase + lane_off + C::DQ_COL_DQ + ch * 32,
+                          *reinterpret_cast<uint32_t(*)[32]>(&dq[ch * 32]));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::DQB_DQEMPTY));
+            store_row<D, kBF16>(a.dq, a, U.b, U.h, grow, dq, a.alpha);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dK/dV kernel (key-parallel).  The unit's key tile K, V stays in shared
+// memory; per query tile i (causal: i from the diagonal on):
+//   G1  S^T(i) = K Q_i^T,   G2  dP^T(i) = V dO_i^T        (TMEM S^T, dP^T)
+//   P^T = exp2(S^T c - LSE2[q]) -> 16 bit over S^T        (elementwise)
+//   G3  dV += P^T dO_i                                     (dO_i MN-major)
+//   dS^T = P^T o (dP^T - D[q]) -> 16 bit over dP^T         (elementwise)
+//   G4  dK += dS^T Q_i                                     (Q_i MN-major)
+// MMA order per tile: G3(i), G1(i+1), G4(i), G2(i+1), so the exponentials
+// of tile i+1 overlap G4(i) and G2(i+1), and dS(i+1) overlaps G3(i+1) and
+// G1(i+2).  The producer warp stages LSE2 and D of each query tile next to
+// Q_i and dO_i in the ring (LSE2 = +inf and D = 0 beyond N, which zero P).
+// ---------------------------------------------------------------------------
+template <int D, bool kCausal, bool kBF16>
+__global__ void __launch_bounds__(192, 1)
+fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdArgs a) {
+    using C = BwdCfg<D, kBF16>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *gbase = smem_raw + (base - raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    auto bar = [&](int i) -> uint32_t { return base + C::KV_BAR_OFF + 8u * i; };
+    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF);
+    volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF + 4);
+    auto first_q = [&](const BwdUnit &U) { return kCausal ? U.m : 0; };
+    auto stage_q = [&](int s) { return base + C::KV_RING_OFF + s * C::STAGE; };
+    auto stage_do = [&](int s) { return base + C::KV_RING_OFF + s * C::STAGE + C::TILE; };
+    auto stage_vec = [&](int s) { return gbase + C::KV_RING_OFF + s * C::STAGE + 2 * C::TILE; };
+
+    if (warp == 5) tmem_alloc(base + C::KV_MISC_OFF, C::TMEM_COLS);
+    if (tid == 0) {
+        *abort_flag = 0u;
+        mbar_init(bar(C::KVB_KVFULL), 1);
+        mbar_init(bar(C::KVB_KVEMPTY), 1);
+        mbar_init(bar(C::KVB_STFULL), 1);
+        mbar_init(bar(C::KVB_DPTFULL), 1);
+        mbar_init(bar(C::KVB_PFULL), 4);
+        mbar_init(bar(C::KVB_DSFULL), 4);
+        mbar_init(bar(C::KVB_ACCFULL), 1);
+        mbar_init(bar(C::KVB_ACCEMPTY), 4);
+        mbar_init(bar(C::KVB_MMADONE), 1);
+        for (int s = 0; s < C::KV_NSTAGE; ++s) {
+            mbar_init(bar(C::KVB_QFULL + s), 1);
+            mbar_init(bar(C::KVB_QEMPTY + s), 1);
+        }
+        fence_barrier_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    if (warp == 4) {
+        // =================== producer (whole warp: vectors; lane 0: TMA) ===================
+        WaitCtx w{abort_flag, a.status, kRoleProducer};
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_do);
+        }
+        uint32_t slot = 0, phase = 0, armed = 0, armed_par = 0;
+        int kvn = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
+            ok = mbar_wait_warp(bar(C::KVB_KVEMPTY), (kvn & 1) ^ 1, w, 80);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bar(C::KVB_KVFULL), 2 * C::TILE);
+                load_tile<C::NCH>(&tm_k, base + C::KV_K_OFF, bar(C::KVB_KVFULL), U.h, U.m * 128, U.b);
+                load_tile<C::NCH>(&tm_v, base + C::KV_V_OFF, bar(C::KVB_KVFULL), U.h, U.m * 128, U.b);
+            }
+            ++kvn;
+            const size_t vbase = (static_cast<size_t>(U.b) * a.H + U.h) * a.N;
+            for (int i = first_q(U); ok && i < a.n_t; ++i) {
+                ok = mbar_wait_warp(bar(C::KVB_QEMPTY + slot), phase ^ 1, w, 81);
+                if (!ok) break;
+                // LSE2 and D of the 128 query rows of tile i, 4 per lane
+                float *vec = reinterpret_cast<float *>(stage_vec(slot));
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int q = i * 128 + r * 32 + lane;
+                    float l2 = INFINITY, dd = 0.f;
+                    if (q < a.N) {
+                        const float l = a.lse[vbase + q];
+                        l2 = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+                        dd = a.delta[vbase + q];
+                    }
+                    vec[r * 32 + lane] = l2;
+                    vec[128 + r * 32 + lane] = dd;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar(C::KVB_QFULL + slot), 2 * C::TILE);
+                    load_tile<C::NCH>(&tm_q, stage_q(slot), bar(C::KVB_QFULL + slot), U.h, i * 128, U.b);
+                    load_tile<C::NCH>(&tm_do, stage_do(slot), bar(C::KVB_QFULL + slot), U.h, i * 128, U.b);
+                }
+                armed |= 1u << slot;
+                armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
+                if (++slot == C::KV_NSTAGE) { slot = 0; phase ^= 1; }
+            }
+        }
+        if (lane == 0) {
+            for (int s = 0; s < C::KV_NSTAGE; ++s)
+                if (armed & (1u << s))
+                    mbar_wait_quiet(bar(C::KVB_QFULL + s), (armed_par >> s) & 1u, 500000000ull);
+            if (kvn > 0) mbar_wait_quiet(bar(C::KVB_KVFULL), (kvn - 1) & 1, 500000000ull);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // =================== MMA issuer ===================
+        WaitCtx w{abort_flag, a.status, kRoleMma};
+        uint32_t q_item = 0, kvph = 0, pph = 0, dsph = 0, accph = 0;
+        bool ok = true;
+        auto item = [&](uint32_t i, uint32_t &s, uint32_t &p) {
+            s = i % C::KV_NSTAGE;
+            p = (i / C::KV_NSTAGE) & 1u;
+        };
+        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
+            const int Ti = a.n_t - first_q(U);
+            ok = mbar_wait_warp(bar(C::KVB_KVFULL), kvph, w, 90);
+            if (!ok) break;
+            kvph ^= 1;
+            uint32_t s0, p0;
+            item(q_item, s0, p0);
+            ok = mbar_wait_warp(bar(C::KVB_QFULL + s0), p0, w, 91);
+            if (!ok) break;
+            tc_fence_after();
+            gemm_ss_kmajor<D>(tbase + C::KV_COL_ST, base + C::KV_K_OFF, stage_q(s0), C::IDESC_SS);
+            mma_commit_elect(bar(C::KVB_STFULL));
+            gemm_ss_kmajor<D>(tbase + C::KV_COL_DPT, base + C::KV_V_OFF, stage_do(s0), C::IDESC_SS);
+            mma_commit_elect(bar(C::KVB_DPTFULL));
+            for (int k = 0; ok && k < Ti; ++k) {
+                uint32_t sc, pc, sn = 0, pn = 0;
+                item(q_item + k, sc, pc);
+                const bool more = k + 1 < Ti;
+                if (more) item(q_item + k + 1, sn, pn);
+                // ---- G3: dV += P^T dO_i ----
+                ok = mbar_wait_warp(bar(C::KVB_PFULL), pph, w, 92);
+                if (ok && k == 0) ok = mbar_wait_warp(bar(C::KVB_ACCEMPTY), accph ^ 1, w, 93);
+                if (!ok) break;
+                pph ^= 1;
+                if (k == 0) accph ^= 1;
+                tc_fence_after();
+                gemm_ts_mn(tbase + C::KV_COL_DV, tbase + C::KV_COL_ST, stage_do(sc), C::IDESC_ACC, k > 0);
+                // ---- G1(i+1) ----
+                if (more) {
+                    ok = mbar_wait_warp(bar(C::KVB_QFULL + sn), pn, w, 94);
+                    if (!ok) break;
+                    tc_fence_after();
+                    gemm_ss_kmajor<D>(tbase + C::KV_COL_ST, base + C::KV_K_OFF, stage_q(sn), C::IDESC_SS);
+                    mma_commit_elect(bar(C::KVB_STFULL));
+                }
+                // ---- G4: dK += dS^T Q_i ----
+                ok = mbar_wait_warp(bar(C::KVB_DSFULL), dsph, w, 95);
+                if (!ok) break;
+                dsph ^= 1;
+                tc_fence_after();
+                gemm_ts_mn(tbase + C::KV_COL_DK, tbase + C::KV_COL_DPT, stage_q(sc), C::IDESC_ACC, k > 0);
+                mma_commit_elect(bar(C::KVB_QEMPTY + sc));
+                // ---- G2(i+1) ----
+                if (more) {
+                    gemm_ss_kmajor<D>(tbase + C::KV_COL_DPT, base + C::KV_V_OFF, stage_do(sn), C::IDESC_SS);
+                    mma_commit_elect(bar(C::KVB_DPTFULL));
+                }
+            }
+            if (!ok) break;
+            mma_commit_elect(bar(C::KVB_ACCFULL));
+            mma_commit_elect(bar(C::KVB_KVEMPTY));
+            q_item += Ti;
+        }
+        mma_commit_elect(bar(C::KVB_MMADONE));
+        mbar_wait_quiet(bar(C::KVB_MMADONE), 0, 500000000ull);
+        __syncwarp();
+    } else {
+        // =================== elementwise group (warps 0-3) ===================
+        const int row = tid;                       // key row of the tile
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        WaitCtx w{abort_flag, a.status, kRoleSoftmax0};
+        const float sl2 = a.scale_log2;
+        const float2 c2 = make_float2(sl2, sl2);
+        uint32_t stph = 0, dpph = 0, accph = 0, q_item = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
+            const int i0 = first_q(U);
+            const int Ti = a.n_t - i0;
+            const int krow = U.m * 128 + row;
+            for (int k = 0; k < Ti; ++k) {
+                const int i = i0 + k;
+                const int sc = static_cast<int>((q_item + k) % C::KV_NSTAGE);
+                const uint32_t scp = ((q_item + k) / C::KV_NSTAGE) & 1u;
+                const float *vec = reinterpret_cast<const float *>(stage_vec(sc));
+                // ---- P^T = exp2(S^T c - LSE2[q]) ----
+                // The stage's full phase (already complete for the MMA warp)
+                // orders the producer's stores of LSE2 and D before the reads
+                // below; it cannot advance before this tile's G4 releases it.
+                ok = mbar_wait(bar(C::KVB_QFULL + sc), scp, w, 103) &&
+                     mbar_wait(bar(C::KVB_STFULL), stph, w, 100);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                stph ^= 1;
+                tc_fence_after();
+                uint32_t s[128];
+                const uint32_t tST = tbase + lane_off + C::KV_COL_ST;
+#pragma unroll
+                for (int c = 0; c < 128; c += 32)
+                    tmem_ld32(tST + c, *reinterpret_cast<uint32_t(*)[32]>(&s[c]));
+                tmem_ld_wait();
+                // causal: query column q sees this key row iff krow <= q
+                const int lo = kCausal ? krow - i * 128 : 0;   // first visible column
+                float *pf = reinterpret_cast<float *>(s);
+                uint32_t pk[64];
+#pragma unroll
+                for (int c = 0; c < 128; c += 4) {
+                    const float4 l4 = *reinterpret_cast<const float4 *>(vec + c);
+                    const float2 x01 = __ffma2_rn(make_float2(pf[c], pf[c + 1]), c2,
+                                                  make_float2(-l4.x, -l4.y));
+                    const float2 x23 = __ffma2_rn(make_float2(pf[c + 2], pf[c + 3]), c2,
+                                                  make_float2(-l4.z, -l4.w));
+                    pf[c + 0] = c + 0 >= lo ? ex2_approx(x01.x) : 0.f;
+                    pf[c + 1] = c + 1 >= lo ? ex2_approx(x01.y) : 0.f;
+                    pf[c + 2] = c + 2 >= lo ? ex2_approx(x23.x) : 0.f;
+                    pf[c + 3] = c + 3 >= lo ? ex2_approx(x23.y) : 0.f;
+                    pk[c / 2] = pack2<kBF16>(pf[c], pf[c + 1]);
+                    pk[c / 2 + 1] = pack2<kBF16>(pf[c + 2], pf[c + 3]);
+                }
+                tmem_st32(tST + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+                tmem_st32(tST + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::KVB_PFULL));
+                // ---- dS^T = P^T o (dP^T - D[q]) ----
+                ok = mbar_wait(bar(C::KVB_DPTFULL), dpph, w, 101);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                dpph ^= 1;
+                tc_fence_after();
+                const uint32_t tDPT = tbase + lane_off + C::KV_COL_DPT;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t dp[32];
+                    tmem_ld32(tDPT + ch * 32, dp);
+                    tmem_ld_wait();
+                    uint32_t dk[16];
+#pragma unroll
+                    for (int t4 = 0; t4 < 32; t4 += 4) {
+                        const int c = ch * 32 + t4;
+                        const float4 d4 = *reinterpret_cast<const float4 *>(vec + 128 + c);
+                        const float2 g01 = __fadd2_rn(
+                            make_float2(__uint_as_float(dp[t4]), __uint_as_float(dp[t4 + 1])),
+                            make_float2(-d4.x, -d4.y));
+                        const float2 g23 = __fadd2_rn(
+                            make_float2(__uint_as_float(dp[t4 + 2]), __uint_as_float(dp[t4 + 3])),
+                            make_float2(-d4.z, -d4.w));
+                        const float2 ds01 = __fmul2_rn(make_float2(pf[c], pf[c + 1]), g01);
+                        const float2 ds23 = __fmul2_rn(make_float2(pf[c + 2], pf[c + 3]), g23);
+                        dk[t4 / 2] = pack2<kBF16>(ds01.x, ds01.y);
+                        dk[t4 / 2 + 1] = pack2<kBF16>(ds23.x, ds23.y);
+                    }
+                    tmem_st16(tDPT + ch * 16, dk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::KVB_DSFULL));
+            }
+            if (!ok) break;
+            q_item += Ti;
+            // ---- epilogue: dV, dK * alpha -> global ----
+            ok = mbar_wait(bar(C::KVB_ACCFULL), accph, w, 102);
+            if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+            accph ^= 1;
+            tc_fence_after();
+            uint32_t acc[D];
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch)
+                tmem_ld32(tbase + lane_off + C::KV_COL_DV + ch * 32,
+                          *reinterpret_cast<uint32_t(*)[32]>(&acc[ch * 32]));
+            tmem_ld_wait();
+            store_row<D, kBF16>(a.dv, a, U.b, U.h, krow, acc, 1.f);
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch)
+                tmem_ld32(tbase + lane_off + C::KV_COL_DK + ch * 32,
+                          *reinterpret_cast<uint32_t(*)[32]>(&acc[ch * 32]));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::KVB_ACCEMPTY));
+            store_row<D, kBF16>(a.dk, a, U.b, U.h, krow, acc, a.alpha);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+}  // namespace fa

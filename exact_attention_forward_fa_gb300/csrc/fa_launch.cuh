@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa_bwd_kernel.cuh"
 #include "fa_fwd_1q_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
@@ -23,6 +24,20 @@ cudaError_t launch_fwd_d64(const FwdLaunch &L);
 cudaError_t launch_fwd_d128(const FwdLaunch &L);
 cudaError_t launch_fwd_d256(const FwdLaunch &L);   // K/V maps with 64-row boxes
 cudaError_t launch_fwd_fp8(const FwdLaunch &L);    // e4m3 maps, 128-byte boxes
+// Backward: maps {d, H, N, B} with box {64, 1, 128, 1} (128-byte swizzle)
+// for Q, K, V and dO; grid = persistent CTAs of both main kernels.
+struct BwdLaunch {
+    CUtensorMap q, k, v, dout;
+    BwdArgs args;
+    int grid;
+    int grid_delta;
+    int d;
+    bool causal;
+    bool bf16;
+    cudaStream_t stream;
+};
+cudaError_t launch_bwd(const BwdLaunch &L);
+
 // FP8 pre-pass: persistent CTAs over (b, h, 128-row tile); x arrives by
 // TMA (map {d, H, N, B}, box {d, 1, 128, 1}, no swizzle, rows >= N zero).
 struct QuantArgs {

@@ -90,7 +90,9 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
  *            the signs).  Use the same signs for Q and K, none for V: the
  *            product (QM)(KM)^T equals Q K^T because M is orthogonal.
  *   d in {64, 128, 256}.
- * codes = e4m3(y / scale), round to nearest even, saturating at +-448.
+ * codes = e4m3(y * (1/scale)) with the FP32 reciprocal formed once per tile
+ * (within one rounding of y / scale), round to nearest even, saturating at
+ * +-448.
  */
 fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
                           const float *hadamard_signs, int B, int H, int N, int d,
@@ -112,6 +114,33 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
                      const float *q_scale, const float *k_scale, const float *v_scale,
                      void *o, float *lse, int B, int H, int N, int d, float alpha,
                      int causal, void *stream);
+
+/*
+ * fa_bwd -- gradients of the attention of fa_fwd ("FlashAttention-3 on
+ * Hopper", ch. 7): with S = alpha Q K^T (masked as in fa_fwd),
+ * P = softmax(S) and O = P V, for the upstream gradient dO:
+ *   dV = P^T dO,  dP = dO V^T,  D_i = rowsum(dO_i o O_i),
+ *   dS = P o (dP - D),  dQ = alpha dS K,  dK = alpha dS^T Q.
+ * P is recomputed from Q, K and the forward's LSE (sec. 7.1.3).
+ *   q, k, v, o, dout : device, dtype [B][N][H][d], 16-byte aligned; o and
+ *            lse are the outputs of fa_fwd on the same q, k, v, alpha and
+ *            causal.
+ *   lse    : device, float [B][H][N] (natural log, as fa_fwd writes it).
+ *   delta  : device, float [B][H][N], caller-owned workspace; receives D.
+ *   dq, dk, dv : device, dtype [B][N][H][d], 16-byte aligned (written).
+ *   d in {64, 128} (others return FA_ERR_UNSUPPORTED); alpha, causal,
+ *   dtype and stream as fa_fwd.
+ * Three kernels run in order on `stream`: the D preprocess, a key-parallel
+ * kernel for dK and dV and a query-parallel kernel for dQ that recomputes S
+ * and dP (sec. 7.2, first option), so no atomics are used and the results
+ * are identical from run to run.  P and dS are rounded to `dtype` for the
+ * GEMMs that consume them; accumulation is FP32; outputs are rounded to
+ * `dtype`.  Nothing is allocated.  Errors as fa_fwd.
+ */
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                 const void *dout, const float *lse, float *delta, void *dq,
+                 void *dk, void *dv, int B, int H, int N, int d, float alpha,
+                 int causal, fa_dtype dtype, void *stream);
 
 /*
  * fa_check_status -- synchronizes `stream`, then reports and clears the

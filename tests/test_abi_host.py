@@ -123,6 +123,33 @@ def test_fp8_validation_codes(lib, kw, code):
     assert _f8call(lib, **kw) == code
 
 
+def _bcall(lib, q=A, k=A, v=A, o=A, do=A, lse=A, delta=A, dq=A, dk=A, dv=A, B=1, H=1,
+           N=128, d=128, alpha=0.088, causal=0, dtype=0):
+    return lib.fa_bwd(q, k, v, o, do, lse, delta, dq, dk, dv, B, H, N, d, alpha, causal,
+                      dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(do=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(delta=None), fa.FA_ERR_INVALID_ARG),
+    (dict(dv=None), fa.FA_ERR_INVALID_ARG),
+    (dict(N=0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(alpha=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=3), fa.FA_ERR_INVALID_ARG),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(o=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(dk=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(delta=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(B=1 << 20, H=1 << 10, N=1 << 20, d=128), fa.FA_ERR_TOO_LARGE),
+])
+def test_bwd_validation_codes(lib, kw, code):
+    assert _bcall(lib, **kw) == code
+
+
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     import torch
     if torch.cuda.is_available():
