@@ -6,7 +6,7 @@ fixed seeds.  Metric: attention forward TFLOP/s = 4*B*H*N^2*d / time
 (halved for causal) and its percentage of the 2250 TFLOP/s dense BF16 peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--causal]
-                  [--impl ours|reference] [--skip-cpu]
+                  [--impl ours|reference] [--skip-cpu] [--fp8 | --bwd]
 
 The device-resident number times K back-to-back launches with CUDA events
 on the launching stream (inputs of 192 MiB exceed the 126 MB L2, so no
@@ -15,6 +15,9 @@ C ABI with pinned host buffers: host->device copies of Q/K/V, the launch and
 the device->host copy of O and LSE, every step.  ``cpu_baseline`` is the
 FP64 CPU oracle on a bounded sample of the same workload.
 ``--impl reference`` times that oracle alone, as the reference arm.
+``--fp8`` times the FP8 forward (the quantization pre-pass reported
+separately); ``--bwd`` times the backward (fa_bwd: dQ, dK, dV from O, LSE
+and dO), counting its FLOPs as 2.5x the forward's as the pages do.
 Under torchrun every rank runs the full workload on its own GPU (independent
 replicas, weak scaling, no collective on the data path).
 """
@@ -37,6 +40,9 @@ PEAK_SPEC = 2250.0          # TFLOP/s dense BF16, the metric's denominator
 METRIC = "attention fwd TFLOP/s (BF16, d=128) and % of 2250 TFLOP/s dense peak"
 METRIC_FP8 = "attention fwd TFLOP/s (FP8 e4m3, d=128) and % of 4500 TFLOP/s dense FP8 peak"
 PEAK_SPEC_FP8 = 4500.0
+METRIC_BWD = ("attention bwd TFLOP/s (BF16, d=128; FLOPs = 2.5 x forward) "
+              "and % of 2250 TFLOP/s dense peak")
+BWD_FACTOR = 2.5            # five GEMMs against the forward's two
 WORKLOAD = dict(B=4, H=16, N=4096, d=128)
 
 
@@ -197,8 +203,208 @@ def cpu_baseline(args, B, H, N, d):
             "sample": desc, "seconds": round(dt, 2)}
 
 
+def oracle_bwd_sample_rate(B, H, N, d, causal, rows, n_heads, threads):
+    """Times the FP64 gradient oracle on `n_heads` heads with the first `rows`
+    query rows (all keys).  Returns (TFLOP/s counted as 2.5x the forward's
+    FLOPs of those rows, seconds, description)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from exact_attention_forward_fa_gb300 import synth
+    alpha = synth.default_alpha(d)
+    heads = [(i // H % B, i % H) for i in range(n_heads)]
+    nb = max(b for b, _ in heads) + 1
+    q, k, v = synth.qkv(nb, H, N, d, seed=synth.BASE_SEED)
+    do = synth.normal((nb, N, H, d), seed=synth.BASE_SEED + 3)
+    rows = int(min(rows, N))
+    hq = [(oracle._f64(q[b, :rows, h]), oracle._f64(k[b, :, h]), oracle._f64(v[b, :, h]),
+           oracle._f64(do[b, :rows, h])) for b, h in heads]
+
+    def one(t):
+        oracle.attention_bwd_head(*t, alpha, causal)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, hq))
+    dt = time.perf_counter() - t0
+    vis = rows * (N - rows) + rows * (rows + 1) / 2 if causal else rows * N
+    fl = BWD_FACTOR * 4.0 * d * float(vis) * n_heads
+    desc = (f"{n_heads} heads x {rows} query rows (all keys) of B{B} H{H} N{N} d{d}"
+            f"{' causal' if causal else ''}, FP64 C gradient oracle")
+    return fl / dt / 1e12, dt, desc
+
+
+def run_bwd(args, B, H, N, d, rank, world):
+    """fa_bwd on the workload: O and LSE from one fa_fwd, then K timed
+    launches of the backward (three kernels each)."""
+    import torch
+    import torch.distributed as dist
+    import exact_attention_forward_fa_gb300 as fa
+    from exact_attention_forward_fa_gb300 import synth
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.load()
+    alpha = synth.default_alpha(d)
+    causal = int(args.causal)
+    qh, kh, vh = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + rank)
+    doh = torch.from_numpy(synth.normal((B, N, H, d), seed=synth.BASE_SEED + rank + 3)).to(qh.dtype)
+    q, k, v, do = qh.to(dev), kh.to(dev), vh.to(dev), doh.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty((fa.bwd_workspace_floats(B, H, N),), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    def fwd():
+        rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
+        if rc != fa.FA_OK:
+            raise fa.FaError(rc, "fa_fwd")
+
+    def launch():
+        rc = fa.fa_bwd(q, k, v, o, do, lse, ws, dq, dk, dv, B, H, N, d, alpha, causal,
+                       fa.FA_BF16, sp)
+        if rc != fa.FA_OK:
+            raise fa.FaError(rc, "fa_bwd")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        fwd()
+        for _ in range(args.warmup):
+            launch()
+    stream.synchronize()
+    if fa.fa_check_status(sp) != fa.FA_OK:
+        raise RuntimeError("device status after warm-up: " + str(fa.fa_status_detail()))
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(args.steps):
+                launch()
+            stop.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize(dev)
+        barrier()
+    ms_total = start.elapsed_time(stop)
+    if fa.fa_check_status(sp) != fa.FA_OK:
+        raise RuntimeError("device status after timing: " + str(fa.fa_status_detail()))
+    ms_max = reduce_max(ms_total, world, dev)
+    ms_step = ms_max / args.steps
+    fl = BWD_FACTOR * flops(B, H, N, d, args.causal)
+    value = aggregate_value(fl, args.steps, ms_max, world)
+
+    # ---- end to end: Q, K, V, O, dO, LSE in; dQ, dK, dV out, every step ----
+    pins = [x.pin_memory() for x in (qh, kh, vh)]
+    with torch.cuda.stream(stream):
+        fwd()
+    stream.synchronize()
+    op, lp, dop = o.cpu().pin_memory(), lse.cpu().pin_memory(), doh.pin_memory()
+    outs = [torch.empty(qh.shape, dtype=qh.dtype).pin_memory() for _ in range(3)]
+    e2e_steps = max(3, min(args.steps, 30))
+
+    def e2e_step():
+        for dst, src in zip((q, k, v, o, do, lse), (*pins, op, dop, lp)):
+            dst.copy_(src, non_blocking=True)
+        launch()
+        for dst, src in zip(outs, (dq, dk, dv)):
+            dst.copy_(src, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    stream.synchronize()
+    barrier()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        stop.record(stream)
+    stream.synchronize()
+    barrier()
+    e2e_ms = reduce_max(start.elapsed_time(stop), world, dev)
+    e2e_value = aggregate_value(fl, e2e_steps, e2e_ms, world)
+    h2d = 5 * qh.numel() * qh.element_size() + lse.numel() * 4
+    d2h = 3 * qh.numel() * qh.element_size()
+
+    if rank != 0:
+        return
+    burst, sustained, src = measured_peaks()
+    achieved = fl / (ms_step * 1e-3) / 1e12
+    if ms_max >= 1000.0 and sustained > 0:
+        peak, peak_kind = sustained, "sustained"
+    else:
+        peak, peak_kind = burst, "burst"
+    wkey = config_name(B, H, N, d, args.causal).replace("attention fwd", "attention bwd")
+    line = {
+        "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs and dO)",
+        "config": {"workload": wkey, "B": B, "H": H, "N": N, "d": d,
+                   "causal": bool(args.causal),
+                   "l2": "no flush: 320 MiB of inputs exceed the 126 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_2250": 100.0 * value / world / PEAK_SPEC,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "kernel": "fa_bwd step: D preprocess, dK/dV kernel, dQ kernel",
+                     "peak_source": f"{src} bf16 {peak_kind} (cuBLAS 8192^3)",
+                     "timed_region_ms": ms_max,
+                     "traffic": profiled_traffic(wkey)},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.skip_cpu:
+        threads = os.cpu_count() or 1
+        n0 = min(threads, B * H)
+        rate, dt, desc = oracle_bwd_sample_rate(B, H, N, d, args.causal, 256, n0, threads)
+        # scale the sample to ~20 s of host time: more query rows per head
+        rows = int(max(256, min(N, 256 * 20.0 / max(dt, 1e-3))))
+        rate, dt, desc = oracle_bwd_sample_rate(B, H, N, d, args.causal, rows, n0, threads)
+        line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, B, H, N, d, rank, world):
     if rank != 0:
+        return
+    if args.bwd:
+        threads = os.cpu_count() or 1
+        n0 = min(threads, B * H)
+        _, dt0, _ = oracle_bwd_sample_rate(B, H, N, d, args.causal, 16, n0, threads)
+        budget = 90.0 / max(1, args.steps + args.warmup)
+        rows = int(max(1, min(N, 16 * budget / max(dt0, 1e-6))))
+        for _ in range(args.warmup):
+            oracle_bwd_sample_rate(B, H, N, d, args.causal, rows, n0, threads)
+        rates, secs, desc = [], 0.0, ""
+        for _ in range(args.steps):
+            r, dt, desc = oracle_bwd_sample_rate(B, H, N, d, args.causal, rows, n0, threads)
+            rates.append(r)
+            secs += dt
+        value = float(np.median(rates))
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": config_name(B, H, N, d, args.causal).replace(
+                "attention fwd", "attention bwd"), "B": B,
+                       "H": H, "N": N, "d": d, "causal": args.causal},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "pct_of_2250": 100.0 * value / PEAK_SPEC}), flush=True)
         return
     threads = os.cpu_count() or 1
     rate0, dt0, _ = oracle_sample_rate(B, H, N, d, args.causal, 16, threads, threads)
@@ -406,6 +612,8 @@ def main():
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 e4m3 path (outlier inputs, Hadamard rotation); times "
                          "fa_fwd_fp8, reports the quantization pre-pass separately")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward pass (fa_bwd) instead of the forward")
     ap.add_argument("--skip-cpu", action="store_true",
                     help="omit the cpu_baseline leg (profiling runs)")
     ap.add_argument("--B", type=int, default=WORKLOAD["B"])
@@ -415,6 +623,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.bwd and args.fp8:
+        ap.error("--bwd and --fp8 are exclusive")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and args.impl == "ours":
@@ -423,6 +633,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, args.B, args.H, args.N, args.d, rank, world)
+        elif args.bwd:
+            run_bwd(args, args.B, args.H, args.N, args.d, rank, world)
         else:
             run_ours(args, args.B, args.H, args.N, args.d, rank, world)
     finally:

@@ -151,11 +151,16 @@ def attention_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False,
     return out, lse
 
 
-def fa_bwd(q, k, v, o, dout, lse, delta, dq, dk, dv, B: int, H: int, N: int, d: int,
+def bwd_workspace_floats(B: int, H: int, N: int) -> int:
+    """Size of fa_bwd's workspace: float [2][B][H][ceil(N/128)*128]."""
+    return 2 * B * H * ((N + 127) // 128) * 128
+
+
+def fa_bwd(q, k, v, o, dout, lse, workspace, dq, dk, dv, B: int, H: int, N: int, d: int,
            alpha: float, causal: int, dtype: int, stream=None) -> int:
     """Direct call of the C entry point (see include/fa.h)."""
     return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
-                         _ptr(delta), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N),
+                         _ptr(workspace), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N),
                          int(d), float(alpha), int(causal), int(dtype), _stream(stream))
 
 
@@ -163,7 +168,7 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False,
                        alpha: float | None = None, stream=None):
     """Gradients (dQ, dK, dV) for torch tensors on the GPU; ``o`` and ``lse``
     come from ``attention`` on the same inputs.  Allocates the outputs and
-    the D workspace with torch; raises FaError on a non-OK status."""
+    the workspace with torch; raises FaError on a non-OK status."""
     import torch
     if q.dtype == torch.bfloat16:
         dt = FA_BF16
@@ -175,8 +180,8 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False,
     if alpha is None:
         alpha = 1.0 / math.sqrt(d)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
-    delta = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    rc = fa_bwd(q, k, v, o, dout, lse, delta, dq, dk, dv, B, H, N, d, alpha,
+    ws = torch.empty((bwd_workspace_floats(B, H, N),), dtype=torch.float32, device=q.device)
+    rc = fa_bwd(q, k, v, o, dout, lse, ws, dq, dk, dv, B, H, N, d, alpha,
                 int(bool(causal)), dt, stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")

@@ -259,10 +259,10 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
 }
 
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
-                 const float *lse, float *delta, void *dq, void *dk, void *dv, int B, int H,
+                 const float *lse, float *workspace, void *dq, void *dk, void *dv, int B, int H,
                  int N, int d, float alpha, int causal, fa_dtype dtype, void *stream) {
     // ---- host-side validation: nothing is launched on failure ----
-    if (!q || !k || !v || !o || !dout || !lse || !delta || !dq || !dk || !dv)
+    if (!q || !k || !v || !o || !dout || !lse || !workspace || !dq || !dk || !dv)
         return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
@@ -272,7 +272,7 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return FA_ERR_MISALIGNED;
-    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(delta) & 3u))
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || !aligned16(workspace))
         return FA_ERR_MISALIGNED;
     const uint64_t batch_stride = 2ull * d * H * static_cast<uint64_t>(N);
     if (batch_stride >= (1ull << 40)) return FA_ERR_TOO_LARGE;
@@ -294,7 +294,9 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
     if ((st = encode_bshd(&L.v, v, dt, B, H, N, d, 128)) != FA_OK) return st;
     if ((st = encode_bshd(&L.dout, dout, dt, B, H, N, d, 128)) != FA_OK) return st;
     L.args.lse = lse;
-    L.args.delta = delta;
+    L.args.ws_d = workspace;
+    L.args.ws_l = workspace + static_cast<size_t>(B) * H * n_t * 128;
+    L.args.NP = static_cast<int>(n_t * 128);
     L.args.o = o;
     L.args.dout = dout;
     L.args.dq = dq;

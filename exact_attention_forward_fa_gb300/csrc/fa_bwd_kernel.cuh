@@ -19,9 +19,18 @@
 //              every run.
 //   sec. 7.3   the preprocessing pass computes D.
 //
-// Both main kernels: 192 threads -- warps 0-3 the elementwise group (one
-// thread per TMEM lane = tile row), warp 4 the TMA producer, warp 5 the MMA
-// issuer (converged warp, elected lane).  All GEMMs are tcgen05.mma
+// Operand rings are per tensor, so the tile the MMA warp needs next lands in
+// a slot freed well before (dQ kernel: K ring of 3, V ring of 2 at d = 128;
+// dK/dV kernel: Q ring of 3, dO ring of 2).  The preprocess writes D and
+// LSE*log2(e) into a workspace padded to whole 128-row tiles (padding: D = 0,
+// LSE2 = +inf, which zero P), read by the elementwise warps through L1.
+//
+// Both main kernels: 320 threads -- warps 0-7 the elementwise group, warp 8
+// the TMA producer, warp 9 the MMA issuer (converged warp, elected lane).
+// The backward's elementwise work has no row reduction (P comes from LSE,
+// dS is pointwise), so two warps share each TMEM lane quarter (one thread
+// per tile row) and split the 128 columns: warp w takes lanes
+// 32 (w mod 4) .. +31 and columns 64 (w / 4) .. +63.  All GEMMs are tcgen05.mma
 // kind::f16 with FP32 accumulation in TMEM; P and dS are rounded to the
 // input's 16-bit type for the GEMMs that consume them.  Every mbarrier wait
 // is bounded and reports through the device status word.
@@ -38,13 +47,15 @@ namespace fa {
 
 struct BwdArgs {
     const float *lse;      // [B][H][N], natural log, from the forward
-    float *delta;          // [B][H][N] D_i = rowsum(dO_i o O_i)
+    float *ws_d;           // [B][H][NP] D_i = rowsum(dO_i o O_i); 0 for n >= N
+    float *ws_l;           // [B][H][NP] LSE_i log2(e); +inf for n >= N and empty rows
     const void *o;         // [B][N][H][d] forward output (preprocess only)
     const void *dout;      // [B][N][H][d] upstream gradient (preprocess only)
     void *dq, *dk, *dv;    // [B][N][H][d] outputs, input dtype
     uint32_t *status;
     int B, H, N;
     int n_t;               // 128-row tiles per sequence
+    int NP;                // n_t * 128: padded row count of the workspace
     int n_units;           // B * H * n_t
     float scale_log2;      // alpha * log2(e)
     float alpha;
@@ -56,7 +67,8 @@ struct BwdCfg {
     static constexpr int NCH = D / 64;                   // 128-byte column chunks
     static constexpr uint32_t CHUNK = 128u * 128u;       // 128 rows x 128 B
     static constexpr uint32_t TILE = NCH * CHUNK;        // one 128 x D tile
-    static constexpr int NTHREADS = 192;
+    static constexpr int NTHREADS = 320;
+    static constexpr int N_EW = 8;                        // elementwise warps
     static constexpr uint32_t TMEM_COLS = 512;
     // S = Q K^T style: both operands K-major, M = N = 128
     static constexpr uint32_t IDESC_SS = idesc_f16(128, 128, kBF16, false, false);
@@ -65,14 +77,16 @@ struct BwdCfg {
     static constexpr int QK_STEPS = D / 16;              // K = D in steps of 16
     static constexpr int ACC_STEPS = 128 / 16;           // K = 128 rows in steps of 16
 
-    // ---- dQ kernel: Q, dO resident per unit; ring of K / V tiles ----
-    static constexpr int DQ_NSTAGE = D == 128 ? 5 : 10;
-    static constexpr uint32_t DQ_Q_OFF = 0, DQ_DO_OFF = TILE, DQ_KV_OFF = 2 * TILE;
-    static constexpr uint32_t DQ_BAR_OFF = DQ_KV_OFF + DQ_NSTAGE * TILE;
+    // ---- dQ kernel: Q, dO resident per unit; a K ring and a V ring ----
+    static constexpr int KN = D == 128 ? 3 : 6, VN = D == 128 ? 2 : 5;
+    static constexpr uint32_t DQ_Q_OFF = 0, DQ_DO_OFF = TILE, DQ_K_OFF = 2 * TILE,
+                              DQ_V_OFF = DQ_K_OFF + KN * TILE;
+    static constexpr uint32_t DQ_BAR_OFF = DQ_V_OFF + VN * TILE;
     static constexpr int DQB_QFULL = 0, DQB_QEMPTY = 1, DQB_SFULL = 2, DQB_DPFULL = 3,
                          DQB_SFREE = 4, DQB_DSFULL = 5 /* x2 */, DQB_DQFULL = 7,
-                         DQB_DQEMPTY = 8, DQB_MMADONE = 9, DQB_KVFULL = 10,
-                         DQB_KVEMPTY = 10 + DQ_NSTAGE, DQ_NBAR = 10 + 2 * DQ_NSTAGE;
+                         DQB_DQEMPTY = 8, DQB_MMADONE = 9, DQB_KFULL = 10,
+                         DQB_KEMPTY = DQB_KFULL + KN, DQB_VFULL = DQB_KEMPTY + KN,
+                         DQB_VEMPTY = DQB_VFULL + VN, DQ_NBAR = DQB_VEMPTY + VN;
     static constexpr uint32_t DQ_MISC_OFF = DQ_BAR_OFF + DQ_NBAR * 8;
     static constexpr uint32_t DQ_SMEM = DQ_MISC_OFF + 16 + 1024;
     // TMEM: S [0,128), dP [128,256), dQ [256,256+D), dS0, dS1 (64 columns each)
@@ -80,16 +94,16 @@ struct BwdCfg {
                               DQ_COL_DS = 256 + D;
     static_assert(DQ_COL_DS + 128 <= TMEM_COLS, "dQ kernel TMEM budget");
 
-    // ---- dK/dV kernel: K, V resident per unit; ring of (Q, dO, LSE, D) ----
-    static constexpr int KV_NSTAGE = D == 128 ? 2 : 4;
-    static constexpr uint32_t VEC_BYTES = 2u * 128u * 4u;          // lse2[128], D[128]
-    static constexpr uint32_t STAGE = 2 * TILE + VEC_BYTES;        // Q, dO, vectors
-    static constexpr uint32_t KV_K_OFF = 0, KV_V_OFF = TILE, KV_RING_OFF = 2 * TILE;
-    static constexpr uint32_t KV_BAR_OFF = KV_RING_OFF + KV_NSTAGE * STAGE;
+    // ---- dK/dV kernel: K, V resident per unit; a Q ring and a dO ring ----
+    static constexpr int QN = D == 128 ? 3 : 6, DN = D == 128 ? 2 : 5;
+    static constexpr uint32_t KV_K_OFF = 0, KV_V_OFF = TILE, KV_Q_OFF = 2 * TILE,
+                              KV_DO_OFF = KV_Q_OFF + QN * TILE;
+    static constexpr uint32_t KV_BAR_OFF = KV_DO_OFF + DN * TILE;
     static constexpr int KVB_KVFULL = 0, KVB_KVEMPTY = 1, KVB_STFULL = 2, KVB_DPTFULL = 3,
                          KVB_PFULL = 4, KVB_DSFULL = 5, KVB_ACCFULL = 6, KVB_ACCEMPTY = 7,
-                         KVB_MMADONE = 8, KVB_QFULL = 9, KVB_QEMPTY = 9 + KV_NSTAGE,
-                         KV_NBAR = 9 + 2 * KV_NSTAGE;
+                         KVB_MMADONE = 8, KVB_QFULL = 9, KVB_QEMPTY = KVB_QFULL + QN,
+                         KVB_DOFULL = KVB_QEMPTY + QN, KVB_DOEMPTY = KVB_DOFULL + DN,
+                         KV_NBAR = KVB_DOEMPTY + DN;
     static constexpr uint32_t KV_MISC_OFF = KV_BAR_OFF + KV_NBAR * 8;
     static constexpr uint32_t KV_SMEM = KV_MISC_OFF + 16 + 1024;
     // TMEM: S^T [0,128) (P^T over its first 64), dP^T [128,256) (dS^T over
@@ -126,10 +140,13 @@ __device__ __forceinline__ BwdUnit make_bwd_unit(int u, const BwdArgs &a) {
 }
 
 // ---------------------------------------------------------------------------
-// Preprocess: D[b][h][n] = sum_c dO[b][n][h][c] * O[b][n][h][c] in FP32
-// ("FlashAttention-3 on Hopper", sec. 7.1.2 and 7.3).  HBM-bound: reads
-// 2 x 2 B per element.  A row of D elements is read by D/8 threads with
-// 16-byte loads; each thread handles 4 rows per pass for memory parallelism.
+// Preprocess ("FlashAttention-3 on Hopper", sec. 7.1.2, 7.1.3 and 7.3):
+//   ws_d[b][h][n] = sum_c dO[b][n][h][c] * O[b][n][h][c]   (FP32)
+//   ws_l[b][h][n] = LSE[b][h][n] * log2(e)                  (+inf if empty)
+// and the padding rows N <= n < NP get D = 0, LSE2 = +inf.  HBM-bound:
+// reads 2 x 2 B per element.  A row of D elements is read by D/8 threads
+// with 16-byte loads; each thread handles 4 rows per pass for memory
+// parallelism.
 // ---------------------------------------------------------------------------
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(256)
@@ -176,9 +193,22 @@ fa_bwd_delta_kernel(const BwdArgs a) {
                 const long h = row % a.H;
                 const long bn = row / a.H;
                 const long n = bn % a.N, b = bn / a.N;
-                a.delta[(b * a.H + h) * a.N + n] = acc;
+                a.ws_d[(b * a.H + h) * a.NP + n] = acc;
             }
         }
+    }
+    const long n_pad = static_cast<long>(a.B) * a.H * a.NP;
+    for (long idx = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n_pad;
+         idx += static_cast<long>(gridDim.x) * blockDim.x) {
+        const long bh = idx / a.NP, n = idx % a.NP;
+        float l2 = INFINITY;
+        if (n < a.N) {
+            const float l = a.lse[bh * a.N + n];
+            l2 = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
+        } else {
+            a.ws_d[idx] = 0.f;
+        }
+        a.ws_l[idx] = l2;
     }
 }
 
@@ -192,6 +222,21 @@ __device__ __forceinline__ void load_tile(const CUtensorMap *m, uint32_t dst, ui
     for (int c = 0; c < NCH; ++c)
         tma_load_4d(m, dst + c * 128u * 128u, bar, c * 64, h, row0, b);
 }
+
+// A ring of NS shared-memory slots filled and drained in order: item i
+// lives in slot i % NS, in phase (i / NS) of that slot's barriers.
+template <int NS>
+struct Ring {
+    __device__ static uint32_t slot(uint32_t i) { return i % NS; }
+    __device__ static uint32_t phase(uint32_t i) { return (i / NS) & 1u; }
+    // teardown: wait for the copy of the last item issued into each slot
+    __device__ static void drain(uint32_t n_issued, uint32_t full0, const uint32_t full_bar_base) {
+        for (uint32_t s = 0; s < NS && s < n_issued; ++s) {
+            const uint32_t last = s + ((n_issued - 1 - s) / NS) * NS;
+            mbar_wait_quiet(full_bar_base + 8u * (full0 + s), phase(last), 500000000ull);
+        }
+    }
+};
 
 // 16-bit A x B^T over the full K = D: both tiles K-major (S = Q K^T style).
 template <int D>
@@ -217,15 +262,15 @@ __device__ __forceinline__ void gemm_ts_mn(uint32_t d_tmem, uint32_t a_tmem, uin
                          (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// Epilogue row store: v (D FP32 values of one row) * scale -> 16 bit.
-template <int D, bool kBF16>
-__device__ __forceinline__ void store_row(void *dst_base, const BwdArgs &a, int b, int h,
-                                          int row, const uint32_t (&v)[D], float scale) {
+// Epilogue store: columns [col0, col0 + W) of one row, v * scale -> 16 bit.
+template <int D, int W, bool kBF16>
+__device__ __forceinline__ void store_cols(void *dst_base, const BwdArgs &a, int b, int h,
+                                           int row, int col0, const uint32_t (&v)[W], float scale) {
     if (row >= a.N) return;
     uint16_t *dst = reinterpret_cast<uint16_t *>(dst_base) +
-                    ((static_cast<size_t>(b) * a.N + row) * a.H + h) * D;
+                    ((static_cast<size_t>(b) * a.N + row) * a.H + h) * D + col0;
 #pragma unroll
-    for (int ch = 0; ch < D / 8; ++ch) {
+    for (int ch = 0; ch < W / 8; ++ch) {
         uint32_t pk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -247,7 +292,7 @@ __device__ __forceinline__ void store_row(void *dst_base, const BwdArgs &a, int 
 // written.
 // ---------------------------------------------------------------------------
 template <int D, bool kCausal, bool kBF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                  const BwdArgs a) {
@@ -262,22 +307,26 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF + 4);
     auto n_key_tiles = [&](const BwdUnit &U) { return kCausal ? U.m + 1 : a.n_t; };
 
-    if (warp == 5) tmem_alloc(base + C::DQ_MISC_OFF, C::TMEM_COLS);
+    if (warp == 9) tmem_alloc(base + C::DQ_MISC_OFF, C::TMEM_COLS);
     if (tid == 0) {
         *abort_flag = 0u;
         mbar_init(bar(C::DQB_QFULL), 1);
         mbar_init(bar(C::DQB_QEMPTY), 1);
         mbar_init(bar(C::DQB_SFULL), 1);
         mbar_init(bar(C::DQB_DPFULL), 1);
-        mbar_init(bar(C::DQB_SFREE), 4);
-        mbar_init(bar(C::DQB_DSFULL + 0), 4);
-        mbar_init(bar(C::DQB_DSFULL + 1), 4);
+        mbar_init(bar(C::DQB_SFREE), C::N_EW);
+        mbar_init(bar(C::DQB_DSFULL + 0), C::N_EW);
+        mbar_init(bar(C::DQB_DSFULL + 1), C::N_EW);
         mbar_init(bar(C::DQB_DQFULL), 1);
-        mbar_init(bar(C::DQB_DQEMPTY), 4);
+        mbar_init(bar(C::DQB_DQEMPTY), C::N_EW);
         mbar_init(bar(C::DQB_MMADONE), 1);
-        for (int s = 0; s < C::DQ_NSTAGE; ++s) {
-            mbar_init(bar(C::DQB_KVFULL + s), 1);
-            mbar_init(bar(C::DQB_KVEMPTY + s), 1);
+        for (int s = 0; s < C::KN; ++s) {
+            mbar_init(bar(C::DQB_KFULL + s), 1);
+            mbar_init(bar(C::DQB_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::VN; ++s) {
+            mbar_init(bar(C::DQB_VFULL + s), 1);
+            mbar_init(bar(C::DQB_VEMPTY + s), 1);
         }
         fence_barrier_init();
     }
@@ -286,7 +335,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // =================== TMA producer (one lane) ===================
         if (lane == 0) {
             WaitCtx w{abort_flag, a.status, kRoleProducer};
@@ -294,7 +343,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_do);
-            uint32_t slot = 0, phase = 0, armed = 0, armed_par = 0;
+            using RK = Ring<C::KN>;
+            using RV = Ring<C::VN>;
+            uint32_t nk = 0, nv = 0;
             int qn = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
@@ -308,33 +359,41 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const int T = n_key_tiles(U);
                 for (int t = 0; ok && t < T; ++t) {
                     const int j = T - 1 - t;
-                    for (int kv = 0; kv < 2; ++kv) {      // K(t), then V(t)
-                        ok = mbar_wait(bar(C::DQB_KVEMPTY + slot), phase ^ 1, w, 51);
-                        if (!ok) break;
-                        mbar_arrive_expect_tx(bar(C::DQB_KVFULL + slot), C::TILE);
-                        load_tile<C::NCH>(kv ? &tm_v : &tm_k, base + C::DQ_KV_OFF + slot * C::TILE,
-                                          bar(C::DQB_KVFULL + slot), U.h, j * 128, U.b);
-                        armed |= 1u << slot;
-                        armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
-                        if (++slot == C::DQ_NSTAGE) { slot = 0; phase ^= 1; }
-                    }
+                    const uint32_t ks = RK::slot(nk), vs = RV::slot(nv);
+                    ok = mbar_wait(bar(C::DQB_KEMPTY + ks), RK::phase(nk) ^ 1, w, 51);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(C::DQB_KFULL + ks), C::TILE);
+                    load_tile<C::NCH>(&tm_k, base + C::DQ_K_OFF + ks * C::TILE, bar(C::DQB_KFULL + ks),
+                                      U.h, j * 128, U.b);
+                    ++nk;
+                    ok = mbar_wait(bar(C::DQB_VEMPTY + vs), RV::phase(nv) ^ 1, w, 52);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(C::DQB_VFULL + vs), C::TILE);
+                    load_tile<C::NCH>(&tm_v, base + C::DQ_V_OFF + vs * C::TILE, bar(C::DQB_VFULL + vs),
+                                      U.h, j * 128, U.b);
+                    ++nv;
                 }
             }
-            for (int s = 0; s < C::DQ_NSTAGE; ++s)
-                if (armed & (1u << s))
-                    mbar_wait_quiet(bar(C::DQB_KVFULL + s), (armed_par >> s) & 1u, 500000000ull);
+            RK::drain(nk, C::DQB_KFULL, base + C::DQ_BAR_OFF);
+            RV::drain(nv, C::DQB_VFULL, base + C::DQ_BAR_OFF);
             if (qn > 0) mbar_wait_quiet(bar(C::DQB_QFULL), (qn - 1) & 1, 500000000ull);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // =================== MMA issuer ===================
         WaitCtx w{abort_flag, a.status, kRoleMma};
-        uint32_t kv_item = 0;               // ring items consumed so far
+        using RK = Ring<C::KN>;
+        using RV = Ring<C::VN>;
+        uint32_t k0 = 0;                    // K and V items of earlier units
         uint32_t qph = 0, sfree_ph = 0, ds_ph0 = 0, ds_ph1 = 0, dqe_ph = 0;
         bool ok = true;
-        auto item = [&](uint32_t i, uint32_t &s, uint32_t &p) {
-            s = i % C::DQ_NSTAGE;
-            p = (i / C::DQ_NSTAGE) & 1u;
+        auto k_tile = [&](uint32_t i) { return base + C::DQ_K_OFF + RK::slot(i) * C::TILE; };
+        auto v_tile = [&](uint32_t i) { return base + C::DQ_V_OFF + RV::slot(i) * C::TILE; };
+        auto wait_k = [&](uint32_t i) {
+            return mbar_wait_warp(bar(C::DQB_KFULL + RK::slot(i)), RK::phase(i), w, 61);
+        };
+        auto wait_v = [&](uint32_t i) {
+            return mbar_wait_warp(bar(C::DQB_VFULL + RV::slot(i)), RV::phase(i), w, 62);
         };
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
             const BwdUnit U = make_bwd_unit<kCausal, false>(u, a);
@@ -343,35 +402,26 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (!ok) break;
             qph ^= 1;
             // S(0), dP(0)
-            uint32_t ks, kp, vs, vp;
-            item(kv_item + 0, ks, kp);
-            item(kv_item + 1, vs, vp);
-            ok = mbar_wait_warp(bar(C::DQB_KVFULL + ks), kp, w, 61) &&
-                 mbar_wait_warp(bar(C::DQB_KVFULL + vs), vp, w, 62);
+            ok = wait_k(k0) && wait_v(k0);
             if (!ok) break;
             tc_fence_after();
-            gemm_ss_kmajor<D>(tbase + C::DQ_COL_S, base + C::DQ_Q_OFF,
-                              base + C::DQ_KV_OFF + ks * C::TILE, C::IDESC_SS);
+            gemm_ss_kmajor<D>(tbase + C::DQ_COL_S, base + C::DQ_Q_OFF, k_tile(k0), C::IDESC_SS);
             mma_commit_elect(bar(C::DQB_SFULL));
-            gemm_ss_kmajor<D>(tbase + C::DQ_COL_DP, base + C::DQ_DO_OFF,
-                              base + C::DQ_KV_OFF + vs * C::TILE, C::IDESC_SS);
+            gemm_ss_kmajor<D>(tbase + C::DQ_COL_DP, base + C::DQ_DO_OFF, v_tile(k0), C::IDESC_SS);
             mma_commit_elect(bar(C::DQB_DPFULL));
-            mma_commit_elect(bar(C::DQB_KVEMPTY + vs));
+            mma_commit_elect(bar(C::DQB_VEMPTY + RV::slot(k0)));
             if (T == 1) mma_commit_elect(bar(C::DQB_QEMPTY));
             for (int t = 0; ok && t < T; ++t) {
-                uint32_t kts, ktp;
-                item(kv_item + 2 * t, kts, ktp);             // K(t) slot
+                const uint32_t it = k0 + t;          // item index of tile t in both rings
                 // ---- S(t+1) once S(t) has been read ----
                 ok = mbar_wait_warp(bar(C::DQB_SFREE), sfree_ph, w, 63);
                 if (!ok) break;
                 sfree_ph ^= 1;
                 if (t + 1 < T) {
-                    item(kv_item + 2 * (t + 1), ks, kp);
-                    ok = mbar_wait_warp(bar(C::DQB_KVFULL + ks), kp, w, 64);
+                    ok = wait_k(it + 1);
                     if (!ok) break;
                     tc_fence_after();
-                    gemm_ss_kmajor<D>(tbase + C::DQ_COL_S, base + C::DQ_Q_OFF,
-                                      base + C::DQ_KV_OFF + ks * C::TILE, C::IDESC_SS);
+                    gemm_ss_kmajor<D>(tbase + C::DQ_COL_S, base + C::DQ_Q_OFF, k_tile(it + 1), C::IDESC_SS);
                     mma_commit_elect(bar(C::DQB_SFULL));
                 }
                 // ---- dS(t) ready: dP(t+1), then dQ += dS(t) K(t) ----
@@ -380,14 +430,12 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (!ok) break;
                 if (b2) ds_ph1 ^= 1; else ds_ph0 ^= 1;
                 if (t + 1 < T) {
-                    item(kv_item + 2 * (t + 1) + 1, vs, vp);
-                    ok = mbar_wait_warp(bar(C::DQB_KVFULL + vs), vp, w, 66);
+                    ok = wait_v(it + 1);
                     if (!ok) break;
                     tc_fence_after();
-                    gemm_ss_kmajor<D>(tbase + C::DQ_COL_DP, base + C::DQ_DO_OFF,
-                                      base + C::DQ_KV_OFF + vs * C::TILE, C::IDESC_SS);
+                    gemm_ss_kmajor<D>(tbase + C::DQ_COL_DP, base + C::DQ_DO_OFF, v_tile(it + 1), C::IDESC_SS);
                     mma_commit_elect(bar(C::DQB_DPFULL));
-                    mma_commit_elect(bar(C::DQB_KVEMPTY + vs));
+                    mma_commit_elect(bar(C::DQB_VEMPTY + RV::slot(it + 1)));
                     if (t + 2 == T) mma_commit_elect(bar(C::DQB_QEMPTY));   // last use of Q, dO
                 }
                 if (t == 0) {
@@ -396,21 +444,23 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     dqe_ph ^= 1;
                 }
                 tc_fence_after();
-                gemm_ts_mn(tbase + C::DQ_COL_DQ, tbase + C::DQ_COL_DS + b2 * 64u,
-                           base + C::DQ_KV_OFF + kts * C::TILE, C::IDESC_ACC, t > 0);
-                mma_commit_elect(bar(C::DQB_KVEMPTY + kts));
+                gemm_ts_mn(tbase + C::DQ_COL_DQ, tbase + C::DQ_COL_DS + b2 * 64u, k_tile(it),
+                           C::IDESC_ACC, t > 0);
+                mma_commit_elect(bar(C::DQB_KEMPTY + RK::slot(it)));
             }
             if (!ok) break;
             mma_commit_elect(bar(C::DQB_DQFULL));
-            kv_item += 2 * T;
+            k0 += T;
         }
         mma_commit_elect(bar(C::DQB_MMADONE));
         mbar_wait_quiet(bar(C::DQB_MMADONE), 0, 500000000ull);
         __syncwarp();
     } else {
-        // =================== elementwise group (warps 0-3) ===================
-        const int row = tid;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        // =================== elementwise group (warps 0-7) ===================
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;                 // TMEM lane == tile row
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const int col0 = half * 64;                          // this warp's key columns
         WaitCtx w{abort_flag, a.status, kRoleSoftmax0};
         const float sl2 = a.scale_log2;
         uint32_t sph = 0, dpph = 0, dqph = 0;
@@ -419,17 +469,13 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const BwdUnit U = make_bwd_unit<kCausal, false>(u, a);
             const int T = n_key_tiles(U);
             const int grow = U.m * 128 + row;
-            // log2-domain LSE of this row (+inf hides rows beyond N and
-            // empty rows: their P is 0), and D of this row
-            float lse2 = INFINITY, drow = 0.f;
-            if (grow < a.N) {
-                const size_t idx = (static_cast<size_t>(U.b) * a.H + U.h) * a.N + grow;
-                const float l = a.lse[idx];
-                lse2 = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
-                drow = a.delta[idx];
-            }
+            // log2-domain LSE of this row (+inf for rows beyond N and empty
+            // rows: their P is 0) and D of this row, from the workspace
+            const size_t widx = (static_cast<size_t>(U.b) * a.H + U.h) * a.NP + grow;
+            const float lse2 = a.ws_l[widx], drow = a.ws_d[widx];
             const float2 c2 = make_float2(sl2, sl2);
             const float2 nl2 = make_float2(-lse2, -lse2);
+            const float2 nd2 = make_float2(-drow, -drow);
             for (int t = 0; t < T; ++t) {
                 const int j = T - 1 - t;
                 // ---- P(t) = exp2(S c - LSE2) from S(t) ----
@@ -437,20 +483,19 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 sph ^= 1;
                 tc_fence_after();
-                uint32_t s[128];
-                const uint32_t tS = tbase + lane_off + C::DQ_COL_S;
-#pragma unroll
-                for (int c = 0; c < 128; c += 32)
-                    tmem_ld32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&s[c]));
+                uint32_t sv[64];
+                const uint32_t tS = tbase + lane_off + C::DQ_COL_S + col0;
+                tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tmem_ld_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::DQB_SFREE));
-                int lim = min(128, a.N - j * 128);              // keys beyond N
-                if (kCausal) lim = min(lim, grow - j * 128 + 1);
-                float *pf = reinterpret_cast<float *>(s);
+                int lim = min(128, a.N - j * 128) - col0;        // keys beyond N
+                if (kCausal) lim = min(lim, grow - j * 128 + 1 - col0);
+                float *pf = reinterpret_cast<float *>(sv);
 #pragma unroll
-                for (int c = 0; c < 128; c += 2) {
+                for (int c = 0; c < 64; c += 2) {
                     const float2 x = __ffma2_rn(make_float2(pf[c], pf[c + 1]), c2, nl2);
                     pf[c] = c < lim ? ex2_approx(x.x) : 0.f;
                     pf[c + 1] = c + 1 < lim ? ex2_approx(x.y) : 0.f;
@@ -460,51 +505,48 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 dpph ^= 1;
                 tc_fence_after();
-                const uint32_t tDP = tbase + lane_off + C::DQ_COL_DP;
-                const uint32_t tDS = tbase + lane_off + C::DQ_COL_DS + (t & 1) * 64u;
-                const float2 nd2 = make_float2(-drow, -drow);
+                uint32_t dp[64];
+                const uint32_t tDP = tbase + lane_off + C::DQ_COL_DP + col0;
+                tmem_ld32(tDP, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+                tmem_ld32(tDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+                tmem_ld_wait();
+                uint32_t pk[32];
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t dp[32];
-                    tmem_ld32(tDP + ch * 32, dp);
-                    tmem_ld_wait();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float2 g = __fadd2_rn(
-                            make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), nd2);
-                        const float2 ds = __fmul2_rn(make_float2(pf[ch * 32 + i], pf[ch * 32 + i + 1]), g);
-                        pk[i / 2] = pack2<kBF16>(ds.x, ds.y);
-                    }
-                    tmem_st16(tDS + ch * 16, pk);
+                for (int i = 0; i < 64; i += 2) {
+                    const float2 g = __fadd2_rn(
+                        make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), nd2);
+                    const float2 ds = __fmul2_rn(make_float2(pf[i], pf[i + 1]), g);
+                    pk[i / 2] = pack2<kBF16>(ds.x, ds.y);
                 }
+                tmem_st32(tbase + lane_off + C::DQ_COL_DS + (t & 1) * 64u + half * 32, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::DQB_DSFULL + (t & 1)));
             }
             if (!ok) break;
-            // ---- epilogue: dQ * alpha -> global ----
+            // ---- epilogue: dQ * alpha -> global (this warp's half of the columns) ----
             ok = mbar_wait(bar(C::DQB_DQFULL), dqph, w, 72);
             if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
             dqph ^= 1;
             tc_fence_after();
-            uint32_t dq[D];
+            constexpr int W = D / 2;
+            uint32_t dq[W];
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch)
-                tmem_ld32(tbase + lane_off + C::DQ_COL_DQ + ch * 32,
+            for (int ch = 0; ch < W / 32; ++ch)
+                tmem_ld32(tbase + lane_off + C::DQ_COL_DQ + half * W + ch * 32,
                           *reinterpret_cast<uint32_t(*)[32]>(&dq[ch * 32]));
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::DQB_DQEMPTY));
-            store_row<D, kBF16>(a.dq, a, U.b, U.h, grow, dq, a.alpha);
+            store_cols<D, W, kBF16>(a.dq, a, U.b, U.h, grow, half * W, dq, a.alpha);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tbase, C::TMEM_COLS);
@@ -521,11 +563,16 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 //   G4  dK += dS^T Q_i                                     (Q_i MN-major)
 // MMA order per tile: G3(i), G1(i+1), G4(i), G2(i+1), so the exponentials
 // of tile i+1 overlap G4(i) and G2(i+1), and dS(i+1) overlaps G3(i+1) and
-// G1(i+2).  The producer warp stages LSE2 and D of each query tile next to
-// Q_i and dO_i in the ring (LSE2 = +inf and D = 0 beyond N, which zero P).
+// G1(i+2).  The 16-bit P^T and dS^T of the query columns [64h, 64h+64)
+// (h: the warp's column half) go to TMEM columns 32 + 32h .. +32 of the
+// S^T / dP^T regions, which that warp has itself read, so the two warps of
+// a lane quarter need no barrier; G3 and G4 read their A operand from
+// column 32.  Q_i and dO_i come through separate rings (Q is held until G4,
+// dO until G3); LSE2 and D of the query columns are read from the padded
+// workspace through L1, where the producer prefetches each tile's lines.
 // ---------------------------------------------------------------------------
 template <int D, bool kCausal, bool kBF16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdArgs a) {
@@ -539,25 +586,30 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF + 4);
     auto first_q = [&](const BwdUnit &U) { return kCausal ? U.m : 0; };
-    auto stage_q = [&](int s) { return base + C::KV_RING_OFF + s * C::STAGE; };
-    auto stage_do = [&](int s) { return base + C::KV_RING_OFF + s * C::STAGE + C::TILE; };
-    auto stage_vec = [&](int s) { return gbase + C::KV_RING_OFF + s * C::STAGE + 2 * C::TILE; };
+    using RQ = Ring<C::QN>;
+    using RO = Ring<C::DN>;
+    auto q_tile = [&](uint32_t i) { return base + C::KV_Q_OFF + RQ::slot(i) * C::TILE; };
+    auto do_tile = [&](uint32_t i) { return base + C::KV_DO_OFF + RO::slot(i) * C::TILE; };
 
-    if (warp == 5) tmem_alloc(base + C::KV_MISC_OFF, C::TMEM_COLS);
+    if (warp == 9) tmem_alloc(base + C::KV_MISC_OFF, C::TMEM_COLS);
     if (tid == 0) {
         *abort_flag = 0u;
         mbar_init(bar(C::KVB_KVFULL), 1);
         mbar_init(bar(C::KVB_KVEMPTY), 1);
         mbar_init(bar(C::KVB_STFULL), 1);
         mbar_init(bar(C::KVB_DPTFULL), 1);
-        mbar_init(bar(C::KVB_PFULL), 4);
-        mbar_init(bar(C::KVB_DSFULL), 4);
+        mbar_init(bar(C::KVB_PFULL), C::N_EW);
+        mbar_init(bar(C::KVB_DSFULL), C::N_EW);
         mbar_init(bar(C::KVB_ACCFULL), 1);
-        mbar_init(bar(C::KVB_ACCEMPTY), 4);
+        mbar_init(bar(C::KVB_ACCEMPTY), C::N_EW);
         mbar_init(bar(C::KVB_MMADONE), 1);
-        for (int s = 0; s < C::KV_NSTAGE; ++s) {
+        for (int s = 0; s < C::QN; ++s) {
             mbar_init(bar(C::KVB_QFULL + s), 1);
             mbar_init(bar(C::KVB_QEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::DN; ++s) {
+            mbar_init(bar(C::KVB_DOFULL + s), 1);
+            mbar_init(bar(C::KVB_DOEMPTY + s), 1);
         }
         fence_barrier_init();
     }
@@ -566,72 +618,61 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
-    if (warp == 4) {
-        // =================== producer (whole warp: vectors; lane 0: TMA) ===================
-        WaitCtx w{abort_flag, a.status, kRoleProducer};
+    if (warp == 8) {
+        // =================== TMA producer (one lane) ===================
         if (lane == 0) {
+            WaitCtx w{abort_flag, a.status, kRoleProducer};
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_do);
-        }
-        uint32_t slot = 0, phase = 0, armed = 0, armed_par = 0;
-        int kvn = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-            const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
-            ok = mbar_wait_warp(bar(C::KVB_KVEMPTY), (kvn & 1) ^ 1, w, 80);
-            if (!ok) break;
-            if (lane == 0) {
+            uint32_t nq = 0, n_qc = 0, n_dc = 0;     // tiles; Q and dO copies issued
+            int kvn = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+                const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
+                ok = mbar_wait(bar(C::KVB_KVEMPTY), (kvn & 1) ^ 1, w, 80);
+                if (!ok) break;
                 mbar_arrive_expect_tx(bar(C::KVB_KVFULL), 2 * C::TILE);
                 load_tile<C::NCH>(&tm_k, base + C::KV_K_OFF, bar(C::KVB_KVFULL), U.h, U.m * 128, U.b);
                 load_tile<C::NCH>(&tm_v, base + C::KV_V_OFF, bar(C::KVB_KVFULL), U.h, U.m * 128, U.b);
-            }
-            ++kvn;
-            const size_t vbase = (static_cast<size_t>(U.b) * a.H + U.h) * a.N;
-            for (int i = first_q(U); ok && i < a.n_t; ++i) {
-                ok = mbar_wait_warp(bar(C::KVB_QEMPTY + slot), phase ^ 1, w, 81);
-                if (!ok) break;
-                // LSE2 and D of the 128 query rows of tile i, 4 per lane
-                float *vec = reinterpret_cast<float *>(stage_vec(slot));
+                ++kvn;
+                const size_t wrow = (static_cast<size_t>(U.b) * a.H + U.h) * a.NP;
+                for (int i = first_q(U); ok && i < a.n_t; ++i, ++nq) {
+                    // the elementwise warps read LSE2 and D of these 128
+                    // columns: 2 x 512 B, four 128-byte lines each
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int q = i * 128 + r * 32 + lane;
-                    float l2 = INFINITY, dd = 0.f;
-                    if (q < a.N) {
-                        const float l = a.lse[vbase + q];
-                        l2 = l == -INFINITY ? INFINITY : l * 1.4426950408889634f;
-                        dd = a.delta[vbase + q];
+                    for (int l = 0; l < 4; ++l) {
+                        asm volatile("prefetch.global.L1 [%0];" :: "l"(a.ws_l + wrow + i * 128 + l * 32));
+                        asm volatile("prefetch.global.L1 [%0];" :: "l"(a.ws_d + wrow + i * 128 + l * 32));
                     }
-                    vec[r * 32 + lane] = l2;
-                    vec[128 + r * 32 + lane] = dd;
+                    ok = mbar_wait(bar(C::KVB_QEMPTY + RQ::slot(nq)), RQ::phase(nq) ^ 1, w, 81);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(C::KVB_QFULL + RQ::slot(nq)), C::TILE);
+                    load_tile<C::NCH>(&tm_q, q_tile(nq), bar(C::KVB_QFULL + RQ::slot(nq)), U.h, i * 128, U.b);
+                    ++n_qc;
+                    ok = mbar_wait(bar(C::KVB_DOEMPTY + RO::slot(nq)), RO::phase(nq) ^ 1, w, 82);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar(C::KVB_DOFULL + RO::slot(nq)), C::TILE);
+                    load_tile<C::NCH>(&tm_do, do_tile(nq), bar(C::KVB_DOFULL + RO::slot(nq)), U.h, i * 128, U.b);
+                    ++n_dc;
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar(C::KVB_QFULL + slot), 2 * C::TILE);
-                    load_tile<C::NCH>(&tm_q, stage_q(slot), bar(C::KVB_QFULL + slot), U.h, i * 128, U.b);
-                    load_tile<C::NCH>(&tm_do, stage_do(slot), bar(C::KVB_QFULL + slot), U.h, i * 128, U.b);
-                }
-                armed |= 1u << slot;
-                armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
-                if (++slot == C::KV_NSTAGE) { slot = 0; phase ^= 1; }
             }
-        }
-        if (lane == 0) {
-            for (int s = 0; s < C::KV_NSTAGE; ++s)
-                if (armed & (1u << s))
-                    mbar_wait_quiet(bar(C::KVB_QFULL + s), (armed_par >> s) & 1u, 500000000ull);
+            RQ::drain(n_qc, C::KVB_QFULL, base + C::KV_BAR_OFF);
+            RO::drain(n_dc, C::KVB_DOFULL, base + C::KV_BAR_OFF);
             if (kvn > 0) mbar_wait_quiet(bar(C::KVB_KVFULL), (kvn - 1) & 1, 500000000ull);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // =================== MMA issuer ===================
         WaitCtx w{abort_flag, a.status, kRoleMma};
         uint32_t q_item = 0, kvph = 0, pph = 0, dsph = 0, accph = 0;
         bool ok = true;
-        auto item = [&](uint32_t i, uint32_t &s, uint32_t &p) {
-            s = i % C::KV_NSTAGE;
-            p = (i / C::KV_NSTAGE) & 1u;
+        auto wait_q = [&](uint32_t i) {
+            return mbar_wait_warp(bar(C::KVB_QFULL + RQ::slot(i)), RQ::phase(i), w, 91);
+        };
+        auto wait_do = [&](uint32_t i) {
+            return mbar_wait_warp(bar(C::KVB_DOFULL + RO::slot(i)), RO::phase(i), w, 96);
         };
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
             const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
@@ -639,46 +680,51 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             ok = mbar_wait_warp(bar(C::KVB_KVFULL), kvph, w, 90);
             if (!ok) break;
             kvph ^= 1;
-            uint32_t s0, p0;
-            item(q_item, s0, p0);
-            ok = mbar_wait_warp(bar(C::KVB_QFULL + s0), p0, w, 91);
+            ok = wait_q(q_item);
             if (!ok) break;
             tc_fence_after();
-            gemm_ss_kmajor<D>(tbase + C::KV_COL_ST, base + C::KV_K_OFF, stage_q(s0), C::IDESC_SS);
+            gemm_ss_kmajor<D>(tbase + C::KV_COL_ST, base + C::KV_K_OFF, q_tile(q_item), C::IDESC_SS);
             mma_commit_elect(bar(C::KVB_STFULL));
-            gemm_ss_kmajor<D>(tbase + C::KV_COL_DPT, base + C::KV_V_OFF, stage_do(s0), C::IDESC_SS);
+            ok = wait_do(q_item);
+            if (!ok) break;
+            tc_fence_after();
+            gemm_ss_kmajor<D>(tbase + C::KV_COL_DPT, base + C::KV_V_OFF, do_tile(q_item), C::IDESC_SS);
             mma_commit_elect(bar(C::KVB_DPTFULL));
             for (int k = 0; ok && k < Ti; ++k) {
-                uint32_t sc, pc, sn = 0, pn = 0;
-                item(q_item + k, sc, pc);
+                const uint32_t ic = q_item + k, in = ic + 1;
                 const bool more = k + 1 < Ti;
-                if (more) item(q_item + k + 1, sn, pn);
-                // ---- G3: dV += P^T dO_i ----
+                // ---- G3: dV += P^T dO_i (P^T at columns 32..95 of S^T) ----
                 ok = mbar_wait_warp(bar(C::KVB_PFULL), pph, w, 92);
                 if (ok && k == 0) ok = mbar_wait_warp(bar(C::KVB_ACCEMPTY), accph ^ 1, w, 93);
                 if (!ok) break;
                 pph ^= 1;
                 if (k == 0) accph ^= 1;
                 tc_fence_after();
-                gemm_ts_mn(tbase + C::KV_COL_DV, tbase + C::KV_COL_ST, stage_do(sc), C::IDESC_ACC, k > 0);
+                gemm_ts_mn(tbase + C::KV_COL_DV, tbase + C::KV_COL_ST + 32, do_tile(ic), C::IDESC_ACC,
+                           k > 0);
+                mma_commit_elect(bar(C::KVB_DOEMPTY + RO::slot(ic)));
                 // ---- G1(i+1) ----
                 if (more) {
-                    ok = mbar_wait_warp(bar(C::KVB_QFULL + sn), pn, w, 94);
+                    ok = wait_q(in);
                     if (!ok) break;
                     tc_fence_after();
-                    gemm_ss_kmajor<D>(tbase + C::KV_COL_ST, base + C::KV_K_OFF, stage_q(sn), C::IDESC_SS);
+                    gemm_ss_kmajor<D>(tbase + C::KV_COL_ST, base + C::KV_K_OFF, q_tile(in), C::IDESC_SS);
                     mma_commit_elect(bar(C::KVB_STFULL));
                 }
-                // ---- G4: dK += dS^T Q_i ----
+                // ---- G4: dK += dS^T Q_i (dS^T at columns 32..95 of dP^T) ----
                 ok = mbar_wait_warp(bar(C::KVB_DSFULL), dsph, w, 95);
                 if (!ok) break;
                 dsph ^= 1;
                 tc_fence_after();
-                gemm_ts_mn(tbase + C::KV_COL_DK, tbase + C::KV_COL_DPT, stage_q(sc), C::IDESC_ACC, k > 0);
-                mma_commit_elect(bar(C::KVB_QEMPTY + sc));
+                gemm_ts_mn(tbase + C::KV_COL_DK, tbase + C::KV_COL_DPT + 32, q_tile(ic), C::IDESC_ACC,
+                           k > 0);
+                mma_commit_elect(bar(C::KVB_QEMPTY + RQ::slot(ic)));
                 // ---- G2(i+1) ----
                 if (more) {
-                    gemm_ss_kmajor<D>(tbase + C::KV_COL_DPT, base + C::KV_V_OFF, stage_do(sn), C::IDESC_SS);
+                    ok = wait_do(in);
+                    if (!ok) break;
+                    tc_fence_after();
+                    gemm_ss_kmajor<D>(tbase + C::KV_COL_DPT, base + C::KV_V_OFF, do_tile(in), C::IDESC_SS);
                     mma_commit_elect(bar(C::KVB_DPTFULL));
                 }
             }
@@ -691,46 +737,43 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_wait_quiet(bar(C::KVB_MMADONE), 0, 500000000ull);
         __syncwarp();
     } else {
-        // =================== elementwise group (warps 0-3) ===================
-        const int row = tid;                       // key row of the tile
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        // =================== elementwise group (warps 0-7) ===================
+        const int quarter = warp & 3, half = warp >> 2;
+        const int row = quarter * 32 + lane;                 // key row of the tile
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const int col0 = half * 64;                          // this warp's query columns
         WaitCtx w{abort_flag, a.status, kRoleSoftmax0};
         const float sl2 = a.scale_log2;
         const float2 c2 = make_float2(sl2, sl2);
-        uint32_t stph = 0, dpph = 0, accph = 0, q_item = 0;
+        uint32_t stph = 0, dpph = 0, accph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
             const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
             const int i0 = first_q(U);
             const int Ti = a.n_t - i0;
             const int krow = U.m * 128 + row;
+            const size_t wrow = (static_cast<size_t>(U.b) * a.H + U.h) * a.NP;
             for (int k = 0; k < Ti; ++k) {
                 const int i = i0 + k;
-                const int sc = static_cast<int>((q_item + k) % C::KV_NSTAGE);
-                const uint32_t scp = ((q_item + k) / C::KV_NSTAGE) & 1u;
-                const float *vec = reinterpret_cast<const float *>(stage_vec(sc));
+                const float4 *lse4 = reinterpret_cast<const float4 *>(a.ws_l + wrow + i * 128 + col0);
+                const float4 *dd4 = reinterpret_cast<const float4 *>(a.ws_d + wrow + i * 128 + col0);
                 // ---- P^T = exp2(S^T c - LSE2[q]) ----
-                // The stage's full phase (already complete for the MMA warp)
-                // orders the producer's stores of LSE2 and D before the reads
-                // below; it cannot advance before this tile's G4 releases it.
-                ok = mbar_wait(bar(C::KVB_QFULL + sc), scp, w, 103) &&
-                     mbar_wait(bar(C::KVB_STFULL), stph, w, 100);
+                ok = mbar_wait(bar(C::KVB_STFULL), stph, w, 100);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 stph ^= 1;
                 tc_fence_after();
-                uint32_t s[128];
+                uint32_t sv[64];
                 const uint32_t tST = tbase + lane_off + C::KV_COL_ST;
-#pragma unroll
-                for (int c = 0; c < 128; c += 32)
-                    tmem_ld32(tST + c, *reinterpret_cast<uint32_t(*)[32]>(&s[c]));
+                tmem_ld32(tST + col0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                tmem_ld32(tST + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tmem_ld_wait();
                 // causal: query column q sees this key row iff krow <= q
-                const int lo = kCausal ? krow - i * 128 : 0;   // first visible column
-                float *pf = reinterpret_cast<float *>(s);
-                uint32_t pk[64];
+                const int lo = (kCausal ? krow - i * 128 : 0) - col0;   // first visible column
+                float *pf = reinterpret_cast<float *>(sv);
+                uint32_t pk[32];
 #pragma unroll
-                for (int c = 0; c < 128; c += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(vec + c);
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 l4 = __ldg(lse4 + c / 4);
                     const float2 x01 = __ffma2_rn(make_float2(pf[c], pf[c + 1]), c2,
                                                   make_float2(-l4.x, -l4.y));
                     const float2 x23 = __ffma2_rn(make_float2(pf[c + 2], pf[c + 3]), c2,
@@ -742,8 +785,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     pk[c / 2] = pack2<kBF16>(pf[c], pf[c + 1]);
                     pk[c / 2 + 1] = pack2<kBF16>(pf[c + 2], pf[c + 3]);
                 }
-                tmem_st32(tST + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-                tmem_st32(tST + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+                // 16-bit P^T of query columns [col0, col0+64) -> S^T columns
+                // 32 + col0/2 .. +32: columns this warp has read itself
+                tmem_st32(tST + 32 + half * 32, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -753,64 +797,60 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 dpph ^= 1;
                 tc_fence_after();
+                uint32_t dp[64];
                 const uint32_t tDPT = tbase + lane_off + C::KV_COL_DPT;
+                tmem_ld32(tDPT + col0, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+                tmem_ld32(tDPT + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+                tmem_ld_wait();
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t dp[32];
-                    tmem_ld32(tDPT + ch * 32, dp);
-                    tmem_ld_wait();
-                    uint32_t dk[16];
-#pragma unroll
-                    for (int t4 = 0; t4 < 32; t4 += 4) {
-                        const int c = ch * 32 + t4;
-                        const float4 d4 = *reinterpret_cast<const float4 *>(vec + 128 + c);
-                        const float2 g01 = __fadd2_rn(
-                            make_float2(__uint_as_float(dp[t4]), __uint_as_float(dp[t4 + 1])),
-                            make_float2(-d4.x, -d4.y));
-                        const float2 g23 = __fadd2_rn(
-                            make_float2(__uint_as_float(dp[t4 + 2]), __uint_as_float(dp[t4 + 3])),
-                            make_float2(-d4.z, -d4.w));
-                        const float2 ds01 = __fmul2_rn(make_float2(pf[c], pf[c + 1]), g01);
-                        const float2 ds23 = __fmul2_rn(make_float2(pf[c + 2], pf[c + 3]), g23);
-                        dk[t4 / 2] = pack2<kBF16>(ds01.x, ds01.y);
-                        dk[t4 / 2 + 1] = pack2<kBF16>(ds23.x, ds23.y);
-                    }
-                    tmem_st16(tDPT + ch * 16, dk);
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 d4 = __ldg(dd4 + c / 4);
+                    const float2 g01 = __fadd2_rn(
+                        make_float2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                        make_float2(-d4.x, -d4.y));
+                    const float2 g23 = __fadd2_rn(
+                        make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
+                        make_float2(-d4.z, -d4.w));
+                    const float2 ds01 = __fmul2_rn(make_float2(pf[c], pf[c + 1]), g01);
+                    const float2 ds23 = __fmul2_rn(make_float2(pf[c + 2], pf[c + 3]), g23);
+                    pk[c / 2] = pack2<kBF16>(ds01.x, ds01.y);
+                    pk[c / 2 + 1] = pack2<kBF16>(ds23.x, ds23.y);
                 }
+                tmem_st32(tDPT + 32 + half * 32, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::KVB_DSFULL));
             }
             if (!ok) break;
-            q_item += Ti;
-            // ---- epilogue: dV, dK * alpha -> global ----
+            // ---- epilogue: dV, dK * alpha -> global (this warp's half of the columns) ----
             ok = mbar_wait(bar(C::KVB_ACCFULL), accph, w, 102);
             if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
             accph ^= 1;
             tc_fence_after();
-            uint32_t acc[D];
+            constexpr int W = D / 2;
+            uint32_t acc[W];
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch)
-                tmem_ld32(tbase + lane_off + C::KV_COL_DV + ch * 32,
+            for (int ch = 0; ch < W / 32; ++ch)
+                tmem_ld32(tbase + lane_off + C::KV_COL_DV + half * W + ch * 32,
                           *reinterpret_cast<uint32_t(*)[32]>(&acc[ch * 32]));
             tmem_ld_wait();
-            store_row<D, kBF16>(a.dv, a, U.b, U.h, krow, acc, 1.f);
+            store_cols<D, W, kBF16>(a.dv, a, U.b, U.h, krow, half * W, acc, 1.f);
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch)
-                tmem_ld32(tbase + lane_off + C::KV_COL_DK + ch * 32,
+            for (int ch = 0; ch < W / 32; ++ch)
+                tmem_ld32(tbase + lane_off + C::KV_COL_DK + half * W + ch * 32,
                           *reinterpret_cast<uint32_t(*)[32]>(&acc[ch * 32]));
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::KVB_ACCEMPTY));
-            store_row<D, kBF16>(a.dk, a, U.b, U.h, krow, acc, a.alpha);
+            store_cols<D, W, kBF16>(a.dk, a, U.b, U.h, krow, half * W, acc, a.alpha);
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tbase, C::TMEM_COLS);

@@ -126,7 +126,9 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
  *            lse are the outputs of fa_fwd on the same q, k, v, alpha and
  *            causal.
  *   lse    : device, float [B][H][N] (natural log, as fa_fwd writes it).
- *   delta  : device, float [B][H][N], caller-owned workspace; receives D.
+ *   workspace : device, float [2][B][H][ceil(N/128)*128], 16-byte aligned,
+ *            caller-owned; receives D = rowsum(dO o O) and LSE*log2(e) per
+ *            row (rows padded to whole 128-row tiles).
  *   dq, dk, dv : device, dtype [B][N][H][d], 16-byte aligned (written).
  *   d in {64, 128} (others return FA_ERR_UNSUPPORTED); alpha, causal,
  *   dtype and stream as fa_fwd.
@@ -138,7 +140,7 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
  * `dtype`.  Nothing is allocated.  Errors as fa_fwd.
  */
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
-                 const void *dout, const float *lse, float *delta, void *dq,
+                 const void *dout, const float *lse, float *workspace, void *dq,
                  void *dk, void *dv, int B, int H, int N, int d, float alpha,
                  int causal, fa_dtype dtype, void *stream);
 

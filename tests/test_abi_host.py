@@ -123,9 +123,9 @@ def test_fp8_validation_codes(lib, kw, code):
     assert _f8call(lib, **kw) == code
 
 
-def _bcall(lib, q=A, k=A, v=A, o=A, do=A, lse=A, delta=A, dq=A, dk=A, dv=A, B=1, H=1,
+def _bcall(lib, q=A, k=A, v=A, o=A, do=A, lse=A, ws=A, dq=A, dk=A, dv=A, B=1, H=1,
            N=128, d=128, alpha=0.088, causal=0, dtype=0):
-    return lib.fa_bwd(q, k, v, o, do, lse, delta, dq, dk, dv, B, H, N, d, alpha, causal,
+    return lib.fa_bwd(q, k, v, o, do, lse, ws, dq, dk, dv, B, H, N, d, alpha, causal,
                       dtype, None)
 
 
@@ -133,7 +133,7 @@ def _bcall(lib, q=A, k=A, v=A, o=A, do=A, lse=A, delta=A, dq=A, dk=A, dv=A, B=1,
     (dict(q=None), fa.FA_ERR_INVALID_ARG),
     (dict(do=None), fa.FA_ERR_INVALID_ARG),
     (dict(lse=None), fa.FA_ERR_INVALID_ARG),
-    (dict(delta=None), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=None), fa.FA_ERR_INVALID_ARG),
     (dict(dv=None), fa.FA_ERR_INVALID_ARG),
     (dict(N=0), fa.FA_ERR_INVALID_ARG),
     (dict(causal=2), fa.FA_ERR_INVALID_ARG),
@@ -143,7 +143,7 @@ def _bcall(lib, q=A, k=A, v=A, o=A, do=A, lse=A, delta=A, dq=A, dk=A, dv=A, B=1,
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(o=A + 8), fa.FA_ERR_MISALIGNED),
     (dict(dk=A + 2), fa.FA_ERR_MISALIGNED),
-    (dict(delta=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(ws=A + 4), fa.FA_ERR_MISALIGNED),
     (dict(B=1 << 20, H=1 << 10, N=1 << 20, d=128), fa.FA_ERR_TOO_LARGE),
 ])
 def test_bwd_validation_codes(lib, kw, code):
