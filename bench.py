@@ -78,10 +78,12 @@ def measured_peaks():
         return 1900.0, 1700.0, "fallback"
 
 
-def source_hash():
+def source_hash(files=None):
+    """Hash of kernel sources: the listed files of csrc/ (a profiled
+    kernel's own code), or the whole directory."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_forward_fa_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(files) if files else sorted(os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -89,13 +91,13 @@ def source_hash():
 
 def profiled_traffic(workload_key):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of that kernel; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             t = json.load(f)
         e = t[workload_key]
-        if e.get("source_hash") == source_hash():
+        if e.get("source_hash") == source_hash(e.get("files")):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         pass
