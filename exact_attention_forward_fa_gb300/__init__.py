@@ -29,8 +29,8 @@ FA_BF16 = 0
 FA_FP16 = 1
 
 # Every symbol include/fa.h declares (checked by the tests).
-EXPORTS = ("fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_check_status",
-           "fa_status_detail", "fa_status_string", "fa_version")
+EXPORTS = ("fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_noalloc",
+           "fa_check_status", "fa_status_detail", "fa_status_string", "fa_version")
 
 _lib = None
 
@@ -60,6 +60,8 @@ def load():
     lib.fa_fwd_fp8.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+    lib.fa_bwd_noalloc.restype = i
     lib.fa_check_status.argtypes = [vp]
     lib.fa_check_status.restype = i
     lib.fa_status_detail.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -162,6 +164,16 @@ def fa_bwd(q, k, v, o, dout, lse, workspace, dq, dk, dv, B: int, H: int, N: int,
     return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                          _ptr(workspace), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N),
                          int(d), float(alpha), int(causal), int(dtype), _stream(stream))
+
+
+def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int,
+                   alpha: float, causal: int, dtype: int, stream=None) -> int:
+    """Direct call of the C entry point: fa_bwd with the library's own
+    16 MiB device workspace, for callers that must not allocate (see
+    include/fa.h; overlapping calls race on that workspace)."""
+    return load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N), int(d),
+                                 float(alpha), int(causal), int(dtype), _stream(stream))
 
 
 def attention_backward(q, k, v, o, lse, dout, causal: bool = False,

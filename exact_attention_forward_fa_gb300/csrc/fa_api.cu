@@ -324,6 +324,50 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// ---------------------------------------------------------------------------
+// fa_bwd_noalloc: fa_bwd with a workspace that lives in the library image.
+// For callers that must not allocate device memory at the point of the call
+// (for example a host program whose device memory is reserved up front, or
+// a runtime that forbids allocation once a step has started); they still get
+// the backward without passing a workspace.  The workspace is a file-scope
+// device array of kNoallocWorkspaceFloats floats (16 MiB), which bounds the
+// problem: 2 * B * H * ceil(N/128) * 128 floats must fit.  Every element the
+// backward reads is first written by its preprocess in the same call, so
+// nothing needs to start at zero.  One array per device is shared by all
+// calls: calls that overlap in time (other streams, other host threads)
+// race on it.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoallocWorkspaceFloats = size_t(1) << 22;
+static __device__ __align__(256) float g_noalloc_workspace[kNoallocWorkspaceFloats];
+float *g_noalloc_ptr[kMaxDevices] = {};
+
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                         const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
+                         int H, int N, int d, float alpha, int causal, fa_dtype dtype,
+                         void *stream) {
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    const uint64_t need = 2ull * B * H * ((static_cast<uint64_t>(N) + 127) / 128) * 128;
+    if (need > kNoallocWorkspaceFloats) return FA_ERR_TOO_LARGE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    float *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_noalloc_ptr[dev] == nullptr) {
+            // this device is current: its copy of the array
+            float *p = nullptr;
+            if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_noalloc_workspace) !=
+                    cudaSuccess || p == nullptr)
+                return FA_ERR_CUDA;
+            g_noalloc_ptr[dev] = p;
+        }
+        ws = g_noalloc_ptr[dev];
+    }
+    return fa_bwd(q, k, v, o, dout, lse, ws, dq, dk, dv, B, H, N, d, alpha, causal, dtype,
+                  stream);
+}
+
 fa_status fa_check_status(void *stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
     DeviceInfo *dev = nullptr;

@@ -145,6 +145,25 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  int causal, fa_dtype dtype, void *stream);
 
 /*
+ * fa_bwd_noalloc -- fa_bwd without a caller-provided workspace (the pages
+ * have no counterpart: this is an interface convenience of this library).
+ * For callers that must not allocate device memory at the point of the
+ * call, e.g. a program whose device memory is reserved up front or a
+ * runtime that forbids allocation inside a step.  The workspace is a
+ * 16 MiB array in the library's device image (one per device, resolved
+ * once per device); nothing is allocated, and nothing in it needs to start
+ * at zero.  Limit: 2 * B * H * ceil(N/128) * 128 <= 4194304 floats, else
+ * FA_ERR_TOO_LARGE before anything runs.  Calls that overlap in time (on
+ * other streams or host threads) share the array and race; serialise them.
+ * Other arguments, results and errors as fa_bwd.
+ */
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v,
+                         const void *o, const void *dout, const float *lse,
+                         void *dq, void *dk, void *dv, int B, int H, int N,
+                         int d, float alpha, int causal, fa_dtype dtype,
+                         void *stream);
+
+/*
  * fa_check_status -- synchronizes `stream`, then reports and clears the
  * device status word of the current device.  Returns FA_ERR_TIMEOUT if a
  * kernel launched since the last check gave up on a bounded wait (its

@@ -150,6 +150,14 @@ def test_bwd_validation_codes(lib, kw, code):
     assert _bcall(lib, **kw) == code
 
 
+def test_bwd_noalloc_rejects_problems_beyond_its_workspace(lib):
+    # 2 * B * H * ceil(N/128) * 128 floats must fit the 4 Mi-float array;
+    # the check comes before any CUDA call.
+    args = [A] * 9
+    assert lib.fa_bwd_noalloc(*args, 1, 16, 131073, 128, 0.088, 0, 0, None) == fa.FA_ERR_TOO_LARGE
+    assert lib.fa_bwd_noalloc(*args, 0, 1, 128, 128, 0.088, 0, 0, None) == fa.FA_ERR_INVALID_ARG
+
+
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     import torch
     if torch.cuda.is_available():
