@@ -456,6 +456,10 @@ def run_ours(args, B, H, N, d, rank, world):
     alpha = synth.default_alpha(d)
     causal = int(args.causal)
     qh, kh, vh = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + rank, outliers=args.fp8)
+    H_kv = args.hkv or H
+    if H_kv != H:               # grouped K/V heads: K, V with H_kv heads
+        kh = torch.from_numpy(synth.normal((B, N, H_kv, d), seed=synth.BASE_SEED + rank + 1)).to(qh.dtype)
+        vh = torch.from_numpy(synth.normal((B, N, H_kv, d), seed=synth.BASE_SEED + rank + 2)).to(qh.dtype)
     q, k, v = qh.to(dev), kh.to(dev), vh.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -477,7 +481,11 @@ def run_ours(args, B, H, N, d, rank, world):
         if args.fp8:
             rc = fa.fa_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, B, H, N, d, alpha, causal, sp)
         else:
-            rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
+            if H_kv == H:
+                rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
+            else:
+                rc = fa.fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d, alpha, causal,
+                                   fa.FA_BF16, sp)
         if rc != fa.FA_OK:
             raise fa.FaError(rc, "fa_fwd")
 
@@ -556,7 +564,7 @@ def run_ours(args, B, H, N, d, rank, world):
     barrier()
     e2e_ms = reduce_max(start.elapsed_time(stop), world, dev)
     e2e_value = aggregate_value(fl, e2e_steps, e2e_ms, world)
-    h2d = 3 * qh.numel() * qh.element_size()
+    h2d = (qh.numel() + kh.numel() + vh.numel()) * qh.element_size()
     d2h = op.numel() * op.element_size() + lp.numel() * 4
 
     if rank != 0:
@@ -573,6 +581,8 @@ def run_ours(args, B, H, N, d, rank, world):
     else:
         peak, peak_kind = burst, "burst"
     wkey = config_name(B, H, N, d, args.causal, args.fp8)
+    if H_kv != H:
+        wkey = wkey.replace(f" H{H} ", f" H{H} Hkv{H_kv} ")
     line = {
         "metric": METRIC_FP8 if args.fp8 else METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world,
@@ -581,7 +591,7 @@ def run_ours(args, B, H, N, d, rank, world):
         "dtype": "e4m3" if args.fp8 else "bf16",
         "data": ("synthetic (seeded N(0,1) + 0.1% N(0,100) outliers)" if args.fp8
                  else "synthetic (seeded N(0,1) inputs)"),
-        "config": {"workload": wkey, "B": B, "H": H, "N": N, "d": d,
+        "config": {"workload": wkey, "B": B, "H": H, "H_kv": H_kv, "N": N, "d": d,
                    "causal": bool(args.causal),
                    "l2": "no flush: 192 MiB of inputs exceed the 126 MB L2",
                    "parallelism": f"replicas x{world}"},
@@ -614,6 +624,8 @@ def main():
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 e4m3 path (outlier inputs, Hadamard rotation); times "
                          "fa_fwd_fp8, reports the quantization pre-pass separately")
+    ap.add_argument("--hkv", type=int, default=0,
+                    help="grouped K/V heads (GQA/MQA, fa_fwd_gqa); default: H")
     ap.add_argument("--bwd", action="store_true",
                     help="time the backward pass (fa_bwd) instead of the forward")
     ap.add_argument("--skip-cpu", action="store_true",
@@ -627,6 +639,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.bwd and args.fp8:
         ap.error("--bwd and --fp8 are exclusive")
+    if args.hkv and (args.bwd or args.fp8 or args.H % args.hkv):
+        ap.error("--hkv applies to the BF16 forward and must divide --H")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and args.impl == "ours":

@@ -29,7 +29,7 @@ FA_BF16 = 0
 FA_FP16 = 1
 
 # Every symbol include/fa.h declares (checked by the tests).
-EXPORTS = ("fa_fwd", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_noalloc",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_noalloc",
            "fa_check_status", "fa_status_detail", "fa_status_string", "fa_version")
 
 _lib = None
@@ -54,6 +54,8 @@ def load():
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_gqa.restype = i
     lib.fa_quantize_fp8.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
     lib.fa_quantize_fp8.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
@@ -105,6 +107,15 @@ def fa_fwd(q, k, v, o, lse, B: int, H: int, N: int, d: int, alpha: float,
     return load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                          int(B), int(H), int(N), int(d), float(alpha),
                          int(causal), int(dtype), _stream(stream))
+
+
+def fa_fwd_gqa(q, k, v, o, lse, B: int, H: int, H_kv: int, N: int, d: int, alpha: float,
+               causal: int, dtype: int, stream=None) -> int:
+    """Direct call of the C entry point: K/V with H_kv heads shared by groups
+    of H / H_kv query heads (see include/fa.h)."""
+    return load().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                             int(H_kv), int(N), int(d), float(alpha), int(causal), int(dtype),
+                             _stream(stream))
 
 
 def fa_quantize_fp8(x, x8, scales, hadamard_signs, B: int, H: int, N: int,
@@ -216,7 +227,8 @@ def fa_version() -> int:
 
 def attention(q, k, v, causal: bool = False, alpha: float | None = None,
               out=None, lse=None, want_lse: bool = True, stream=None):
-    """Convenience wrapper over ``fa_fwd`` for torch tensors on the GPU.
+    """Convenience wrapper over ``fa_fwd`` for torch tensors on the GPU
+    (``fa_fwd_gqa`` when K/V have fewer heads than Q).
 
     Allocates O (and LSE) with torch when not given, launches, and raises
     FaError on a non-OK status.  Returns (O, LSE or None)."""
@@ -234,8 +246,12 @@ def attention(q, k, v, causal: bool = False, alpha: float | None = None,
         out = torch.empty_like(q)
     if lse is None and want_lse:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    rc = fa_fwd(q, k, v, out, lse, B, H, N, d, alpha, int(bool(causal)), dt,
-                stream)
+    H_kv = k.shape[2]
+    if H_kv == H:
+        rc = fa_fwd(q, k, v, out, lse, B, H, N, d, alpha, int(bool(causal)), dt, stream)
+    else:
+        rc = fa_fwd_gqa(q, k, v, out, lse, B, H, H_kv, N, d, alpha, int(bool(causal)), dt,
+                        stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
     return out, lse

@@ -108,12 +108,15 @@ const char *fa_status_string(fa_status s) {
     return "FA_ERR_UNKNOWN";
 }
 
-fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
-                 int H, int N, int d, float alpha, int causal, fa_dtype dtype,
-                 void *stream) {
+// The forward for H query heads over H_kv key/value heads (H_kv divides H;
+// query head h reads key/value head h / (H / H_kv)).
+static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int H, int H_kv, int N, int d, float alpha, int causal,
+                          fa_dtype dtype, void *stream) {
     // ---- host-side validation: nothing is launched on failure ----
     if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
     if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
@@ -141,8 +144,8 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
         dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint32_t kv_rows = d == 256 ? 64 : 128;     // key tile height
     if ((st = encode_bshd(&L.q, q, dt, B, H, N, d, 128)) != FA_OK) return st;
-    if ((st = encode_bshd(&L.k, k, dt, B, H, N, d, kv_rows)) != FA_OK) return st;
-    if ((st = encode_bshd(&L.v, v, dt, B, H, N, d, kv_rows)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.k, k, dt, B, H_kv, N, d, kv_rows)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.v, v, dt, B, H_kv, N, d, kv_rows)) != FA_OK) return st;
     L.args.o = o;
     L.args.lse = lse;
     L.args.status = dev->status;
@@ -152,6 +155,7 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
     L.args.n_kv = static_cast<int>(d == 256 ? (static_cast<uint64_t>(N) + 63) / 64 : n_qt);
     L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
     L.args.n_units = static_cast<int>(units);
+    L.args.group = H / H_kv;
     L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
     L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
     L.stream = static_cast<cudaStream_t>(stream);
@@ -161,6 +165,18 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
     cudaError_t e = (d == 64) ? fa::launch_fwd_d64(L)
                     : (d == 128) ? fa::launch_fwd_d128(L) : fa::launch_fwd_d256(L);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                 int H, int N, int d, float alpha, int causal, fa_dtype dtype,
+                 void *stream) {
+    return fwd_impl(q, k, v, o, lse, B, H, H, N, d, alpha, causal, dtype, stream);
+}
+
+fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int H, int H_kv, int N, int d, float alpha, int causal, fa_dtype dtype,
+                     void *stream) {
+    return fwd_impl(q, k, v, o, lse, B, H, H_kv, N, d, alpha, causal, dtype, stream);
 }
 
 fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
@@ -246,6 +262,7 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     L.args.n_kv = static_cast<int>(n_qt);
     L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
     L.args.n_units = static_cast<int>(units);
+    L.args.group = 1;
     L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
     L.args.q_scale = q_scale;
     L.args.k_scale = k_scale;

@@ -149,7 +149,7 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
                     tma_load_4d(tm, base + C::KV_OFF + slot * C::KV_BYTES + c * C::KV_CHUNK,
-                                bar(C::B_KVFULL + slot), c * 64, U.h, j * C::BN, U.b);
+                                bar(C::B_KVFULL + slot), c * 64, U.h / a.group, j * C::BN, U.b);
                 armed |= 1u << slot;
                 armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
                 if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }

@@ -49,6 +49,7 @@ struct FwdArgs {
     int n_kv;            // ceil(N / 128) key tiles
     int n_pairs;         // ceil(ceil(N / 128) / 2) Q-tile pairs per head
     int n_units;         // B * H * n_pairs
+    int group;           // query heads per K/V head (1: one K/V head per query head)
     float scale_log2;    // alpha * log2(e)
     // FP8 only: one FP32 scale per 128-row tile of each head, [B][H][n_kv]
     const float *q_scale, *k_scale, *v_scale;
@@ -231,7 +232,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const CUtensorMap *tm = kv ? &tm_v : &tm_k;
                         for (int c = 0; c < C::NCH; ++c)
                             tma_load_4d(tm, base + C::KV_OFF + slot * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                        bar(C::B_KVFULL + slot), c * (128 / C::ESZ), U.h, j * 128, U.b);
+                                        bar(C::B_KVFULL + slot), c * (128 / C::ESZ), U.h / a.group,
+                                        j * 128, U.b);
                         armed |= 1u << slot;
                         armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
                         if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }

@@ -77,6 +77,19 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
                  int causal, fa_dtype dtype, void *stream);
 
 /*
+ * fa_fwd_gqa -- fa_fwd with grouped key/value heads (grouped-query and
+ * multi-query attention: "FlashAttention-3 on Hopper", ch. 11 and the GQA
+ * remark of sec. 7.2.3): q, o are [B][N][H][d] as in fa_fwd, k, v are
+ * [B][N][H_kv][d], H_kv >= 1 divides H, and query head h attends with key /
+ * value head h / (H / H_kv).  H_kv = H is fa_fwd; H_kv = 1 is multi-query
+ * attention.  H % H_kv != 0 or H_kv < 1 returns FA_ERR_INVALID_ARG; other
+ * arguments, results and errors as fa_fwd.
+ */
+fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o,
+                     float *lse, int B, int H, int H_kv, int N, int d,
+                     float alpha, int causal, fa_dtype dtype, void *stream);
+
+/*
  * fa_quantize_fp8 -- FP8 pre-pass: block quantization with optional
  * incoherent processing ("FlashAttention-3 on Hopper", sec. 6.3 and 6.4).
  *   x      : device, bf16 [B][N][H][d], 16-byte aligned.

@@ -16,6 +16,8 @@ computes, and the passage it follows, is stated in ``fa_oracle.c``:
 * ``attention_online``: the tiled online recurrence with the conditional
   rescale rule, "FlashAttention-3 on Hopper" sec. 4.2 and "FlashAttention
   v1-v4" (conditional rescale).
+* ``attention_gqa``: grouped key/value heads (GQA/MQA), each query head with
+  its own key/value head h // (H / H_kv), "FlashAttention-3 on Hopper" ch. 11.
 * ``attention_bwd`` / ``attention_bwd_head``: the gradients dQ, dK, dV from
   the definition, "FlashAttention-3 on Hopper" sec. 7.1.
 * ``hadamard_rotate``, ``e4m3_encode`` / ``e4m3_decode``,
@@ -122,6 +124,21 @@ def attention(q, k, v, alpha: float, causal: bool, n_threads: int = 1):
     if rc:
         raise RuntimeError(f"oracle_attention_fwd failed ({rc})")
     return o, lse
+
+
+def attention_gqa(q, k, v, alpha: float, causal: bool, n_threads: int = 1):
+    """Grouped key/value heads: q [B,N,H,d], k/v [B,N,H_kv,d] with H_kv
+    dividing H; query head h attends with key/value head h // (H // H_kv).
+    The definition is the per-head attention with each query head's own key
+    and value head, so K and V are repeated per query head and the plain
+    definition is applied ("FlashAttention-3 on Hopper", ch. 11)."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    H, H_kv = q.shape[2], k.shape[2]
+    if H_kv < 1 or H % H_kv:
+        raise ValueError("H_kv must divide H")
+    g = H // H_kv
+    return attention(q, np.repeat(k, g, axis=2), np.repeat(v, g, axis=2), alpha, causal,
+                     n_threads)
 
 
 def attention_bwd(q, k, v, dout, alpha: float, causal: bool, n_threads: int = 1):

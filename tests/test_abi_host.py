@@ -86,6 +86,12 @@ def test_validation_codes(lib, kw, code):
     assert _call(lib, **kw) == code
 
 
+@pytest.mark.parametrize("H,H_kv,code", [(6, 4, fa.FA_ERR_INVALID_ARG), (4, 0, fa.FA_ERR_INVALID_ARG),
+                                         (4, 8, fa.FA_ERR_INVALID_ARG)])
+def test_gqa_validation_codes(lib, H, H_kv, code):
+    assert lib.fa_fwd_gqa(A, A, A, A, None, 1, H, H_kv, 128, 64, 0.125, 0, 0, None) == code
+
+
 def _qcall(lib, x=A, x8=A, sc=A, signs=None, B=1, H=1, N=128, d=128):
     return lib.fa_quantize_fp8(x, x8, sc, signs, B, H, N, d, None)
 

@@ -394,3 +394,28 @@ def test_bwd_planted_mistakes_are_caught():
     assert not _fd_agrees(oracle.attention_bwd_head(q, k, v, dout, 1.0, True), fd)
     # mask ignored
     assert not _fd_agrees(oracle.attention_bwd_head(q, k, v, dout, a, False), fd)
+
+
+# ---------------------------------------------------------------------------
+# Grouped key/value heads ("FlashAttention-3 on Hopper", ch. 11)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,H_kv", [(4, 4), (4, 2), (6, 3), (4, 1)])
+def test_gqa_maps_query_head_to_its_kv_head(H, H_kv):
+    # Each query head h must attend with key/value head h // (H // H_kv):
+    # checked head by head against the one-head definition (a mapping by
+    # h % H_kv, or a shared head for all, fails this).
+    B, N, d = 2, 9, 3
+    q = _rand(B, N, H, d)
+    k, v = _rand(B, N, H_kv, d), _rand(B, N, H_kv, d)
+    a = 0.7
+    for causal in (False, True):
+        o, lse = oracle.attention_gqa(q, k, v, a, causal)
+        g = H // H_kv
+        for b in range(B):
+            for h in range(H):
+                oh, lh = oracle.attention_head(q[b, :, h], k[b, :, h // g], v[b, :, h // g],
+                                               a, causal)
+                assert np.array_equal(o[b, :, h], oh) and np.array_equal(lse[b, h], lh)
+    with pytest.raises(ValueError):
+        oracle.attention_gqa(q, _rand(B, N, H + 1, d), _rand(B, N, H + 1, d), a, False)

@@ -209,3 +209,27 @@ def test_outputs_beyond_n_untouched(gpu_lib):
     assert rc == fa.FA_OK and fa.fa_check_status() == fa.FA_OK
     assert torch.all(big[:, N:] == 7.0)
     assert torch.all(lse[:, :, N:] == 9.0)
+
+
+GQA_CASES = [
+    # (B, H, H_kv, N, d, causal)
+    (2, 8, 2, 1000, 128, True),
+    (2, 8, 2, 1000, 128, False),
+    (1, 8, 1, 513, 64, True),           # multi-query
+    (1, 6, 3, 257, 64, False),
+    (1, 4, 2, 300, 256, True),
+    (1, 4, 1, 129, 256, False),
+]
+
+
+@pytest.mark.parametrize("B,H,H_kv,N,d,causal", GQA_CASES)
+def test_gqa_parity(gpu_lib, B, H, H_kv, N, d, causal):
+    # Grouped key/value heads: query head h attends with K/V head
+    # h // (H // H_kv) ("FlashAttention-3 on Hopper", ch. 11).
+    q = torch.from_numpy(synth.normal((B, N, H, d), seed=N + 1)).to(torch.bfloat16)
+    k = torch.from_numpy(synth.normal((B, N, H_kv, d), seed=N + 2)).to(torch.bfloat16)
+    v = torch.from_numpy(synth.normal((B, N, H_kv, d), seed=N + 3)).to(torch.bfloat16)
+    a = synth.default_alpha(d)
+    o, lse = _run(gpu_lib, q, k, v, causal, a)
+    o_ref, lse_ref = oracle.attention_gqa(q, k, v, a, causal, n_threads=THREADS)
+    _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref)
