@@ -465,6 +465,11 @@ def run_ours(args, B, H, N, d, rank, world):
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
+    n_splits = 0
+    if args.splits is not None:     # split key ranges: partials + combine
+        n_splits = args.splits or fa.fa_splitkv_auto(B, H, N, d)
+        ws = torch.empty((fa.fa_splitkv_workspace_floats(B, H, N, d, n_splits),),
+                         dtype=torch.float32, device=dev)
     if args.fp8:
         signs = torch.from_numpy(synth.hadamard_signs(d)).to(dev)
         nt = (N + 127) // 128
@@ -481,7 +486,10 @@ def run_ours(args, B, H, N, d, rank, world):
         if args.fp8:
             rc = fa.fa_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, B, H, N, d, alpha, causal, sp)
         else:
-            if H_kv == H:
+            if n_splits:
+                rc = fa.fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16,
+                                       n_splits, ws, sp)
+            elif H_kv == H:
                 rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
             else:
                 rc = fa.fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d, alpha, causal,
@@ -583,6 +591,8 @@ def run_ours(args, B, H, N, d, rank, world):
     wkey = config_name(B, H, N, d, args.causal, args.fp8)
     if H_kv != H:
         wkey = wkey.replace(f" H{H} ", f" H{H} Hkv{H_kv} ")
+    if n_splits:
+        wkey += f" split-KV x{n_splits}"
     line = {
         "metric": METRIC_FP8 if args.fp8 else METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world,
@@ -606,7 +616,7 @@ def run_ours(args, B, H, N, d, rank, world):
                      "traffic": profiled_traffic(wkey)},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if n_splits else 1),
         "clocks": clk.summary(),
     }
     if not args.skip_cpu:
@@ -624,6 +634,9 @@ def main():
     ap.add_argument("--fp8", action="store_true",
                     help="FP8 e4m3 path (outlier inputs, Hadamard rotation); times "
                          "fa_fwd_fp8, reports the quantization pre-pass separately")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="split-KV forward (fa_fwd_splitkv) with this many key splits "
+                         "(0: the library's choice for the device)")
     ap.add_argument("--hkv", type=int, default=0,
                     help="grouped K/V heads (GQA/MQA, fa_fwd_gqa); default: H")
     ap.add_argument("--bwd", action="store_true",
@@ -641,6 +654,8 @@ def main():
         ap.error("--bwd and --fp8 are exclusive")
     if args.hkv and (args.bwd or args.fp8 or args.H % args.hkv):
         ap.error("--hkv applies to the BF16 forward and must divide --H")
+    if args.splits is not None and (args.bwd or args.fp8 or args.hkv or args.d not in (64, 128)):
+        ap.error("--splits applies to the BF16 forward, d 64 or 128, without --hkv")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and args.impl == "ours":

@@ -29,7 +29,8 @@ FA_BF16 = 0
 FA_FP16 = 1
 
 # Every symbol include/fa.h declares (checked by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_noalloc",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_splitkv_workspace_floats",
+           "fa_splitkv_auto", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_noalloc",
            "fa_check_status", "fa_status_detail", "fa_status_string", "fa_version")
 
 _lib = None
@@ -56,6 +57,12 @@ def load():
     lib.fa_fwd.restype = i
     lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_gqa.restype = i
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp, vp]
+    lib.fa_fwd_splitkv.restype = i
+    lib.fa_splitkv_workspace_floats.argtypes = [i, i, i, i, i]
+    lib.fa_splitkv_workspace_floats.restype = ctypes.c_longlong
+    lib.fa_splitkv_auto.argtypes = [i, i, i, i]
+    lib.fa_splitkv_auto.restype = i
     lib.fa_quantize_fp8.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
     lib.fa_quantize_fp8.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
@@ -116,6 +123,44 @@ def fa_fwd_gqa(q, k, v, o, lse, B: int, H: int, H_kv: int, N: int, d: int, alpha
     return load().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
                              int(H_kv), int(N), int(d), float(alpha), int(causal), int(dtype),
                              _stream(stream))
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B: int, H: int, N: int, d: int, alpha: float, causal: int,
+                   dtype: int, n_splits: int, workspace, stream=None) -> int:
+    """Direct call of the C entry point (see include/fa.h)."""
+    return load().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                                 int(N), int(d), float(alpha), int(causal), int(dtype),
+                                 int(n_splits), _ptr(workspace), _stream(stream))
+
+
+def fa_splitkv_workspace_floats(B: int, H: int, N: int, d: int, n_splits: int) -> int:
+    return load().fa_splitkv_workspace_floats(int(B), int(H), int(N), int(d), int(n_splits))
+
+
+def fa_splitkv_auto(B: int, H: int, N: int, d: int) -> int:
+    return load().fa_splitkv_auto(int(B), int(H), int(N), int(d))
+
+
+def attention_splitkv(q, k, v, causal: bool = False, alpha: float | None = None,
+                      n_splits: int = 0, want_lse: bool = True, stream=None):
+    """Split-KV forward for torch tensors on the GPU (n_splits 0: the
+    library's choice for this device).  Returns (O, LSE or None)."""
+    import torch
+    dt = FA_BF16 if q.dtype == torch.bfloat16 else FA_FP16
+    B, N, H, d = q.shape
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    if n_splits <= 0:
+        n_splits = fa_splitkv_auto(B, H, N, d)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if want_lse else None
+    ws = torch.empty((fa_splitkv_workspace_floats(B, H, N, d, n_splits),), dtype=torch.float32,
+                     device=q.device)
+    rc = fa_fwd_splitkv(q, k, v, out, lse, B, H, N, d, alpha, int(bool(causal)), dt, n_splits,
+                        ws, stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_splitkv")
+    return out, lse
 
 
 def fa_quantize_fp8(x, x8, scales, hadamard_signs, B: int, H: int, N: int,

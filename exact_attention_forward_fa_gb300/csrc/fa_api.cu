@@ -156,6 +156,7 @@ static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, 
     L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
     L.args.n_units = static_cast<int>(units);
     L.args.group = H / H_kv;
+    L.args.n_splits = 1;
     L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
     L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
     L.stream = static_cast<cudaStream_t>(stream);
@@ -177,6 +178,112 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float
                      int H, int H_kv, int N, int d, float alpha, int causal, fa_dtype dtype,
                      void *stream) {
     return fwd_impl(q, k, v, o, lse, B, H, H_kv, N, d, alpha, causal, dtype, stream);
+}
+
+// Split-KV: workspace floats for S splits (partial O in FP32 plus LSE).
+static uint64_t splitkv_floats(uint64_t B, uint64_t H, uint64_t N, uint64_t d, uint64_t S) {
+    return S * B * N * H * d + S * B * H * N;
+}
+
+long long fa_splitkv_workspace_floats(int B, int H, int N, int d, int n_splits) {
+    if (B < 1 || H < 1 || N < 1 || d < 1 || n_splits < 1) return -1;
+    return static_cast<long long>(splitkv_floats(B, H, N, d, n_splits));
+}
+
+int fa_splitkv_auto(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 1;
+    DeviceInfo *dev = nullptr;
+    if (get_device(&dev) != FA_OK) return 1;
+    const long long n_kv = (N + 127) / 128;
+    const long long units = static_cast<long long>(B) * H * ((n_kv + 1) / 2);
+    const long long sm = dev->sm_count;
+    // Measured on GB300: splitting pays only while every split unit still
+    // runs in one wave -- a second wave repeats each unit's fixed cost.  So:
+    // the fewest splits that occupy >= 80 % of the SMs, at most one wave,
+    // at least 4 key tiles per split, at most 16.
+    if (units * 5 >= sm * 4) return 1;
+    long long s = (sm * 4 + units * 5 - 1) / (units * 5);
+    s = s < sm / units ? s : sm / units;
+    s = s < n_kv / 4 ? s : n_kv / 4;
+    s = s < 16 ? s : 16;
+    return static_cast<int>(s < 1 ? 1 : s);
+}
+
+fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int H, int N, int d, float alpha, int causal, fa_dtype dtype,
+                         int n_splits, float *workspace, void *stream) {
+    // ---- host-side validation: nothing is launched on failure ----
+    if (!q || !k || !v || !o || !workspace) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (n_splits < 1 || n_splits > 16) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace))
+        return FA_ERR_MISALIGNED;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_MISALIGNED;
+    const uint64_t batch_stride = 2ull * d * H * static_cast<uint64_t>(N);
+    if (batch_stride >= (1ull << 40)) return FA_ERR_TOO_LARGE;
+    const uint64_t n_qt = (static_cast<uint64_t>(N) + 127) / 128;
+    const uint64_t units = static_cast<uint64_t>(n_splits) * B * H * ((n_qt + 1) / 2);
+    if (units > 0x7fffffffull ||
+        splitkv_floats(B, H, N, d, n_splits) > 0x3fffffffffffull)
+        return FA_ERR_TOO_LARGE;
+
+    DeviceInfo *dev = nullptr;
+    fa_status st = get_device(&dev);
+    if (st != FA_OK) return st;
+
+    fa::FwdLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const CUtensorMapDataType dt =
+        dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if ((st = encode_bshd(&L.q, q, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.k, k, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.v, v, dt, B, H, N, d, 128)) != FA_OK) return st;
+    float *o_part = workspace;
+    float *lse_part = workspace + static_cast<size_t>(n_splits) * B * N * H * d;
+    L.args.o = o;
+    L.args.lse = nullptr;
+    L.args.status = dev->status;
+    L.args.B = B;
+    L.args.H = H;
+    L.args.N = N;
+    L.args.n_kv = static_cast<int>(n_qt);
+    L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
+    L.args.n_units = static_cast<int>(units);
+    L.args.group = 1;
+    L.args.n_splits = n_splits;
+    L.args.o_part = o_part;
+    L.args.lse_part = lse_part;
+    L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
+    L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.causal = causal != 0;
+    L.bf16 = dtype == FA_BF16;
+    L.d64 = d == 64;
+    cudaError_t e = fa::launch_fwd_split(L);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+
+    fa::CombineArgs c;
+    c.o_part = o_part;
+    c.lse_part = lse_part;
+    c.o = o;
+    c.lse = lse;
+    c.B = B;
+    c.H = H;
+    c.N = N;
+    c.d = d;
+    c.S = n_splits;
+    c.n_kv = static_cast<int>(n_qt);
+    c.causal = causal;
+    c.bf16 = dtype == FA_BF16;
+    const uint64_t rows = static_cast<uint64_t>(B) * N * H;
+    const uint64_t g = (rows + 7) / 8;                 // 8 rows (warps) per CTA
+    const uint64_t gcap = 16ull * dev->sm_count;
+    e = fa::launch_combine(c, static_cast<int>(g < gcap ? g : gcap), L.stream);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
@@ -263,6 +370,7 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
     L.args.n_units = static_cast<int>(units);
     L.args.group = 1;
+    L.args.n_splits = 1;
     L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
     L.args.q_scale = q_scale;
     L.args.k_scale = k_scale;

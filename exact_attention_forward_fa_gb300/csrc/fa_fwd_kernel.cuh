@@ -50,6 +50,12 @@ struct FwdArgs {
     int n_pairs;         // ceil(ceil(N / 128) / 2) Q-tile pairs per head
     int n_units;         // B * H * n_pairs
     int group;           // query heads per K/V head (1: one K/V head per query head)
+    // Split key ranges (d <= 128, 16-bit): n_splits >= 1; with o_part set,
+    // split s of a unit writes its partial O (FP32, normalised by its own
+    // row sum) to o_part [S][B][N][H][D] and its LSE to lse_part [S][B][H][N]
+    // instead of O and LSE.
+    int n_splits;
+    float *o_part, *lse_part;
     float scale_log2;    // alpha * log2(e)
     // FP8 only: one FP32 scale per 128-row tile of each head, [B][H][n_kv]
     const float *q_scale, *k_scale, *v_scale;
@@ -119,15 +125,22 @@ struct FwdCfg {
 struct Unit {
     int b, h;
     int m[2];       // Q tile indices (L, H)
-    bool act[2];    // tile holds at least one real row
-    int T;          // key tiles visited (descending from T-1 to 0)
+    bool act[2];    // tile takes part in this unit (real rows, keys in range)
+    int T;          // key tiles visited: jhi-1 down to jhi-T
+    int jhi;        // one past the unit's highest key tile
     int t0[2];      // first step at which tile X takes part (T if never)
+    int s;          // split of the key range
 };
 
-template <bool kCausal>
+// kSplit: the key range is cut into a.n_splits parts (otherwise one part,
+// folded away at compile time).
+template <bool kCausal, bool kSplit>
 __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     Unit U;
     const int BH = a.B * a.H;
+    const int S = kSplit ? a.n_splits : 1;
+    U.s = kSplit ? u % S : 0;       // the splits of one pair are adjacent units
+    if (kSplit) u /= S;
     int p, bh;
     if (kCausal) {          // longest-first: the last pairs of every head first
         p = a.n_pairs - 1 - u / BH;
@@ -144,12 +157,20 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
         U.act[x] = U.m[x] * 128 < a.N;
         hi[x] = U.act[x] ? (kCausal ? min(a.n_kv, U.m[x] + 1) : a.n_kv) : 0;
     }
-    U.T = max(hi[0], hi[1]);
-    for (int x = 0; x < 2; ++x) U.t0[x] = U.act[x] ? U.T - hi[x] : U.T;
+    // split s of the pair's key range [0, Tf): tiles [Tf s / S, Tf (s+1) / S)
+    const int Tf = max(hi[0], hi[1]);
+    const int lo = kSplit ? Tf * U.s / S : 0;
+    U.jhi = kSplit ? Tf * (U.s + 1) / S : Tf;
+    U.T = U.jhi - lo;
+    for (int x = 0; x < 2; ++x) {
+        const int cnt = max(0, min(hi[x], U.jhi) - lo);
+        U.act[x] = cnt > 0;
+        U.t0[x] = U.T - cnt;
+    }
     return U;
 }
 
-template <int D, bool kCausal, bool kBF16, bool kFP8 = false>
+template <int D, bool kCausal, bool kBF16, bool kFP8 = false, bool kSplit = false>
 __global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k,
@@ -220,11 +241,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 return true;
             };
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-                const Unit U = make_unit<kCausal>(u, a);
+                const Unit U = make_unit<kCausal, kSplit>(u, a);
                 if (U.act[0]) ok = ok && load_q(0, U, qn0);
                 if (U.act[1]) ok = ok && load_q(1, U, qn1);
+                const int hk = U.h / a.group;        // K/V head of this query head
                 for (int t = 0; t < U.T && ok; ++t) {
-                    const int j = U.T - 1 - t;
+                    const int j = U.jhi - 1 - t;
                     for (int kv = 0; kv < 2; ++kv) {
                         ok = mbar_wait(bar(C::B_KVEMPTY + slot), phase ^ 1, w, 2);
                         if (!ok) break;
@@ -232,8 +254,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const CUtensorMap *tm = kv ? &tm_v : &tm_k;
                         for (int c = 0; c < C::NCH; ++c)
                             tma_load_4d(tm, base + C::KV_OFF + slot * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                        bar(C::B_KVFULL + slot), c * (128 / C::ESZ), U.h / a.group,
-                                        j * 128, U.b);
+                                        bar(C::B_KVFULL + slot), c * (128 / C::ESZ), hk, j * 128, U.b);
                         armed |= 1u << slot;
                         armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
                         if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
@@ -257,7 +278,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint32_t slot = 0, phase = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-                const Unit U = make_unit<kCausal>(u, a);
+                const Unit U = make_unit<kCausal, kSplit>(u, a);
                 for (int t = 0; t <= U.T && ok; ++t) {
                     const bool has_v = t > 0, has_k = t < U.T;
                     uint32_t vslot = 0, vph = 0, kslot = 0, kph = 0;
@@ -349,7 +370,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         uint32_t sph = 0, oph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-            const Unit U = make_unit<kCausal>(u, a);
+            const Unit U = make_unit<kCausal, kSplit>(u, a);
             const bool act = x ? U.act[1] : U.act[0];
             if (!act) continue;
             const int mt = x ? U.m[1] : U.m[0];
@@ -371,7 +392,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             // as the P V product sees them (normalises O; 16-bit P only).
             float r = -INFINITY, le = 0.f, lr = 0.f;
             for (int t = t0; t < U.T; ++t) {
-                const int j = U.T - 1 - t;
+                const int j = U.jhi - 1 - t;
                 ok = mbar_wait(bar(C::B_SFULL + x), sph, w, 20);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 sph ^= 1;
@@ -536,6 +557,21 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + x));
+            if constexpr (kSplit) {
+                // split key range: FP32 partial O and its LSE
+                if (grow < a.N) {
+                    float *prow = a.o_part +
+                        (((static_cast<size_t>(U.s) * a.B + U.b) * a.N + grow) * a.H + U.h) * D;
+#pragma unroll
+                    for (int ch = 0; ch < D / 4; ++ch)
+                        reinterpret_cast<float4 *>(prow)[ch] = make_float4(
+                            __uint_as_float(ov[4 * ch]) * inv, __uint_as_float(ov[4 * ch + 1]) * inv,
+                            __uint_as_float(ov[4 * ch + 2]) * inv, __uint_as_float(ov[4 * ch + 3]) * inv);
+                    a.lse_part[((static_cast<size_t>(U.s) * a.B + U.b) * a.H + U.h) * a.N + grow] =
+                        live ? (r + log2f(le)) * 0.69314718055994530942f : -INFINITY;
+                }
+                continue;
+            }
             if (grow < a.N) {
 #pragma unroll
                 for (int ch = 0; ch < D / 8; ++ch) {

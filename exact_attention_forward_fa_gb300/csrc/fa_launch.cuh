@@ -18,12 +18,25 @@ struct FwdLaunch {
     cudaStream_t stream;
     bool causal;
     bool bf16;
+    bool d64;              // split path only: head dim 64 (else 128)
 };
 
 cudaError_t launch_fwd_d64(const FwdLaunch &L);
 cudaError_t launch_fwd_d128(const FwdLaunch &L);
 cudaError_t launch_fwd_d256(const FwdLaunch &L);   // K/V maps with 64-row boxes
 cudaError_t launch_fwd_fp8(const FwdLaunch &L);    // e4m3 maps, 128-byte boxes
+cudaError_t launch_fwd_split(const FwdLaunch &L);  // split key ranges, d in {64, 128}
+// Split-KV combine: O, LSE from S partials (o_part [S][B][N][H][d] FP32,
+// lse_part [S][B][H][N]); d in {64, 128}.
+struct CombineArgs {
+    const float *o_part, *lse_part;
+    void *o;
+    float *lse;
+    int B, H, N, d, S, n_kv, causal;
+    bool bf16;
+};
+cudaError_t launch_combine(const CombineArgs &a, int grid, cudaStream_t stream);
+
 // Backward: maps {d, H, N, B} with box {64, 1, 128, 1} (128-byte swizzle)
 // for Q, K, V and dO; grid = persistent CTAs of both main kernels.
 struct BwdLaunch {
@@ -58,10 +71,10 @@ cudaError_t launch_quantize(const QuantLaunch &L);
 
 // Shared helper: set the dynamic shared-memory limit once per device, then
 // launch one instantiation.
-template <int D, bool kCausal, bool kBF16, bool kFP8 = false>
+template <int D, bool kCausal, bool kBF16, bool kFP8 = false, bool kSplit = false>
 cudaError_t launch_fwd_inst(const FwdLaunch &L) {
     using Cfg = FwdCfg<D, kCausal, kBF16, kFP8>;
-    auto kern = fa_fwd_kernel<D, kCausal, kBF16, kFP8>;
+    auto kern = fa_fwd_kernel<D, kCausal, kBF16, kFP8, kSplit>;
     static unsigned long long configured = 0ull;   // bit per device id (< 64)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -103,6 +116,16 @@ cudaError_t launch_fwd_dispatch(const FwdLaunch &L) {
         return L.bf16 ? launch_fwd_inst<D, true, true>(L) : launch_fwd_inst<D, true, false>(L);
     }
     return L.bf16 ? launch_fwd_inst<D, false, true>(L) : launch_fwd_inst<D, false, false>(L);
+}
+
+// Split key ranges (partials + combine), d in {64, 128}.
+template <int D>
+cudaError_t launch_fwd_split_dispatch(const FwdLaunch &L) {
+    if (L.causal)
+        return L.bf16 ? launch_fwd_inst<D, true, true, false, true>(L)
+                      : launch_fwd_inst<D, true, false, false, true>(L);
+    return L.bf16 ? launch_fwd_inst<D, false, true, false, true>(L)
+                  : launch_fwd_inst<D, false, false, false, true>(L);
 }
 
 }  // namespace fa

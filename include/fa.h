@@ -90,6 +90,35 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o,
                      float alpha, int causal, fa_dtype dtype, void *stream);
 
 /*
+ * fa_fwd_splitkv -- fa_fwd with each work unit's key range cut into
+ * n_splits parts ("FlashAttention-3 on Hopper", ch. 10: split-KV and its
+ * combine kernel), for problems whose B * H * ceil(N/256) units do not
+ * fill the GPU.  Every split writes its partial O (FP32, normalised over
+ * its own keys) and LSE into `workspace`; a combine kernel then writes
+ *   LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s
+ * to o (dtype) and lse (if not NULL).
+ *   workspace : device, fa_splitkv_workspace_floats(B, H, N, d, n_splits)
+ *            floats, 16-byte aligned, caller-owned; nothing in it needs to
+ *            start at zero.
+ *   n_splits in [1, 16] (FA_ERR_INVALID_ARG otherwise); d in {64, 128}
+ *   (others FA_ERR_UNSUPPORTED).  Other arguments and errors as fa_fwd.
+ */
+fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o,
+                         float *lse, int B, int H, int N, int d, float alpha,
+                         int causal, fa_dtype dtype, int n_splits,
+                         float *workspace, void *stream);
+
+/* fa_splitkv_workspace_floats -- workspace size of fa_fwd_splitkv, in
+ * floats: n_splits * (B*N*H*d + B*H*N); -1 for a non-positive argument. */
+long long fa_splitkv_workspace_floats(int B, int H, int N, int d, int n_splits);
+
+/* fa_splitkv_auto -- a split count for the current device: with
+ * u = B * H * ceil(ceil(N/128)/2) work units, 1 when u already occupies 80 %
+ * of the SMs, else the fewest splits S with S u >= 80 % of the SMs, keeping
+ * S u within one wave, at least 4 key tiles per split and S <= 16. */
+int fa_splitkv_auto(int B, int H, int N, int d);
+
+/*
  * fa_quantize_fp8 -- FP8 pre-pass: block quantization with optional
  * incoherent processing ("FlashAttention-3 on Hopper", sec. 6.3 and 6.4).
  *   x      : device, bf16 [B][N][H][d], 16-byte aligned.

@@ -92,6 +92,30 @@ def test_gqa_validation_codes(lib, H, H_kv, code):
     assert lib.fa_fwd_gqa(A, A, A, A, None, 1, H, H_kv, 128, 64, 0.125, 0, 0, None) == code
 
 
+def _scall(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=1, N=128, d=128, alpha=0.088, causal=0,
+           dtype=0, S=2, ws=A):
+    return lib.fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, alpha, causal, dtype, S, ws, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=None), fa.FA_ERR_INVALID_ARG),
+    (dict(S=0), fa.FA_ERR_INVALID_ARG),
+    (dict(S=17), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(ws=A + 4), fa.FA_ERR_MISALIGNED),
+    (dict(o=A + 2), fa.FA_ERR_MISALIGNED),
+])
+def test_splitkv_validation_codes(lib, kw, code):
+    assert _scall(lib, **kw) == code
+
+
+def test_splitkv_workspace_size(lib):
+    assert fa.fa_splitkv_workspace_floats(2, 3, 100, 64, 4) == 4 * (2 * 100 * 3 * 64 + 2 * 3 * 100)
+    assert fa.fa_splitkv_workspace_floats(1, 1, 1, 64, 0) == -1
+    assert 1 <= fa.fa_splitkv_auto(1, 1, 128, 128) <= 16
+
+
 def _qcall(lib, x=A, x8=A, sc=A, signs=None, B=1, H=1, N=128, d=128):
     return lib.fa_quantize_fp8(x, x8, sc, signs, B, H, N, d, None)
 

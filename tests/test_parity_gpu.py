@@ -233,3 +233,39 @@ def test_gqa_parity(gpu_lib, B, H, H_kv, N, d, causal):
     o, lse = _run(gpu_lib, q, k, v, causal, a)
     o_ref, lse_ref = oracle.attention_gqa(q, k, v, a, causal, n_threads=THREADS)
     _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref)
+
+
+SPLIT_CASES = [
+    # (B, H, N, d, causal, n_splits)
+    (1, 2, 1000, 128, True, 3),
+    (1, 2, 1000, 128, False, 2),
+    (2, 1, 777, 64, True, 5),
+    (1, 1, 300, 64, False, 4),
+    (1, 1, 128, 128, False, 2),        # one key tile: one split holds nothing
+    (1, 3, 4096, 128, True, 7),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,causal,S", SPLIT_CASES)
+def test_splitkv_parity(gpu_lib, B, H, N, d, causal, S):
+    # Split-KV ("FlashAttention-3 on Hopper", ch. 10): partials over split
+    # key ranges, merged by their LSEs, equal the one-pass definition.
+    q, k, v = synth.qkv(B, H, N, d, seed=N + S)
+    a = synth.default_alpha(d)
+    dev = torch.device("cuda")
+    o, lse = gpu_lib.attention_splitkv(q.to(dev), k.to(dev), v.to(dev), causal=causal,
+                                       alpha=a, n_splits=S)
+    assert gpu_lib.fa_check_status() == gpu_lib.FA_OK
+    o_ref, lse_ref = oracle.attention(q, k, v, a, causal, n_threads=THREADS)
+    _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref)
+
+
+def test_splitkv_one_split_equals_fa_fwd(gpu_lib):
+    # One split is the whole key range: the combine weight is exactly 1, so
+    # the result is fa_fwd's, bit for bit.
+    B, H, N, d = 2, 2, 700, 128
+    q, k, v = (x.cuda() for x in synth.qkv(B, H, N, d, seed=3))
+    for causal in (False, True):
+        o1, l1 = gpu_lib.attention(q, k, v, causal=causal)
+        o2, l2 = gpu_lib.attention_splitkv(q, k, v, causal=causal, n_splits=1)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2)
