@@ -18,6 +18,10 @@ computes, and the passage it follows, is stated in ``fa_oracle.c``:
   v1-v4" (conditional rescale).
 * ``attention_gqa``: grouped key/value heads (GQA/MQA), each query head with
   its own key/value head h // (H / H_kv), "FlashAttention-3 on Hopper" ch. 11.
+* ``attention_ext`` / ``attention_ext_head``: the variants -- local
+  (sliding-window) masks, tanh softcap and a per-head sink logit,
+  "FlashAttention-3 on Hopper" sec. 4.6 (sinks) and 4.7 (local masks,
+  transform before mask), "03 FA3" sec. 5 (softcap).
 * ``attention_bwd`` / ``attention_bwd_head``: the gradients dQ, dK, dV from
   the definition, "FlashAttention-3 on Hopper" sec. 7.1.
 * ``hadamard_rotate``, ``e4m3_encode`` / ``e4m3_decode``,
@@ -85,6 +89,17 @@ def _load():
         ctypes.c_int, _ip, _ip, ctypes.c_int, ctypes.c_double, _dp,
         ctypes.c_long, _dp, ctypes.POINTER(ctypes.c_long)]
     lib.oracle_attention_online_head.restype = ctypes.c_int
+    lib.oracle_attention_ext_head.argtypes = [
+        _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_long, ctypes.c_long, ctypes.c_long, ctypes.c_double,
+        ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _ip, ctypes.c_int,
+        _dp, ctypes.c_long, _dp]
+    lib.oracle_attention_ext_head.restype = ctypes.c_int
+    lib.oracle_attention_ext_fwd.argtypes = [
+        _dp, _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+        ctypes.c_double, _dp, ctypes.c_int]
+    lib.oracle_attention_ext_fwd.restype = ctypes.c_int
     lib.oracle_hadamard_rotate.argtypes = [
         _dp, _dp, ctypes.c_long, ctypes.c_int, ctypes.c_long, _dp]
     lib.oracle_hadamard_rotate.restype = ctypes.c_int
@@ -139,6 +154,74 @@ def attention_gqa(q, k, v, alpha: float, causal: bool, n_threads: int = 1):
     g = H // H_kv
     return attention(q, np.repeat(k, g, axis=2), np.repeat(v, g, axis=2), alpha, causal,
                      n_threads)
+
+
+def attention_ext(q, k, v, alpha: float, window=(-1, -1), softcap: float = 0.0,
+                  sinks=None, n_threads: int = 1):
+    """The variants on [B,N,H,d] tensors: window = (wl, wr) hides key j from
+    query i when j > i + wr (wr >= 0) or j < i - wl (wl >= 0), -1 = no bound;
+    softcap c > 0 replaces each visible score s by c tanh(s / c); sinks [H]
+    (or None) is one extra logit per head in every row's softmax denominator.
+    k, v may have H_kv heads dividing H (query head h uses h // (H / H_kv)).
+    Returns O [B,N,H,d] and LSE [B,H,N] in float64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, H, d = q.shape
+    H_kv = k.shape[2]
+    if H_kv < 1 or H % H_kv:
+        raise ValueError("H_kv must divide H")
+    if H_kv != H:
+        k = np.ascontiguousarray(np.repeat(k, H // H_kv, axis=2))
+        v = np.ascontiguousarray(np.repeat(v, H // H_kv, axis=2))
+    o = np.zeros_like(q)
+    lse = np.zeros((B, H, N), dtype=np.float64)
+    sk = None if sinks is None else np.ascontiguousarray(_f64(sinks).reshape(H))
+    wl, wr = int(window[0]), int(window[1])
+    rc = _load().oracle_attention_ext_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d, float(alpha),
+        wl, wr, float(softcap), _ptr(sk) if sk is not None else None,
+        int(n_threads))
+    if rc:
+        raise RuntimeError(f"oracle_attention_ext_fwd failed ({rc})")
+    return o, lse
+
+
+def attention_ext_head(q, k, v, alpha: float, window=(-1, -1),
+                       softcap: float = 0.0, sink=None, rows=None):
+    """One head of ``attention_ext``: q [Nq,d], k/v [Nk,d], sink a scalar or
+    None; the diagonal is bottom-right aligned, i + (Nk - Nq).  With ``rows``
+    only those query rows are computed."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    Nq, d = q.shape
+    Nk = k.shape[0]
+    if rows is None:
+        n, rows_arr = Nq, None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+        n = len(rows_arr)
+    o = np.zeros((n, d), dtype=np.float64)
+    lse = np.zeros((n,), dtype=np.float64)
+    sk = None if sink is None else np.array([float(sink)], dtype=np.float64)
+    rc = _load().oracle_attention_ext_head(
+        _ptr(q), _ptr(k), _ptr(v), Nq, Nk, d, d, d, d, float(alpha),
+        int(window[0]), int(window[1]), float(softcap),
+        _ptr(sk) if sk is not None else None,
+        rows_arr.ctypes.data_as(_ip) if rows_arr is not None else None, n,
+        _ptr(o), d, _ptr(lse))
+    if rc:
+        raise RuntimeError(f"oracle_attention_ext_head failed ({rc})")
+    return o, lse
+
+
+def attention_ext_rows(q, k, v, alpha: float, b: int, h: int, rows,
+                       window=(-1, -1), softcap: float = 0.0, sinks=None):
+    """Rows ``rows`` of head (b, h) of [B,N,H,d] tensors with the variants;
+    k, v may have fewer (grouped) heads."""
+    H, H_kv = q.shape[2], k.shape[2]
+    hk = h // (H // H_kv)
+    sink = None if sinks is None else float(_f64(sinks).reshape(-1)[h])
+    return attention_ext_head(_f64(q[b, :, h, :]), _f64(k[b, :, hk, :]),
+                              _f64(v[b, :, hk, :]), alpha, window, softcap, sink,
+                              rows)
 
 
 def attention_bwd(q, k, v, dout, alpha: float, causal: bool, n_threads: int = 1):

@@ -24,7 +24,11 @@
  *           section "conditional rescale" (reference point r, threshold tau,
  *           LSE = r ln2 + ln l_r).
  *   [FA3A]  "03 FA3: Hopper asynchrony and overlap" (llm-infra-atlas), sec. 4
- *           FP8: per-tile scales folded into the softmax scale.
+ *           FP8: per-tile scales folded into the softmax scale; sec. 5
+ *           softcap s' = c tanh(s / c) on the scaled scores.
+ *   Variants ([FA3H] sec. 4.6 learnable sinks folded into the row sum,
+ *           sec. 4.7 local (sliding-window) masks with a left boundary,
+ *           and the order transform-then-mask).
  *
  * Layout conventions (chosen by this library, stated in include/fa.h):
  *   Q, K, V, O rows are addressed through a leading dimension (element
@@ -189,6 +193,159 @@ int oracle_attention_fwd(const double *q, const double *k, const double *v,
         ++started;
     }
     if (started == 0) fwd_worker(&J);
+    for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+    return J.err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Score and mask variants, one head ([FA3H] sec. 4.6 "learnable sinks",     */
+/* sec. 4.7 local attention and the rule that a score transformation comes   */
+/* before the final mask; [FA3A] sec. 5 softcap).                            */
+/*                                                                           */
+/* Visibility, with the diagonal bottom-right aligned, diag = i + (Nk - Nq): */
+/*   key j is hidden from query i when j > diag + wr (right window, wr >= 0) */
+/*   or when j < diag - wl (left window, wl >= 0); -1 means no bound on that */
+/*   side.  (wl, wr) = (-1, 0) is the causal mask, (-1, -1) no mask.         */
+/* Scores, for visible keys only (so the transform never sees a masked       */
+/* entry, which is the transform-then-mask order):                          */
+/*   S_ij = alpha q_i . k_j;  softcap c > 0:  S_ij <- c tanh(S_ij / c).      */
+/* Sink: one extra logit sigma per row that joins the softmax denominator    */
+/* and carries no value:                                                     */
+/*   m_i  = max(max_j S_ij, sigma)                                           */
+/*   l_i  = sum_j exp(S_ij - m_i) + exp(sigma - m_i)                         */
+/*   O_i  = sum_j exp(S_ij - m_i) v_j / l_i,  LSE_i = m_i + log l_i.         */
+/* Without a sink, a row with no visible key gets O = 0 and LSE = -inf; with */
+/* one it gets O = 0 and LSE = sigma.                                        */
+/* ------------------------------------------------------------------------ */
+
+static int visible_ext(int i, int j, int Nq, int Nk, int wl, int wr)
+{
+    long diag = (long)i + ((long)Nk - (long)Nq);
+    if (wr >= 0 && (long)j > diag + wr) return 0;
+    if (wl >= 0 && (long)j < diag - wl) return 0;
+    return 1;
+}
+
+static void attention_row_ext(const double *q, const double *k, const double *v,
+                              int i, int Nq, int Nk, int d, long ldk, long ldv,
+                              double alpha, int wl, int wr, double softcap,
+                              int has_sink, double sink, double *s,
+                              double *o_row, double *lse_out)
+{
+    double m = has_sink ? sink : -INFINITY;
+    for (int j = 0; j < Nk; ++j) {
+        if (visible_ext(i, j, Nq, Nk, wl, wr)) {
+            double dot = 0.0;
+            const double *kj = k + (long)j * ldk;
+            for (int c = 0; c < d; ++c) dot += q[c] * kj[c];
+            double x = alpha * dot;
+            if (softcap > 0.0) x = softcap * tanh(x / softcap);
+            s[j] = x;
+        } else {
+            s[j] = -INFINITY;
+        }
+        if (s[j] > m) m = s[j];
+    }
+    for (int c = 0; c < d; ++c) o_row[c] = 0.0;
+    if (m == -INFINITY) {               /* no visible key and no sink */
+        *lse_out = -INFINITY;
+        return;
+    }
+    double l = has_sink ? exp(sink - m) : 0.0;
+    for (int j = 0; j < Nk; ++j) {
+        if (s[j] == -INFINITY) continue;
+        double p = exp(s[j] - m);
+        l += p;
+        const double *vj = v + (long)j * ldv;
+        for (int c = 0; c < d; ++c) o_row[c] += p * vj[c];
+    }
+    for (int c = 0; c < d; ++c) o_row[c] /= l;
+    *lse_out = m + log(l);
+}
+
+/*
+ * oracle_attention_ext_head: one (batch, head) with the variants above.
+ * sink == NULL: no sink; otherwise *sink is this head's sigma.  rows as in
+ * oracle_attention_head.  Returns 0, or -1 on a bad argument (softcap < 0,
+ * a window bound below -1) or an allocation failure.
+ */
+int oracle_attention_ext_head(const double *q, const double *k, const double *v,
+                              int Nq, int Nk, int d, long ldq, long ldk, long ldv,
+                              double alpha, int wl, int wr, double softcap,
+                              const double *sink, const int *rows, int n_rows,
+                              double *o, long ldo, double *lse)
+{
+    if (Nq < 0 || Nk < 0 || d < 1 || !q || !k || !v || !o || !lse) return -1;
+    if (wl < -1 || wr < -1 || !(softcap >= 0.0)) return -1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+    if (!s) return -1;
+    int count = rows ? n_rows : Nq;
+    for (int t = 0; t < count; ++t) {
+        int i = rows ? rows[t] : t;
+        if (i < 0 || i >= Nq) { free(s); return -1; }
+        attention_row_ext(q + (long)i * ldq, k, v, i, Nq, Nk, d, ldk, ldv, alpha,
+                          wl, wr, softcap, sink != NULL, sink ? *sink : 0.0, s,
+                          o + (long)t * ldo, &lse[t]);
+    }
+    free(s);
+    return 0;
+}
+
+typedef struct {
+    const double *q, *k, *v, *sinks;
+    double *o, *lse;
+    int B, H, N, d, wl, wr;
+    double alpha, softcap;
+    int next;
+    int err;
+    pthread_mutex_t mu;
+} ext_job;
+
+static void *ext_worker(void *arg)
+{
+    ext_job *J = (ext_job *)arg;
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        int u = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (u >= J->B * J->H) break;
+        int b = u / J->H, h = u % J->H;
+        long ld = (long)J->H * J->d;
+        long off = ((long)b * J->N * J->H + h) * J->d;
+        int rc = oracle_attention_ext_head(J->q + off, J->k + off, J->v + off,
+                                           J->N, J->N, J->d, ld, ld, ld, J->alpha,
+                                           J->wl, J->wr, J->softcap,
+                                           J->sinks ? J->sinks + h : NULL, NULL, 0,
+                                           J->o + off, ld,
+                                           J->lse + ((long)b * J->H + h) * J->N);
+        if (rc) {
+            pthread_mutex_lock(&J->mu);
+            J->err = rc;
+            pthread_mutex_unlock(&J->mu);
+        }
+    }
+    return NULL;
+}
+
+/* Whole [B][N][H][d] tensors with the variants; sinks: NULL or sigma per
+ * head, [H]. */
+int oracle_attention_ext_fwd(const double *q, const double *k, const double *v,
+                             double *o, double *lse, int B, int H, int N, int d,
+                             double alpha, int wl, int wr, double softcap,
+                             const double *sinks, int n_threads)
+{
+    if (B < 1 || H < 1 || N < 0 || d < 1) return -1;
+    if (n_threads < 1) n_threads = 1;
+    if (n_threads > 512) n_threads = 512;
+    ext_job J = {q, k, v, sinks, o, lse, B, H, N, d, wl, wr, alpha, softcap, 0, 0,
+                 PTHREAD_MUTEX_INITIALIZER};
+    pthread_t th[512];
+    int started = 0;
+    for (int t = 0; t < n_threads; ++t) {
+        if (pthread_create(&th[t], NULL, ext_worker, &J) != 0) break;
+        ++started;
+    }
+    if (started == 0) ext_worker(&J);
     for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
     return J.err;
 }
