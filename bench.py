@@ -68,6 +68,41 @@ def flops(B, H, N, d, causal):
     return f / 2 if causal else f
 
 
+def window_pairs(rows, N, window):
+    """Visible (row, key) pairs of the given query rows under the window
+    (wl, wr): key j is visible from row i when i - wl <= j <= i + wr, a bound
+    of -1 being absent."""
+    wl, wr = window
+    rows = np.asarray(rows, dtype=np.int64)
+    lo = np.zeros_like(rows) if wl < 0 else np.maximum(0, rows - wl)
+    hi = np.full_like(rows, N) if wr < 0 else np.minimum(N, rows + wr + 1)
+    return float(np.maximum(0, hi - lo).sum())
+
+
+def variant_flops(B, H, N, d, window):
+    """4 d FLOPs (two GEMMs) per visible (row, key) pair."""
+    return 4.0 * B * H * d * window_pairs(np.arange(N), N, window)
+
+
+def variant_of(args):
+    """The score and mask variants requested on the command line, or None."""
+    if args.window is None and not args.softcap and not args.sinks:
+        return None
+    return {"window": tuple(args.window) if args.window is not None else (-1, -1),
+            "softcap": float(args.softcap), "sinks": bool(args.sinks)}
+
+
+def variant_suffix(var):
+    if var is None:
+        return ""
+    s = f" window {var['window'][0]},{var['window'][1]}"
+    if var["softcap"]:
+        s += f" softcap {var['softcap']:g}"
+    if var["sinks"]:
+        s += " sinks"
+    return s
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -157,10 +192,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def oracle_sample_rate(B, H, N, d, causal, rows_per_head, n_heads, threads):
+def oracle_sample_rate(B, H, N, d, causal, rows_per_head, n_heads, threads, var=None):
     """Times the FP64 oracle on `n_heads` heads x `rows_per_head` query rows
-    of the workload (full key range per row).  Returns (TFLOP/s, seconds,
-    description)."""
+    of the workload (full key range per row; with `var`, the variant oracle
+    over each row's window).  Returns (TFLOP/s, seconds, description)."""
     import oracle
     from concurrent.futures import ThreadPoolExecutor
     from exact_attention_forward_fa_gb300 import synth
@@ -170,22 +205,30 @@ def oracle_sample_rate(B, H, N, d, causal, rows_per_head, n_heads, threads):
     q, k, v = synth.qkv(nb, H, N, d, seed=synth.BASE_SEED)
     rng = np.random.default_rng(0)
     rows = np.sort(rng.choice(N, size=min(rows_per_head, N), replace=False))
-    hq = [(oracle._f64(q[b, :, h]), oracle._f64(k[b, :, h]), oracle._f64(v[b, :, h]))
+    hq = [(oracle._f64(q[b, :, h]), oracle._f64(k[b, :, h]), oracle._f64(v[b, :, h]), h)
           for b, h in heads]
+    sinks = synth.sinks(H) if var is not None and var["sinks"] else None
 
     def one(t):
-        qq, kk, vv = t
-        oracle.attention_head(qq, kk, vv, alpha, causal, rows=rows)
+        qq, kk, vv, h = t
+        if var is None:
+            oracle.attention_head(qq, kk, vv, alpha, causal, rows=rows)
+        else:
+            oracle.attention_ext_head(qq, kk, vv, alpha, var["window"], var["softcap"],
+                                      None if sinks is None else float(sinks[h]), rows=rows)
 
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(one, hq))
     dt = time.perf_counter() - t0
     # FLOPs of the sampled rows: 4*d per visible (row, key) pair
-    vis = (rows + 1).sum() if causal else len(rows) * N
+    if var is not None:
+        vis = window_pairs(rows, N, var["window"])
+    else:
+        vis = (rows + 1).sum() if causal else len(rows) * N
     fl = 4.0 * d * float(vis) * n_heads
     desc = (f"{n_heads} heads x {len(rows)} query rows (all keys) of B{B} H{H} N{N} d{d}"
-            f"{' causal' if causal else ''}, FP64 C oracle")
+            f"{' causal' if causal else ''}{variant_suffix(var)}, FP64 C oracle")
     return fl / dt / 1e12, dt, desc
 
 
@@ -194,13 +237,14 @@ def cpu_baseline(args, B, H, N, d):
     ~30 s, else as many heads (all rows) as fit in ~20 s."""
     threads = os.cpu_count() or 1
     n0 = min(threads, B * H)
-    rate, dt, _ = oracle_sample_rate(B, H, N, d, args.causal, N, n0, threads)
+    var = variant_of(args)
+    rate, dt, _ = oracle_sample_rate(B, H, N, d, args.causal, N, n0, threads, var)
     per_head = dt * threads / n0                 # seconds for one head per thread
     if per_head * (B * H) / threads <= 30.0:
         heads = B * H
     else:
         heads = int(max(n0, min(B * H, 20.0 * threads / per_head)))
-    rate, dt, desc = oracle_sample_rate(B, H, N, d, args.causal, N, heads, threads)
+    rate, dt, desc = oracle_sample_rate(B, H, N, d, args.causal, N, heads, threads, var)
     return {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": desc, "seconds": round(dt, 2)}
 
@@ -409,15 +453,16 @@ def run_reference(args, B, H, N, d, rank, world):
             "pct_of_2250": 100.0 * value / PEAK_SPEC}), flush=True)
         return
     threads = os.cpu_count() or 1
-    rate0, dt0, _ = oracle_sample_rate(B, H, N, d, args.causal, 16, threads, threads)
+    var = variant_of(args)
+    rate0, dt0, _ = oracle_sample_rate(B, H, N, d, args.causal, 16, threads, threads, var)
     per_row = dt0 / 16.0
     budget = 90.0 / max(1, args.steps + args.warmup)
     rows = int(max(1, min(N, budget / per_row)))
     for _ in range(args.warmup):
-        oracle_sample_rate(B, H, N, d, args.causal, rows, threads, threads)
+        oracle_sample_rate(B, H, N, d, args.causal, rows, threads, threads, var)
     rates, secs, desc = [], 0.0, ""
     for _ in range(args.steps):
-        r, dt, desc = oracle_sample_rate(B, H, N, d, args.causal, rows, threads, threads)
+        r, dt, desc = oracle_sample_rate(B, H, N, d, args.causal, rows, threads, threads, var)
         rates.append(r)
         secs += dt
     value = float(np.median(rates))
@@ -426,8 +471,9 @@ def run_reference(args, B, H, N, d, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": config_name(B, H, N, d, args.causal), "B": B, "H": H,
-                   "N": N, "d": d, "causal": args.causal},
+        "config": {"workload": config_name(B, H, N, d, args.causal) + variant_suffix(var),
+                   "B": B, "H": H, "N": N, "d": d, "causal": args.causal,
+                   **({"variant": var} if var else {})},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -465,6 +511,10 @@ def run_ours(args, B, H, N, d, rank, world):
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
+    var = variant_of(args)
+    if var is not None:             # window / softcap / sinks: fa_fwd_ext
+        wl, wr = var["window"]
+        sinks_t = (torch.from_numpy(synth.sinks(H)).to(dev) if var["sinks"] else None)
     n_splits = 0
     if args.splits is not None:     # split key ranges: partials + combine
         n_splits = args.splits or fa.fa_splitkv_auto(B, H, N, d)
@@ -486,7 +536,10 @@ def run_ours(args, B, H, N, d, rank, world):
         if args.fp8:
             rc = fa.fa_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, B, H, N, d, alpha, causal, sp)
         else:
-            if n_splits:
+            if var is not None:
+                rc = fa.fa_fwd_ext(q, k, v, o, lse, B, H, H_kv, N, d, alpha, wl, wr,
+                                   var["softcap"], sinks_t, fa.FA_BF16, sp)
+            elif n_splits:
                 rc = fa.fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16,
                                        n_splits, ws, sp)
             elif H_kv == H:
@@ -539,7 +592,7 @@ def run_ours(args, B, H, N, d, rank, world):
         raise RuntimeError("device status after timing: " + str(fa.fa_status_detail()))
     ms_max = reduce_max(ms_total, world, dev)
     ms_step = ms_max / args.steps
-    fl = flops(B, H, N, d, args.causal)
+    fl = flops(B, H, N, d, args.causal) if var is None else variant_flops(B, H, N, d, var["window"])
     value = aggregate_value(fl, args.steps, ms_max, world)
 
     # ---- end to end through the C ABI with pinned host buffers ----
@@ -593,6 +646,7 @@ def run_ours(args, B, H, N, d, rank, world):
         wkey = wkey.replace(f" H{H} ", f" H{H} Hkv{H_kv} ")
     if n_splits:
         wkey += f" split-KV x{n_splits}"
+    wkey += variant_suffix(var)
     line = {
         "metric": METRIC_FP8 if args.fp8 else METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world,
@@ -602,7 +656,8 @@ def run_ours(args, B, H, N, d, rank, world):
         "data": ("synthetic (seeded N(0,1) + 0.1% N(0,100) outliers)" if args.fp8
                  else "synthetic (seeded N(0,1) inputs)"),
         "config": {"workload": wkey, "B": B, "H": H, "H_kv": H_kv, "N": N, "d": d,
-                   "causal": bool(args.causal),
+                   "causal": bool(args.causal), **({"variant": var,
+                   "flops": "4 d per visible (row, key) pair"} if var else {}),
                    "l2": "no flush: 192 MiB of inputs exceed the 126 MB L2",
                    "parallelism": f"replicas x{world}"},
         "pct_of_2250": 100.0 * value / world / PEAK_SPEC,
@@ -639,6 +694,13 @@ def main():
                          "(0: the library's choice for the device)")
     ap.add_argument("--hkv", type=int, default=0,
                     help="grouped K/V heads (GQA/MQA, fa_fwd_gqa); default: H")
+    ap.add_argument("--window", type=int, nargs=2, default=None, metavar=("LEFT", "RIGHT"),
+                    help="local window (fa_fwd_ext): key j visible from row i when "
+                         "i - LEFT <= j <= i + RIGHT; -1 = no bound on that side")
+    ap.add_argument("--softcap", type=float, default=0.0,
+                    help="tanh softcap c on the scores (fa_fwd_ext); 0 = none")
+    ap.add_argument("--sinks", action="store_true",
+                    help="per-head sink logits (fa_fwd_ext), seeded N(2, 2)")
     ap.add_argument("--bwd", action="store_true",
                     help="time the backward pass (fa_bwd) instead of the forward")
     ap.add_argument("--skip-cpu", action="store_true",
@@ -656,6 +718,10 @@ def main():
         ap.error("--hkv applies to the BF16 forward and must divide --H")
     if args.splits is not None and (args.bwd or args.fp8 or args.hkv or args.d not in (64, 128)):
         ap.error("--splits applies to the BF16 forward, d 64 or 128, without --hkv")
+    if variant_of(args) is not None and (args.bwd or args.fp8 or args.splits is not None
+                                         or args.causal or args.d not in (64, 128)):
+        ap.error("--window/--softcap/--sinks apply to the BF16 forward, d 64 or 128, "
+                 "without --causal (use --window -1 0), --splits, --fp8 or --bwd")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and args.impl == "ours":

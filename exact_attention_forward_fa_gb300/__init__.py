@@ -29,7 +29,7 @@ FA_BF16 = 0
 FA_FP16 = 1
 
 # Every symbol include/fa.h declares (checked by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_splitkv", "fa_splitkv_workspace_floats",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_ext", "fa_fwd_splitkv", "fa_splitkv_workspace_floats",
            "fa_splitkv_auto", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_noalloc",
            "fa_check_status", "fa_status_detail", "fa_status_string", "fa_version")
 
@@ -57,6 +57,8 @@ def load():
     lib.fa_fwd.restype = i
     lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_gqa.restype = i
+    lib.fa_fwd_ext.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, f, vp, i, vp]
+    lib.fa_fwd_ext.restype = i
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp, vp]
     lib.fa_fwd_splitkv.restype = i
     lib.fa_splitkv_workspace_floats.argtypes = [i, i, i, i, i]
@@ -123,6 +125,45 @@ def fa_fwd_gqa(q, k, v, o, lse, B: int, H: int, H_kv: int, N: int, d: int, alpha
     return load().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
                              int(H_kv), int(N), int(d), float(alpha), int(causal), int(dtype),
                              _stream(stream))
+
+
+def fa_fwd_ext(q, k, v, o, lse, B: int, H: int, H_kv: int, N: int, d: int, alpha: float,
+               window_left: int, window_right: int, softcap: float, sinks, dtype: int,
+               stream=None) -> int:
+    """Direct call of the C entry point: local window, softcap and per-head
+    sinks (see include/fa.h); ``sinks`` may be None."""
+    return load().fa_fwd_ext(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                             int(H_kv), int(N), int(d), float(alpha), int(window_left),
+                             int(window_right), float(softcap), _ptr(sinks), int(dtype),
+                             _stream(stream))
+
+
+def attention_ext(q, k, v, window=(-1, -1), softcap: float = 0.0, sinks=None,
+                  alpha: float | None = None, out=None, lse=None, want_lse: bool = True,
+                  stream=None):
+    """Forward with the score and mask variants for torch tensors on the GPU:
+    window = (left, right) key bounds around the diagonal (-1: none),
+    softcap c (0: none), sinks float32 [H] on the GPU or None.  K/V may have
+    fewer heads than Q (grouped).  Returns (O, LSE or None)."""
+    import torch
+    if q.dtype == torch.bfloat16:
+        dt = FA_BF16
+    elif q.dtype == torch.float16:
+        dt = FA_FP16
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    B, N, H, d = q.shape
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    rc = fa_fwd_ext(q, k, v, out, lse, B, H, k.shape[2], N, d, alpha, int(window[0]),
+                    int(window[1]), float(softcap), sinks, dt, stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_ext")
+    return out, lse
 
 
 def fa_fwd_splitkv(q, k, v, o, lse, B: int, H: int, N: int, d: int, alpha: float, causal: int,

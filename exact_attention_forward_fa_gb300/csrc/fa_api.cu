@@ -180,6 +180,68 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float
     return fwd_impl(q, k, v, o, lse, B, H, H_kv, N, d, alpha, causal, dtype, stream);
 }
 
+fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int H, int H_kv, int N, int d, float alpha, int window_left,
+                     int window_right, float softcap, const float *sinks, fa_dtype dtype,
+                     void *stream) {
+    // ---- host-side validation: nothing is launched on failure ----
+    if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
+    if (window_left < -1 || window_right < -1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha) || !std::isfinite(softcap) || softcap < 0.f)
+        return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(sinks) & 3u))
+        return FA_ERR_MISALIGNED;
+    const uint64_t batch_stride = 2ull * d * H * static_cast<uint64_t>(N);
+    if (batch_stride >= (1ull << 40)) return FA_ERR_TOO_LARGE;
+    const uint64_t n_qt = (static_cast<uint64_t>(N) + 127) / 128;
+    const uint64_t units = static_cast<uint64_t>(B) * H * ((n_qt + 1) / 2);
+    if (units > 0x7fffffffull || static_cast<uint64_t>(B) * H * N > 0x7fffffffffffull)
+        return FA_ERR_TOO_LARGE;
+    // alpha / c must stay a finite float for the softcap's first constant
+    const double pre = softcap > 0.f ? static_cast<double>(alpha) / softcap : 0.0;
+    if (!std::isfinite(static_cast<float>(pre))) return FA_ERR_INVALID_ARG;
+
+    DeviceInfo *dev = nullptr;
+    fa_status st = get_device(&dev);
+    if (st != FA_OK) return st;
+
+    fa::FwdLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const CUtensorMapDataType dt =
+        dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    if ((st = encode_bshd(&L.q, q, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.k, k, dt, B, H_kv, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.v, v, dt, B, H_kv, N, d, 128)) != FA_OK) return st;
+    L.args.o = o;
+    L.args.lse = lse;
+    L.args.status = dev->status;
+    L.args.B = B;
+    L.args.H = H;
+    L.args.N = N;
+    L.args.n_kv = static_cast<int>(n_qt);
+    L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
+    L.args.n_units = static_cast<int>(units);
+    L.args.group = H / H_kv;
+    L.args.n_splits = 1;
+    L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
+    L.args.wl = window_left;
+    L.args.wr = window_right;
+    L.args.sc_pre = static_cast<float>(pre);
+    L.args.sc_post = static_cast<float>(static_cast<double>(softcap) * 1.4426950408889634);
+    L.args.sinks = sinks;
+    L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.bf16 = dtype == FA_BF16;
+    L.d64 = d == 64;
+    cudaError_t e = softcap > 0.f ? fa::launch_fwd_ext_softcap(L) : fa::launch_fwd_ext(L);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 // Split-KV: workspace floats for S splits (partial O in FP32 plus LSE).
 static uint64_t splitkv_floats(uint64_t B, uint64_t H, uint64_t N, uint64_t d, uint64_t S) {
     return S * B * N * H * d + S * B * H * N;

@@ -356,6 +356,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Hardware tanh (MUFU); its error bound is measured and stated where the
+// softcap uses it.
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

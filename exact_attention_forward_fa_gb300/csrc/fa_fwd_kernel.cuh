@@ -57,6 +57,15 @@ struct FwdArgs {
     int n_splits;
     float *o_part, *lse_part;
     float scale_log2;    // alpha * log2(e)
+    // Score and mask variants (kExt instantiations only).  Key j is hidden
+    // from query i when j > i + wr (wr >= 0) or j < i - wl (wl >= 0); -1 is
+    // no bound.  Softcap c: each score s becomes c tanh(alpha s / c), formed
+    // as sc_post * tanh(sc_pre * s) with sc_pre = alpha / c and
+    // sc_post = c log2(e) (sc_pre = 0: no softcap).  sinks: one logit per
+    // query head, added to every row's softmax denominator, or null.
+    int wl, wr;
+    float sc_pre, sc_post;
+    const float *sinks;
     // FP8 only: one FP32 scale per 128-row tile of each head, [B][H][n_kv]
     const float *q_scale, *k_scale, *v_scale;
 };
@@ -129,12 +138,26 @@ struct Unit {
     int T;          // key tiles visited: jhi-1 down to jhi-T
     int jhi;        // one past the unit's highest key tile
     int t0[2];      // first step at which tile X takes part (T if never)
+    int t1[2];      // one past its last step (T unless a left window ends it)
     int s;          // split of the key range
 };
 
+// Visible keys [klo, khi) of query row i under the window (wl, wr); every
+// row in [0, N) sees at least key i.  Written with min() so that no
+// intermediate leaves [0, N] for any window value.
+__device__ __forceinline__ int window_lo(int i, const FwdArgs &a) {
+    return a.wl >= 0 ? i - min(a.wl, i) : 0;
+}
+__device__ __forceinline__ int window_hi(int i, const FwdArgs &a) {
+    return a.wr >= 0 ? i + 1 + min(a.wr, a.N - 1 - i) : a.N;
+}
+
 // kSplit: the key range is cut into a.n_splits parts (otherwise one part,
-// folded away at compile time).
-template <bool kCausal, bool kSplit>
+// folded away at compile time).  kExt: the key range of each Q tile comes
+// from the window ("FlashAttention-3 on Hopper", sec. 4.7: local attention
+// bounds the loop on both sides), so a tile may also leave the pair's
+// descending key stream before its end.
+template <bool kCausal, bool kSplit, bool kExt = false>
 __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     Unit U;
     const int BH = a.B * a.H;
@@ -142,7 +165,9 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     U.s = kSplit ? u % S : 0;       // the splits of one pair are adjacent units
     if (kSplit) u /= S;
     int p, bh;
-    if (kCausal) {          // longest-first: the last pairs of every head first
+    // a right bound without a left one makes later pairs longer
+    const bool lpt = kExt ? (a.wl < 0 && a.wr >= 0) : kCausal;
+    if (lpt) {              // longest-first: the last pairs of every head first
         p = a.n_pairs - 1 - u / BH;
         bh = u % BH;
     } else {                // consecutive units share a head's K/V in L2
@@ -151,6 +176,28 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     }
     U.b = bh / a.H;
     U.h = bh % a.H;
+    if constexpr (kExt) {
+        int lo[2] = {0, 0}, hi[2] = {0, 0};
+        for (int x = 0; x < 2; ++x) {
+            U.m[x] = 2 * p + x;
+            U.act[x] = U.m[x] * 128 < a.N;
+            if (U.act[x]) {
+                const int r0 = U.m[x] * 128, r1 = min(a.N, r0 + 128) - 1;
+                const int klo = window_lo(r0, a), khi = window_hi(r1, a);
+                lo[x] = klo >> 7;
+                hi[x] = (khi >> 7) + ((khi & 127) != 0);
+            }
+        }
+        // tile H's range ends at or above tile L's and starts at or above
+        // it, and the two ranges touch (each row sees its diagonal key)
+        U.jhi = U.act[1] ? hi[1] : hi[0];
+        U.T = U.jhi - lo[0];
+        for (int x = 0; x < 2; ++x) {
+            U.t0[x] = U.act[x] ? U.jhi - hi[x] : U.T;
+            U.t1[x] = U.act[x] ? U.jhi - lo[x] : U.T;
+        }
+        return U;
+    }
     int hi[2];
     for (int x = 0; x < 2; ++x) {
         U.m[x] = 2 * p + x;
@@ -166,16 +213,24 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
         const int cnt = max(0, min(hi[x], U.jhi) - lo);
         U.act[x] = cnt > 0;
         U.t0[x] = U.T - cnt;
+        U.t1[x] = U.T;
     }
     return U;
 }
 
-template <int D, bool kCausal, bool kBF16, bool kFP8 = false, bool kSplit = false>
+// kVar: the score and mask variants of FwdArgs -- 1: window and sinks,
+// 2: window, sinks and softcap; kCausal is then unused (the causal mask is
+// the window (-1, 0)).
+template <int D, bool kCausal, bool kBF16, bool kFP8 = false, bool kSplit = false,
+          int kVar = 0>
 __global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
     using C = FwdCfg<D, kCausal, kBF16, kFP8>;
+    constexpr bool kExt = kVar != 0;
+    constexpr bool kCap = kVar == 2;
+    static_assert(!kExt || (!kFP8 && !kSplit && !kCausal), "variants: 16-bit, one split");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -241,7 +296,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 return true;
             };
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-                const Unit U = make_unit<kCausal, kSplit>(u, a);
+                const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
                 if (U.act[0]) ok = ok && load_q(0, U, qn0);
                 if (U.act[1]) ok = ok && load_q(1, U, qn1);
                 const int hk = U.h / a.group;        // K/V head of this query head
@@ -278,7 +333,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint32_t slot = 0, phase = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-                const Unit U = make_unit<kCausal, kSplit>(u, a);
+                const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
                 for (int t = 0; t <= U.T && ok; ++t) {
                     const bool has_v = t > 0, has_k = t < U.T;
                     uint32_t vslot = 0, vph = 0, kslot = 0, kph = 0;
@@ -287,10 +342,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     bool v_ready = false, k_ready = false;
                     // One Q tile's two GEMMs of this step; x is a literal at
                     // each call site, so every per-tile counter is a register.
-                    auto step_x = [&](const int x, const int t0x, int &qn, int &un,
-                                      uint32_t &pph) __attribute__((always_inline)) -> bool {
+                    auto step_x = [&](const int x, const int t0x, const int t1x, int &qn,
+                                      int &un, uint32_t &pph) __attribute__((always_inline)) -> bool {
                         // ---- O_x += P_x V_(t-1) ----
-                        if (has_v && t - 1 >= t0x) {
+                        if (has_v && t - 1 >= t0x && (!kExt || t - 1 < t1x)) {
                             if (!v_ready) {
                                 if (!mbar_wait_warp(bar(C::B_KVFULL + vslot), vph, w, 10)) return false;
                                 v_ready = true;
@@ -313,10 +368,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                      bd, C::IDESC_PV, (acc | kk) ? 1u : 0u);
                             }
                             pph ^= 1;
-                            if (t == U.T) mma_commit_elect(bar(C::B_OFULL + x));
+                            if (t == t1x) mma_commit_elect(bar(C::B_OFULL + x));
                         }
                         // ---- S_x = Q_x K_t^T ----
-                        if (has_k && t >= t0x) {
+                        if (has_k && t >= t0x && (!kExt || t < t1x)) {
                             if (!k_ready) {
                                 if (!mbar_wait_warp(bar(C::B_KVFULL + kslot), kph, w, 13)) return false;
                                 k_ready = true;
@@ -339,11 +394,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                      C::IDESC_QK, kk > 0 ? 1u : 0u);
                             }
                             mma_commit_elect(bar(C::B_SFULL + x));
-                            if (t == U.T - 1) mma_commit_elect(bar(C::B_QEMPTY + x));
+                            if (t == t1x - 1) mma_commit_elect(bar(C::B_QEMPTY + x));
                         }
                         return true;
                     };
-                    ok = step_x(0, U.t0[0], qn0, un0, pph0) && step_x(1, U.t0[1], qn1, un1, pph1);
+                    ok = step_x(0, U.t0[0], kExt ? U.t1[0] : U.T, qn0, un0, pph0) &&
+                         step_x(1, U.t0[1], kExt ? U.t1[1] : U.T, qn1, un1, pph1);
                     if (!ok) break;
                     if (has_k) mma_commit_elect(bar(C::B_KVEMPTY + kslot));
                     if (has_v) mma_commit_elect(bar(C::B_KVEMPTY + vslot));
@@ -366,15 +422,26 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t tS = tbase + lane_off + C::col_s(x);
         const uint32_t tO = tbase + lane_off + C::col_o(x);
         WaitCtx w{abort_flag, a.status, x ? kRoleSoftmax1 : kRoleSoftmax0};
-        const float sl2 = a.scale_log2;
+        // With a softcap the scores reaching the softmax are tanh values in
+        // [-1, 1], scaled to log2 units by c log2(e).
+        const float sc_pre = kCap ? a.sc_pre : 0.f;
+        const float sl2 = kCap ? a.sc_post : a.scale_log2;
         uint32_t sph = 0, oph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-            const Unit U = make_unit<kCausal, kSplit>(u, a);
+            const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
             const bool act = x ? U.act[1] : U.act[0];
             if (!act) continue;
             const int mt = x ? U.m[1] : U.m[0];
             const int t0 = x ? U.t0[1] : U.t0[0];
+            const int t1 = kExt ? (x ? U.t1[1] : U.t1[0]) : U.T;
+            // this row's visible keys (rows past N: any non-empty range)
+            int klo = 0, khi = a.N;
+            if constexpr (kExt) {
+                const int gr = min(mt * 128 + row, a.N - 1);
+                klo = window_lo(gr, a);
+                khi = window_hi(gr, a);
+            }
             // FP8: the Q tile's scale and the largest V scale of the head
             // (the per-tile V scales are folded into P relative to it).
             const size_t sbase = (static_cast<size_t>(U.b) * a.H + U.h) * a.n_kv;
@@ -391,7 +458,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             // exponentials (for LSE); lr: row sum of the same values rounded
             // as the P V product sees them (normalises O; 16-bit P only).
             float r = -INFINITY, le = 0.f, lr = 0.f;
-            for (int t = t0; t < U.T; ++t) {
+            for (int t = t0; t < t1; ++t) {
                 const int j = U.jhi - 1 - t;
                 ok = mbar_wait(bar(C::B_SFULL + x), sph, w, 20);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
@@ -399,19 +466,39 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 tc_fence_after();
                 uint32_t s[128];
                 float *sf = reinterpret_cast<float *>(s);
-                // ---- S -> registers, masks: sequence tail and causal diagonal ----
-                int lim = 128;
-                if (j == a.n_kv - 1) lim = min(lim, a.N - j * 128);
-                if (kCausal && j == mt) lim = min(lim, row + 1);
+                // ---- S -> registers, masks: sequence tail and causal diagonal
+                //      (variants: the row's window [klo, khi), after the
+                //      softcap -- "FlashAttention-3 on Hopper", sec. 4.7:
+                //      a score transformation precedes the mask) ----
+                int lim = 128, llo = 0;
+                if constexpr (kExt) {
+                    lim = min(lim, khi - j * 128);
+                    llo = klo - j * 128;
+                } else {
+                    if (j == a.n_kv - 1) lim = min(lim, a.N - j * 128);
+                    if (kCausal && j == mt) lim = min(lim, row + 1);
+                }
                 auto load_s = [&]() __attribute__((always_inline)) {
                     tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
                     tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
                     tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
                     tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
                     tmem_ld_wait();
-                    if (lim < 128) {
+                    if constexpr (kExt) {
+                        if constexpr (kCap) {
 #pragma unroll
-                        for (int c = 0; c < 128; ++c) if (c >= lim) sf[c] = -INFINITY;
+                            for (int c = 0; c < 128; ++c) sf[c] = tanh_approx(sf[c] * sc_pre);
+                        }
+                        if (lim < 128 || llo > 0) {
+#pragma unroll
+                            for (int c = 0; c < 128; ++c)
+                                if (c >= lim || c < llo) sf[c] = -INFINITY;
+                        }
+                    } else {
+                        if (lim < 128) {
+#pragma unroll
+                            for (int c = 0; c < 128; ++c) if (c >= lim) sf[c] = -INFINITY;
+                        }
                     }
                 };
                 load_s();
@@ -543,7 +630,24 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             tc_fence_after();
             // 16-bit P: O / l_r.  FP8: O v_max / l (O accumulated P' = P v_j/v_max).
             const bool live = (le > 0.f) && (kFP8 || lr > 0.f);
-            const float inv = live ? (kFP8 ? vmax / le : 1.f / lr) : 0.f;
+            float inv = live ? (kFP8 ? vmax / le : 1.f / lr) : 0.f;
+            // LSE in log2 units
+            float lse2 = live ? r - C::P_OFFSET + log2f(le) : -INFINITY;
+            if constexpr (kExt) {
+                // Sink ("FlashAttention-3 on Hopper", sec. 4.6): one more
+                // term 2^(sigma log2 e - r) in both row sums, no value.
+                if (a.sinks != nullptr) {
+                    const float sg = a.sinks[U.h] * 1.44269504088896340736f;
+                    if (!live) {
+                        inv = 0.f;
+                        lse2 = sg;
+                    } else {
+                        const float M = fmaxf(r, sg);
+                        lse2 = M + log2f(le * ex2_approx(r - M) + ex2_approx(sg - M));
+                        inv = 1.f / (lr + ex2_approx(sg - r));    // 2^+big -> inf -> 0
+                    }
+                }
+            }
             const int grow = mt * 128 + row;
             uint16_t *orow = reinterpret_cast<uint16_t *>(a.o) +
                              ((static_cast<size_t>(U.b) * a.N + grow) * a.H + U.h) * D;
@@ -583,11 +687,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     reinterpret_cast<uint4 *>(orow)[ch] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
-            if (a.lse != nullptr && grow < a.N) {
-                const float lse = live ? (r - C::P_OFFSET + log2f(le)) * 0.69314718055994530942f
-                                       : -INFINITY;
-                a.lse[(static_cast<size_t>(U.b) * a.H + U.h) * a.N + grow] = lse;
-            }
+            if (a.lse != nullptr && grow < a.N)
+                a.lse[(static_cast<size_t>(U.b) * a.H + U.h) * a.N + grow] =
+                    lse2 * 0.69314718055994530942f;
         }
     }
 

@@ -18,7 +18,7 @@ struct FwdLaunch {
     cudaStream_t stream;
     bool causal;
     bool bf16;
-    bool d64;              // split path only: head dim 64 (else 128)
+    bool d64;              // split and variant paths: head dim 64 (else 128)
 };
 
 cudaError_t launch_fwd_d64(const FwdLaunch &L);
@@ -26,6 +26,8 @@ cudaError_t launch_fwd_d128(const FwdLaunch &L);
 cudaError_t launch_fwd_d256(const FwdLaunch &L);   // K/V maps with 64-row boxes
 cudaError_t launch_fwd_fp8(const FwdLaunch &L);    // e4m3 maps, 128-byte boxes
 cudaError_t launch_fwd_split(const FwdLaunch &L);  // split key ranges, d in {64, 128}
+cudaError_t launch_fwd_ext(const FwdLaunch &L);    // window / sinks, d in {64, 128}
+cudaError_t launch_fwd_ext_softcap(const FwdLaunch &L);   // the same with a softcap
 // Split-KV combine: O, LSE from S partials (o_part [S][B][N][H][d] FP32,
 // lse_part [S][B][H][N]); d in {64, 128}.
 struct CombineArgs {
@@ -71,10 +73,11 @@ cudaError_t launch_quantize(const QuantLaunch &L);
 
 // Shared helper: set the dynamic shared-memory limit once per device, then
 // launch one instantiation.
-template <int D, bool kCausal, bool kBF16, bool kFP8 = false, bool kSplit = false>
+template <int D, bool kCausal, bool kBF16, bool kFP8 = false, bool kSplit = false,
+          int kVar = 0>
 cudaError_t launch_fwd_inst(const FwdLaunch &L) {
     using Cfg = FwdCfg<D, kCausal, kBF16, kFP8>;
-    auto kern = fa_fwd_kernel<D, kCausal, kBF16, kFP8, kSplit>;
+    auto kern = fa_fwd_kernel<D, kCausal, kBF16, kFP8, kSplit, kVar>;
     static unsigned long long configured = 0ull;   // bit per device id (< 64)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -126,6 +129,14 @@ cudaError_t launch_fwd_split_dispatch(const FwdLaunch &L) {
                       : launch_fwd_inst<D, true, false, false, true>(L);
     return L.bf16 ? launch_fwd_inst<D, false, true, false, true>(L)
                   : launch_fwd_inst<D, false, false, false, true>(L);
+}
+
+// Score and mask variants, d in {64, 128}: kVar 1 (window, sinks) or 2
+// (window, sinks, softcap).
+template <int D, int kVar>
+cudaError_t launch_fwd_ext_dispatch(const FwdLaunch &L) {
+    return L.bf16 ? launch_fwd_inst<D, false, true, false, false, kVar>(L)
+                  : launch_fwd_inst<D, false, false, false, false, kVar>(L);
 }
 
 }  // namespace fa

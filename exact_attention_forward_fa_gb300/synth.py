@@ -14,6 +14,9 @@ Recipe (the workloads of "FlashAttention-3" as reviewed on diycv.top,
   an added N(0, 100) term (standard deviation 10).
 * Hadamard signs for incoherent processing: d entries of +-1 from
   ``default_rng(seed)``.
+* Sink logits (one per query head): N(2, 2) from ``default_rng(seed)`` as
+  float32, so that e^sigma ranges from negligible to larger than the row
+  sum of a narrow window.
 
 Layout: [B][N][H][d] (batch, sequence, head, head dim), contiguous.
 """
@@ -54,3 +57,9 @@ def hadamard_signs(d: int, seed: int = BASE_SEED) -> np.ndarray:
 def default_alpha(d: int) -> float:
     """1/sqrt(d) rounded to float32 (the value handed to the kernel)."""
     return float(np.float32(1.0 / np.sqrt(np.float64(d))))
+
+
+def sinks(H: int, seed: int = BASE_SEED) -> np.ndarray:
+    """float32 [H] sink logits, N(2, 2)."""
+    rng = np.random.default_rng(seed)
+    return (np.float32(2.0) + np.float32(2.0) * rng.standard_normal(H, dtype=np.float32))

@@ -90,6 +90,35 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o,
                      float alpha, int causal, fa_dtype dtype, void *stream);
 
 /*
+ * fa_fwd_ext -- fa_fwd_gqa with the score and mask variants of
+ * "FlashAttention-3 on Hopper" sec. 4.6 (learnable sinks folded into the
+ * row sum at finalize) and sec. 4.7 (local / sliding-window masks; a score
+ * transformation precedes the mask), and the softcap of "03 FA3" sec. 5:
+ *   window_left, window_right : key j is hidden from query i when
+ *            j > i + window_right (window_right >= 0) or
+ *            j < i - window_left (window_left >= 0); -1 = no bound on that
+ *            side.  (-1, 0) is causal, (-1, -1) no mask; values below -1
+ *            return FA_ERR_INVALID_ARG.  Every row sees at least key i.
+ *   softcap : 0 for none, else c > 0: each visible score s = alpha q.k
+ *            becomes c tanh(s / c) before the mask and the softmax
+ *            (tanh.approx.f32: max abs error 8e-6, measured);
+ *            negative or non-finite returns FA_ERR_INVALID_ARG.
+ *   sinks  : device, float [H] (one logit sigma per query head, finite or
+ *            -inf), 4-byte aligned, or NULL for none.  sigma joins every
+ *            row's softmax denominator and carries no value:
+ *            O_i = sum_j e^(S_ij) v_j / (sum_j e^(S_ij) + e^sigma),
+ *            LSE_i = log(sum_j e^(S_ij) + e^sigma).
+ *   d in {64, 128} (others FA_ERR_UNSUPPORTED).  Other arguments, results
+ *   and errors as fa_fwd_gqa.  Key tiles entirely outside a Q tile's
+ *   window are neither loaded nor computed.
+ */
+fa_status fa_fwd_ext(const void *q, const void *k, const void *v, void *o,
+                     float *lse, int B, int H, int H_kv, int N, int d,
+                     float alpha, int window_left, int window_right,
+                     float softcap, const float *sinks, fa_dtype dtype,
+                     void *stream);
+
+/*
  * fa_fwd_splitkv -- fa_fwd with each work unit's key range cut into
  * n_splits parts ("FlashAttention-3 on Hopper", ch. 10: split-KV and its
  * combine kernel), for problems whose B * H * ceil(N/256) units do not

@@ -92,6 +92,33 @@ def test_gqa_validation_codes(lib, H, H_kv, code):
     assert lib.fa_fwd_gqa(A, A, A, A, None, 1, H, H_kv, 128, 64, 0.125, 0, 0, None) == code
 
 
+def _xcall(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=2, H_kv=1, N=128, d=128, alpha=0.088,
+           wl=-1, wr=0, softcap=0.0, sinks=None, dtype=0):
+    return lib.fa_fwd_ext(q, k, v, o, lse, B, H, H_kv, N, d, alpha, wl, wr, softcap, sinks,
+                          dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(H=3, H_kv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(wl=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(wr=-5), fa.FA_ERR_INVALID_ARG),
+    (dict(softcap=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(softcap=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(softcap=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(softcap=1e-38, alpha=1e3), fa.FA_ERR_INVALID_ARG),   # alpha / c overflows
+    (dict(alpha=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=2), fa.FA_ERR_INVALID_ARG),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(v=A + 8), fa.FA_ERR_MISALIGNED),
+    (dict(sinks=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(lse=A + 1), fa.FA_ERR_MISALIGNED),
+])
+def test_ext_validation_codes(lib, kw, code):
+    assert _xcall(lib, **kw) == code
+
+
 def _scall(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=1, N=128, d=128, alpha=0.088, causal=0,
            dtype=0, S=2, ws=A):
     return lib.fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, alpha, causal, dtype, S, ws, None)
