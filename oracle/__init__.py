@@ -24,6 +24,8 @@ computes, and the passage it follows, is stated in ``fa_oracle.c``:
   transform before mask), "03 FA3" sec. 5 (softcap).
 * ``attention_bwd`` / ``attention_bwd_head``: the gradients dQ, dK, dV from
   the definition, "FlashAttention-3 on Hopper" sec. 7.1.
+* ``attention_bwd_ext`` / ``attention_bwd_ext_head``: the gradients of the
+  variants (window, softcap, sink), including the sink logit's gradient.
 * ``hadamard_rotate``, ``e4m3_encode`` / ``e4m3_decode``,
   ``quantize_e4m3_tiles``: the FP8 pre-pass pieces, "FlashAttention-3 on
   Hopper" sec. 6.1, 6.3, 6.4.
@@ -100,6 +102,10 @@ def _load():
         ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
         ctypes.c_double, _dp, ctypes.c_int]
     lib.oracle_attention_ext_fwd.restype = ctypes.c_int
+    lib.oracle_attention_bwd_ext_head.argtypes = [
+        _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
+        ctypes.c_int, ctypes.c_int, ctypes.c_double, _dp, _dp, _dp, _dp, _dp]
+    lib.oracle_attention_bwd_ext_head.restype = ctypes.c_int
     lib.oracle_hadamard_rotate.argtypes = [
         _dp, _dp, ctypes.c_long, ctypes.c_int, ctypes.c_long, _dp]
     lib.oracle_hadamard_rotate.restype = ctypes.c_int
@@ -237,6 +243,50 @@ def attention_bwd(q, k, v, dout, alpha: float, causal: bool, n_threads: int = 1)
     if rc:
         raise RuntimeError(f"oracle_attention_bwd failed ({rc})")
     return dq, dk, dv
+
+
+def attention_bwd_ext_head(q, k, v, dout, alpha: float, window=(-1, -1),
+                           softcap: float = 0.0, sink=None):
+    """One head of the variants' gradients: q/dout [Nq,d], k/v [Nk,d], sink a
+    scalar or None.  Returns (dQ, dK, dV, dsigma) with dsigma 0 without a
+    sink."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    Nq, d = q.shape
+    Nk = k.shape[0]
+    dq, dk, dv = np.zeros((Nq, d)), np.zeros((Nk, d)), np.zeros((Nk, d))
+    sk = None if sink is None else np.array([float(sink)])
+    ds = np.zeros(1)
+    rc = _load().oracle_attention_bwd_ext_head(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), Nq, Nk, d, float(alpha), int(window[0]),
+        int(window[1]), float(softcap), _ptr(sk) if sk is not None else None, _ptr(dq),
+        _ptr(dk), _ptr(dv), _ptr(ds))
+    if rc:
+        raise RuntimeError(f"oracle_attention_bwd_ext_head failed ({rc})")
+    return dq, dk, dv, float(ds[0])
+
+
+def attention_bwd_ext(q, k, v, dout, alpha: float, window=(-1, -1), softcap: float = 0.0,
+                      sinks=None, n_threads: int = 1):
+    """The variants' gradients on [B,N,H,d] tensors: (dQ, dK, dV, dsinks [H]),
+    dsinks summed over the batch (zeros without sinks).  Heads are independent
+    and run on a thread pool."""
+    from concurrent.futures import ThreadPoolExecutor
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, N, H, d = q.shape
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(q), np.zeros_like(q)
+    sk = None if sinks is None else _f64(sinks).reshape(H)
+    dsink = np.zeros((B, H))
+
+    def one(bh):
+        b, h = bh
+        g = attention_bwd_ext_head(q[b, :, h], k[b, :, h], v[b, :, h], dout[b, :, h], alpha,
+                                   window, softcap, None if sk is None else sk[h])
+        dq[b, :, h], dk[b, :, h], dv[b, :, h] = g[0], g[1], g[2]
+        dsink[b, h] = g[3]
+
+    with ThreadPoolExecutor(max_workers=max(1, int(n_threads))) as ex:
+        list(ex.map(one, [(b, h) for b in range(B) for h in range(H)]))
+    return dq, dk, dv, dsink.sum(axis=0)
 
 
 def attention_bwd_head(q, k, v, dout, alpha: float, causal: bool):

@@ -481,6 +481,84 @@ int oracle_attention_bwd(const double *q, const double *k, const double *v,
 
 
 /* ------------------------------------------------------------------------ */
+/* Gradients of the variants, one head: [FA3H] sec. 7.1 applied to the      */
+/* definition of the variants above.  With u_ij = alpha q_i.k_j, the score   */
+/* S_ij = u_ij (no softcap) or c tanh(u_ij / c), P_ij = exp(S_ij - LSE_i)    */
+/* over visible keys and the sink's share P_i,sink = exp(sigma - LSE_i):     */
+/*   dV_j  = sum_i P_ij dO_i,   dP_ij = dO_i . v_j,                          */
+/*   D_i   = sum_j P_ij dP_ij   (the sink has no value: dP_i,sink = 0)       */
+/*   dS_ij = P_ij (dP_ij - D_i),  dU_ij = dS_ij dS/du = dS_ij (1 - t_ij^2)   */
+/*           with t_ij = tanh(u_ij / c) (softcap), else dU = dS              */
+/*   dQ_i  = alpha sum_j dU_ij k_j,  dK_j = alpha sum_i dU_ij q_i            */
+/*   dsigma = sum_i P_i,sink (0 - D_i) = -sum_i P_i,sink D_i                  */
+/* dsink (optional) receives dsigma of this head.  Rows with neither a       */
+/* visible key nor a sink contribute nothing.                                */
+/* ------------------------------------------------------------------------ */
+int oracle_attention_bwd_ext_head(const double *q, const double *k, const double *v,
+                                  const double *dout, int Nq, int Nk, int d,
+                                  double alpha, int wl, int wr, double softcap,
+                                  const double *sink, double *dq, double *dk,
+                                  double *dv, double *dsink)
+{
+    if (Nq < 0 || Nk < 0 || d < 1 || !q || !k || !v || !dout || !dq || !dk || !dv)
+        return -1;
+    if (wl < -1 || wr < -1 || !(softcap >= 0.0)) return -1;
+    size_t nk1 = (size_t)(Nk > 0 ? Nk : 1);
+    double *s = (double *)malloc(sizeof(double) * nk1);
+    double *t = (double *)malloc(sizeof(double) * nk1);
+    double *p = (double *)malloc(sizeof(double) * nk1);
+    double *dp = (double *)malloc(sizeof(double) * nk1);
+    if (!s || !t || !p || !dp) { free(s); free(t); free(p); free(dp); return -1; }
+    for (long x = 0; x < (long)Nk * d; ++x) { dk[x] = 0.0; dv[x] = 0.0; }
+    double ds_sink = 0.0;
+    for (int i = 0; i < Nq; ++i) {
+        const double *qi = q + (long)i * d, *doi = dout + (long)i * d;
+        double *dqi = dq + (long)i * d;
+        for (int c = 0; c < d; ++c) dqi[c] = 0.0;
+        double m = sink ? *sink : -INFINITY;
+        for (int j = 0; j < Nk; ++j) {
+            s[j] = -INFINITY;
+            t[j] = 0.0;
+            if (!visible_ext(i, j, Nq, Nk, wl, wr)) continue;
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) dot += qi[c] * k[(long)j * d + c];
+            double u = alpha * dot;
+            if (softcap > 0.0) { t[j] = tanh(u / softcap); s[j] = softcap * t[j]; }
+            else s[j] = u;
+            if (s[j] > m) m = s[j];
+        }
+        if (m == -INFINITY) continue;
+        double l = sink ? exp(*sink - m) : 0.0;
+        for (int j = 0; j < Nk; ++j) {
+            p[j] = (s[j] == -INFINITY) ? 0.0 : exp(s[j] - m);
+            l += p[j];
+        }
+        for (int j = 0; j < Nk; ++j) p[j] /= l;
+        double D = 0.0;
+        for (int j = 0; j < Nk; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) acc += doi[c] * v[(long)j * d + c];
+            dp[j] = acc;
+            D += p[j] * acc;
+        }
+        if (sink) ds_sink -= exp(*sink - m) / l * D;
+        for (int j = 0; j < Nk; ++j) {
+            if (p[j] == 0.0) continue;
+            double du = p[j] * (dp[j] - D);
+            if (softcap > 0.0) du *= 1.0 - t[j] * t[j];
+            for (int c = 0; c < d; ++c) {
+                dqi[c] += alpha * du * k[(long)j * d + c];
+                dk[(long)j * d + c] += alpha * du * qi[c];
+                dv[(long)j * d + c] += p[j] * doi[c];
+            }
+        }
+    }
+    if (dsink) *dsink = sink ? ds_sink : 0.0;
+    free(s); free(t); free(p); free(dp);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* The tiled online algorithm, FP64, one head: the method's own steps, kept  */
 /* separate from the one-pass definition above so that each pins the other. */
 /*                                                                           */

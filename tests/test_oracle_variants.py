@@ -15,7 +15,11 @@ The variant oracle is checked against things other than itself:
   softcapped LSE lies within [-c, c] + log(visible keys);
 * masked keys and values do not influence the result at all;
 * planted mistakes (window off by one, swapped window sides, wrong softcap,
-  the sink of another head) fail the brute-force pin.
+  the sink of another head) fail the brute-force pin;
+* gradients (dQ, dK, dV and the sink logit's): central finite differences
+  of L = sum(O * dO) through the variant forward, the plain gradient oracle
+  for (-1, 0) and (-1, -1), and planted mistakes (softcap factor, window,
+  sink dropped or changed) that the finite-difference pin rejects.
 """
 import math
 
@@ -219,3 +223,90 @@ def test_planted_mistakes_are_caught():
     assert fails(*oracle.attention_ext_head(q, k, v, a, win, c, -0.4))       # another sink
     assert fails(*oracle.attention_ext_head(q, k, v, a, win, c, None))       # sink dropped
     assert fails(*oracle.attention_ext_head(q, k, v, 1.0, win, c, sink))     # alpha dropped
+
+
+# ---------------------------------------------------------------------------
+# Gradients of the variants ("FlashAttention-3 on Hopper", sec. 7.1)
+# ---------------------------------------------------------------------------
+
+def _ext_loss(q, k, v, dout, a, window, softcap, sink):
+    o, _ = oracle.attention_ext_head(q, k, v, a, window, softcap, sink)
+    return float(np.sum(o * dout))
+
+
+def _ext_fd(q, k, v, dout, a, window, softcap, sink, eps=1e-5):
+    grads = []
+    for which in range(3):
+        args = [q.copy(), k.copy(), v.copy()]
+        g = np.zeros_like(args[which])
+        for idx in np.ndindex(g.shape):
+            x0 = args[which][idx]
+            args[which][idx] = x0 + eps
+            lp = _ext_loss(*args, dout, a, window, softcap, sink)
+            args[which][idx] = x0 - eps
+            lm = _ext_loss(*args, dout, a, window, softcap, sink)
+            args[which][idx] = x0
+            g[idx] = (lp - lm) / (2 * eps)
+        grads.append(g)
+    if sink is None:
+        grads.append(0.0)
+    else:
+        lp = _ext_loss(q, k, v, dout, a, window, softcap, sink + eps)
+        lm = _ext_loss(q, k, v, dout, a, window, softcap, sink - eps)
+        grads.append((lp - lm) / (2 * eps))
+    return grads
+
+
+def _grads_agree(g, fd, tol=1e-7):
+    return (all(np.allclose(x, y, rtol=tol, atol=tol) for x, y in zip(g[:3], fd[:3]))
+            and abs(g[3] - fd[3]) <= tol * max(1.0, abs(fd[3])))
+
+
+@pytest.mark.parametrize("window,softcap,sink", [
+    ((-1, -1), 0.0, None), ((-1, 0), 0.0, None), ((1, 0), 0.0, None), ((2, 1), 0.0, 0.4),
+    ((-1, -1), 1.5, None), ((1, 2), 0.8, -0.3), ((-1, 0), 2.0, 1.2), ((0, 0), 0.0, 0.7)])
+@pytest.mark.parametrize("nq,nk,d", [(5, 5, 3), (4, 6, 2)])
+def test_bwd_ext_matches_finite_differences(nq, nk, d, window, softcap, sink):
+    q, k, v, dout = _rand(nq, d), _rand(nk, d), _rand(nk, d), _rand(nq, d)
+    a = 0.9
+    g = oracle.attention_bwd_ext_head(q, k, v, dout, a, window, softcap, sink)
+    assert _grads_agree(g, _ext_fd(q, k, v, dout, a, window, softcap, sink))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_ext_reduces_to_plain_gradients(causal):
+    N, d = 9, 4
+    q, k, v, dout = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+    g = oracle.attention_bwd_ext_head(q, k, v, dout, 0.6, (-1, 0) if causal else (-1, -1))
+    ref = oracle.attention_bwd_head(q, k, v, dout, 0.6, causal)
+    for x, y in zip(g[:3], ref):
+        assert np.allclose(x, y, rtol=1e-13, atol=1e-15)
+    assert g[3] == 0.0
+
+
+def test_bwd_ext_whole_tensor_matches_heads():
+    B, N, H, d = 2, 7, 3, 4
+    q, k, v, dout = (_rand(B, N, H, d) for _ in range(4))
+    sinks = _rand(H)
+    dq, dk, dv, ds = oracle.attention_bwd_ext(q, k, v, dout, 0.5, (2, 0), 1.5, sinks, n_threads=3)
+    tot = np.zeros(H)
+    for b in range(B):
+        for h in range(H):
+            g = oracle.attention_bwd_ext_head(q[b, :, h], k[b, :, h], v[b, :, h], dout[b, :, h],
+                                              0.5, (2, 0), 1.5, float(sinks[h]))
+            assert np.array_equal(dq[b, :, h], g[0]) and np.array_equal(dk[b, :, h], g[1])
+            assert np.array_equal(dv[b, :, h], g[2])
+            tot[h] += g[3]
+    assert np.allclose(ds, tot, rtol=1e-15, atol=0)
+
+
+def test_bwd_ext_planted_mistakes_are_caught():
+    N, d = 6, 3
+    q, k, v, dout = _rand(N, d), _rand(N, d), _rand(N, d), _rand(N, d)
+    a, win, c, sink = 0.8, (2, 1), 1.3, 0.5
+    fd = _ext_fd(q, k, v, dout, a, win, c, sink)
+    assert _grads_agree(oracle.attention_bwd_ext_head(q, k, v, dout, a, win, c, sink), fd)
+    assert not _grads_agree(oracle.attention_bwd_ext_head(q, k, v, dout, a, win, 0.0, sink), fd)
+    assert not _grads_agree(oracle.attention_bwd_ext_head(q, k, v, dout, a, (3, 1), c, sink), fd)
+    assert not _grads_agree(oracle.attention_bwd_ext_head(q, k, v, dout, a, win, c, None), fd)
+    assert not _grads_agree(oracle.attention_bwd_ext_head(q, k, v, dout, a, win, c, -0.5), fd)
