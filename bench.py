@@ -249,7 +249,7 @@ def cpu_baseline(args, B, H, N, d):
             "sample": desc, "seconds": round(dt, 2)}
 
 
-def oracle_bwd_sample_rate(B, H, N, d, causal, rows, n_heads, threads):
+def oracle_bwd_sample_rate(B, H, N, d, causal, rows, n_heads, threads, var=None):
     """Times the FP64 gradient oracle on `n_heads` heads with the first `rows`
     query rows (all keys).  Returns (TFLOP/s counted as 2.5x the forward's
     FLOPs of those rows, seconds, description)."""
@@ -262,20 +262,32 @@ def oracle_bwd_sample_rate(B, H, N, d, causal, rows, n_heads, threads):
     q, k, v = synth.qkv(nb, H, N, d, seed=synth.BASE_SEED)
     do = synth.normal((nb, N, H, d), seed=synth.BASE_SEED + 3)
     rows = int(min(rows, N))
-    hq = [(oracle._f64(q[b, :rows, h]), oracle._f64(k[b, :, h]), oracle._f64(v[b, :, h]),
-           oracle._f64(do[b, :rows, h])) for b, h in heads]
+    # the first `rows` query rows, or with a window the last ones (the
+    # variant oracle aligns the diagonal bottom-right, so they keep their
+    # global positions)
+    r0 = 0 if var is None else N - rows
+    hq = [(oracle._f64(q[b, r0:r0 + rows, h]), oracle._f64(k[b, :, h]), oracle._f64(v[b, :, h]),
+           oracle._f64(do[b, r0:r0 + rows, h])) for b, h in heads]
+    sinks = synth.sinks(H) if var is not None and var["sinks"] else None
 
     def one(t):
-        oracle.attention_bwd_head(*t, alpha, causal)
+        if var is None:
+            oracle.attention_bwd_head(*t, alpha, causal)
+        else:
+            oracle.attention_bwd_ext_head(*t, alpha, var["window"], 0.0,
+                                          None if sinks is None else float(sinks[0]))
 
     t0 = time.perf_counter()
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(one, hq))
     dt = time.perf_counter() - t0
-    vis = rows * (N - rows) + rows * (rows + 1) / 2 if causal else rows * N
+    if var is not None:
+        vis = window_pairs(np.arange(N - rows, N), N, var["window"])
+    else:
+        vis = rows * (N - rows) + rows * (rows + 1) / 2 if causal else rows * N
     fl = BWD_FACTOR * 4.0 * d * float(vis) * n_heads
     desc = (f"{n_heads} heads x {rows} query rows (all keys) of B{B} H{H} N{N} d{d}"
-            f"{' causal' if causal else ''}, FP64 C gradient oracle")
+            f"{' causal' if causal else ''}{variant_suffix(var)}, FP64 C gradient oracle")
     return fl / dt / 1e12, dt, desc
 
 
@@ -302,15 +314,29 @@ def run_bwd(args, B, H, N, d, rank, world):
     ws = torch.empty((fa.bwd_workspace_floats(B, H, N),), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
+    var = variant_of(args)          # window / sinks: fa_fwd_ext + fa_bwd_ext
+    sinks_t = dsinks_t = None
+    if var is not None and var["sinks"]:
+        sinks_t = torch.from_numpy(synth.sinks(H)).to(dev)
+        dsinks_t = torch.empty((H,), dtype=torch.float32, device=dev)
 
     def fwd():
-        rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
+        if var is None:
+            rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
+        else:
+            rc = fa.fa_fwd_ext(q, k, v, o, lse, B, H, H, N, d, alpha, var["window"][0],
+                               var["window"][1], 0.0, sinks_t, fa.FA_BF16, sp)
         if rc != fa.FA_OK:
             raise fa.FaError(rc, "fa_fwd")
 
     def launch():
-        rc = fa.fa_bwd(q, k, v, o, do, lse, ws, dq, dk, dv, B, H, N, d, alpha, causal,
-                       fa.FA_BF16, sp)
+        if var is None:
+            rc = fa.fa_bwd(q, k, v, o, do, lse, ws, dq, dk, dv, B, H, N, d, alpha, causal,
+                           fa.FA_BF16, sp)
+        else:
+            rc = fa.fa_bwd_ext(q, k, v, o, do, lse, ws, dq, dk, dv, B, H, N, d, alpha,
+                               var["window"][0], var["window"][1], sinks_t, dsinks_t,
+                               fa.FA_BF16, sp)
         if rc != fa.FA_OK:
             raise fa.FaError(rc, "fa_bwd")
 
@@ -343,7 +369,8 @@ def run_bwd(args, B, H, N, d, rank, world):
         raise RuntimeError("device status after timing: " + str(fa.fa_status_detail()))
     ms_max = reduce_max(ms_total, world, dev)
     ms_step = ms_max / args.steps
-    fl = BWD_FACTOR * flops(B, H, N, d, args.causal)
+    fl = BWD_FACTOR * (flops(B, H, N, d, args.causal) if var is None
+                       else variant_flops(B, H, N, d, var["window"]))
     value = aggregate_value(fl, args.steps, ms_max, world)
 
     # ---- end to end: Q, K, V, O, dO, LSE in; dQ, dK, dV out, every step ----
@@ -387,7 +414,8 @@ def run_bwd(args, B, H, N, d, rank, world):
         peak, peak_kind = sustained, "sustained"
     else:
         peak, peak_kind = burst, "burst"
-    wkey = config_name(B, H, N, d, args.causal).replace("attention fwd", "attention bwd")
+    wkey = (config_name(B, H, N, d, args.causal).replace("attention fwd", "attention bwd")
+            + variant_suffix(var))
     line = {
         "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -395,6 +423,8 @@ def run_bwd(args, B, H, N, d, rank, world):
         "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs and dO)",
         "config": {"workload": wkey, "B": B, "H": H, "N": N, "d": d,
                    "causal": bool(args.causal),
+                   **({"variant": var, "flops": "2.5 x 4 d per visible (row, key) pair"}
+                      if var else {}),
                    "l2": "no flush: 320 MiB of inputs exceed the 126 MB L2",
                    "parallelism": f"replicas x{world}"},
         "pct_of_2250": 100.0 * value / world / PEAK_SPEC,
@@ -406,16 +436,16 @@ def run_bwd(args, B, H, N, d, rank, world):
                      "traffic": profiled_traffic(wkey)},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (3 + (1 if dsinks_t is not None else 0)) * args.steps,
         "clocks": clk.summary(),
     }
     if not args.skip_cpu:
         threads = os.cpu_count() or 1
         n0 = min(threads, B * H)
-        rate, dt, desc = oracle_bwd_sample_rate(B, H, N, d, args.causal, 256, n0, threads)
+        rate, dt, desc = oracle_bwd_sample_rate(B, H, N, d, args.causal, 256, n0, threads, var)
         # scale the sample to ~20 s of host time: more query rows per head
         rows = int(max(256, min(N, 256 * 20.0 / max(dt, 1e-3))))
-        rate, dt, desc = oracle_bwd_sample_rate(B, H, N, d, args.causal, rows, n0, threads)
+        rate, dt, desc = oracle_bwd_sample_rate(B, H, N, d, args.causal, rows, n0, threads, var)
         line["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads,
                                 "kind": "oracle", "sample": desc, "seconds": round(dt, 2)}
     print(json.dumps(line), flush=True)
@@ -425,16 +455,17 @@ def run_reference(args, B, H, N, d, rank, world):
     if rank != 0:
         return
     if args.bwd:
+        var = variant_of(args)
         threads = os.cpu_count() or 1
         n0 = min(threads, B * H)
-        _, dt0, _ = oracle_bwd_sample_rate(B, H, N, d, args.causal, 16, n0, threads)
+        _, dt0, _ = oracle_bwd_sample_rate(B, H, N, d, args.causal, 16, n0, threads, var)
         budget = 90.0 / max(1, args.steps + args.warmup)
         rows = int(max(1, min(N, 16 * budget / max(dt0, 1e-6))))
         for _ in range(args.warmup):
-            oracle_bwd_sample_rate(B, H, N, d, args.causal, rows, n0, threads)
+            oracle_bwd_sample_rate(B, H, N, d, args.causal, rows, n0, threads, var)
         rates, secs, desc = [], 0.0, ""
         for _ in range(args.steps):
-            r, dt, desc = oracle_bwd_sample_rate(B, H, N, d, args.causal, rows, n0, threads)
+            r, dt, desc = oracle_bwd_sample_rate(B, H, N, d, args.causal, rows, n0, threads, var)
             rates.append(r)
             secs += dt
         value = float(np.median(rates))
@@ -444,7 +475,7 @@ def run_reference(args, B, H, N, d, rank, world):
             "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": config_name(B, H, N, d, args.causal).replace(
-                "attention fwd", "attention bwd"), "B": B,
+                "attention fwd", "attention bwd") + variant_suffix(var), "B": B,
                        "H": H, "N": N, "d": d, "causal": args.causal},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
                              "kind": "oracle", "sample": desc},
@@ -718,10 +749,12 @@ def main():
         ap.error("--hkv applies to the BF16 forward and must divide --H")
     if args.splits is not None and (args.bwd or args.fp8 or args.hkv or args.d not in (64, 128)):
         ap.error("--splits applies to the BF16 forward, d 64 or 128, without --hkv")
-    if variant_of(args) is not None and (args.bwd or args.fp8 or args.splits is not None
+    if variant_of(args) is not None and (args.fp8 or args.splits is not None
                                          or args.causal or args.d not in (64, 128)):
-        ap.error("--window/--softcap/--sinks apply to the BF16 forward, d 64 or 128, "
-                 "without --causal (use --window -1 0), --splits, --fp8 or --bwd")
+        ap.error("--window/--softcap/--sinks apply to BF16, d 64 or 128, without --causal "
+                 "(use --window -1 0), --splits or --fp8")
+    if args.bwd and args.softcap:
+        ap.error("--softcap has no backward")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and args.impl == "ours":

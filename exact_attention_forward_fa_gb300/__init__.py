@@ -30,7 +30,7 @@ FA_FP16 = 1
 
 # Every symbol include/fa.h declares (checked by the tests).
 EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_ext", "fa_fwd_splitkv", "fa_splitkv_workspace_floats",
-           "fa_splitkv_auto", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_noalloc",
+           "fa_splitkv_auto", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_ext", "fa_bwd_noalloc",
            "fa_check_status", "fa_status_detail", "fa_status_string", "fa_version")
 
 _lib = None
@@ -71,6 +71,9 @@ def load():
     lib.fa_fwd_fp8.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_bwd.restype = i
+    lib.fa_bwd_ext.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i,
+                               vp, vp, i, vp]
+    lib.fa_bwd_ext.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_bwd_noalloc.restype = i
     lib.fa_check_status.argtypes = [vp]
@@ -261,6 +264,41 @@ def fa_bwd(q, k, v, o, dout, lse, workspace, dq, dk, dv, B: int, H: int, N: int,
     return load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                          _ptr(workspace), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H), int(N),
                          int(d), float(alpha), int(causal), int(dtype), _stream(stream))
+
+
+def fa_bwd_ext(q, k, v, o, dout, lse, workspace, dq, dk, dv, B: int, H: int, N: int, d: int,
+               alpha: float, window_left: int, window_right: int, sinks, dsinks, dtype: int,
+               stream=None) -> int:
+    """Direct call of the C entry point: the backward of fa_fwd_ext with a
+    local window; sinks/dsinks may be None (see include/fa.h)."""
+    return load().fa_bwd_ext(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                             _ptr(workspace), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H),
+                             int(N), int(d), float(alpha), int(window_left), int(window_right),
+                             _ptr(sinks), _ptr(dsinks), int(dtype), _stream(stream))
+
+
+def attention_backward_ext(q, k, v, o, lse, dout, window=(-1, -1), sinks=None,
+                           alpha: float | None = None, stream=None):
+    """Gradients (dQ, dK, dV, dsinks or None) for the forward of
+    ``attention_ext`` with a window and optional sinks (no softcap)."""
+    import torch
+    if q.dtype == torch.bfloat16:
+        dt = FA_BF16
+    elif q.dtype == torch.float16:
+        dt = FA_FP16
+    else:
+        raise TypeError(f"unsupported dtype {q.dtype}")
+    B, N, H, d = q.shape
+    if alpha is None:
+        alpha = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    ws = torch.empty((bwd_workspace_floats(B, H, N),), dtype=torch.float32, device=q.device)
+    ds = None if sinks is None else torch.empty((H,), dtype=torch.float32, device=q.device)
+    rc = fa_bwd_ext(q, k, v, o, dout, lse, ws, dq, dk, dv, B, H, N, d, alpha, int(window[0]),
+                    int(window[1]), sinks, ds, dt, stream)
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_ext")
+    return dq, dk, dv, ds
 
 
 def fa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int,

@@ -445,12 +445,21 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
-                 const float *lse, float *workspace, void *dq, void *dk, void *dv, int B, int H,
-                 int N, int d, float alpha, int causal, fa_dtype dtype, void *stream) {
+// The backward with the causal flag or, with win set, a local window
+// (wl, wr); sinks / dsinks (window path only) give the sink logits'
+// gradient.
+static fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
+                          const void *dout, const float *lse, float *workspace, void *dq,
+                          void *dk, void *dv, int B, int H, int N, int d, float alpha,
+                          int causal, bool win, int wl, int wr, const float *sinks,
+                          float *dsinks, fa_dtype dtype, void *stream) {
     // ---- host-side validation: nothing is launched on failure ----
     if (!q || !k || !v || !o || !dout || !lse || !workspace || !dq || !dk || !dv)
         return FA_ERR_INVALID_ARG;
+    if (win && (wl < -1 || wr < -1)) return FA_ERR_INVALID_ARG;
+    if (dsinks && !sinks) return FA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(sinks) & 3u) || (reinterpret_cast<uintptr_t>(dsinks) & 3u))
+        return FA_ERR_MISALIGNED;
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
@@ -507,8 +516,27 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
     L.causal = causal != 0;
     L.bf16 = dtype == FA_BF16;
     L.stream = static_cast<cudaStream_t>(stream);
-    cudaError_t e = fa::launch_bwd(L);
+    L.args.wl = wl;
+    L.args.wr = wr;
+    cudaError_t e = win ? fa::launch_bwd_win(L) : fa::launch_bwd(L);
+    if (e == cudaSuccess && dsinks) e = fa::launch_bwd_dsink(L.args, sinks, dsinks, L.stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
+                 const float *lse, float *workspace, void *dq, void *dk, void *dv, int B, int H,
+                 int N, int d, float alpha, int causal, fa_dtype dtype, void *stream) {
+    return bwd_impl(q, k, v, o, dout, lse, workspace, dq, dk, dv, B, H, N, d, alpha, causal,
+                    false, -1, -1, nullptr, nullptr, dtype, stream);
+}
+
+fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
+                     const void *dout, const float *lse, float *workspace, void *dq, void *dk,
+                     void *dv, int B, int H, int N, int d, float alpha, int window_left,
+                     int window_right, const float *sinks, float *dsinks, fa_dtype dtype,
+                     void *stream) {
+    return bwd_impl(q, k, v, o, dout, lse, workspace, dq, dk, dv, B, H, N, d, alpha, 0, true,
+                    window_left, window_right, sinks, dsinks, dtype, stream);
 }
 
 // ---------------------------------------------------------------------------

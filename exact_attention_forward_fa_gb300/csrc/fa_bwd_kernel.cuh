@@ -59,7 +59,29 @@ struct BwdArgs {
     int n_units;           // B * H * n_t
     float scale_log2;      // alpha * log2(e)
     float alpha;
+    // Local window (kWin instantiations): key j is hidden from query i when
+    // j > i + wr (wr >= 0) or j < i - wl (wl >= 0); -1 is no bound.
+    int wl, wr;
 };
+
+// Visible keys [win_klo, win_khi) of query row i (0 <= i < N), and visible
+// queries [win_qlo, win_qhi) of key row j (0 <= j < N), under (wl, wr).
+// Written with min() so no intermediate leaves [0, N].
+__device__ __forceinline__ int win_klo(int i, const BwdArgs &a) {
+    return a.wl >= 0 ? i - min(a.wl, i) : 0;
+}
+__device__ __forceinline__ int win_khi(int i, const BwdArgs &a) {
+    return a.wr >= 0 ? i + 1 + min(a.wr, a.N - 1 - i) : a.N;
+}
+__device__ __forceinline__ int win_qlo(int j, const BwdArgs &a) {
+    return a.wr >= 0 ? j - min(a.wr, j) : 0;
+}
+__device__ __forceinline__ int win_qhi(int j, const BwdArgs &a) {
+    return a.wl >= 0 ? j + 1 + min(a.wl, a.N - 1 - j) : a.N;
+}
+// 128-row tile range [lo, hi) covering rows [r_lo, r_hi) (r_hi > r_lo).
+__device__ __forceinline__ int tile_lo(int r_lo) { return r_lo >> 7; }
+__device__ __forceinline__ int tile_hi(int r_hi) { return (r_hi >> 7) + ((r_hi & 127) != 0); }
 
 template <int D, bool kBF16>
 struct BwdCfg {
@@ -121,12 +143,15 @@ struct BwdUnit {
     int b, h, m;
 };
 
-template <bool kCausal, bool kKeyTiles>
+// kWin: the window's loop bounds; longest-first when it has a right bound
+// and no left one (the causal shape).
+template <bool kCausal, bool kKeyTiles, bool kWin = false>
 __device__ __forceinline__ BwdUnit make_bwd_unit(int u, const BwdArgs &a) {
     BwdUnit U;
     const int BH = a.B * a.H;
     int bh;
-    if (kCausal) {
+    const bool lpt = kWin ? (a.wl < 0 && a.wr >= 0) : kCausal;
+    if (lpt) {
         const int k = u / BH;
         U.m = kKeyTiles ? k : a.n_t - 1 - k;
         bh = u % BH;
@@ -291,7 +316,7 @@ __device__ __forceinline__ void store_cols(void *dst_base, const BwdArgs &a, int
 // and dP(t+1); dS is double-buffered so dQ(t) reads dS(t) while dS(t+1) is
 // written.
 // ---------------------------------------------------------------------------
-template <int D, bool kCausal, bool kBF16>
+template <int D, bool kCausal, bool kBF16, bool kWin = false>
 __global__ void __launch_bounds__(320, 1)
 fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -305,7 +330,17 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     auto bar = [&](int i) -> uint32_t { return base + C::DQ_BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF + 4);
-    auto n_key_tiles = [&](const BwdUnit &U) { return kCausal ? U.m + 1 : a.n_t; };
+    // key tiles [lo, hi) of query tile U.m, visited from hi - 1 down
+    auto key_range = [&](const BwdUnit &U, int &lo, int &hi) {
+        if constexpr (kWin) {
+            const int r0 = U.m * 128, r1 = min(a.N, r0 + 128) - 1;
+            lo = tile_lo(win_klo(r0, a));
+            hi = tile_hi(win_khi(r1, a));
+        } else {
+            lo = 0;
+            hi = kCausal ? U.m + 1 : a.n_t;
+        }
+    };
 
     if (warp == 9) tmem_alloc(base + C::DQ_MISC_OFF, C::TMEM_COLS);
     if (tid == 0) {
@@ -349,16 +384,18 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             int qn = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-                const BwdUnit U = make_bwd_unit<kCausal, false>(u, a);
+                const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
                 ok = mbar_wait(bar(C::DQB_QEMPTY), (qn & 1) ^ 1, w, 50);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(C::DQB_QFULL), 2 * C::TILE);
                 load_tile<C::NCH>(&tm_q, base + C::DQ_Q_OFF, bar(C::DQB_QFULL), U.h, U.m * 128, U.b);
                 load_tile<C::NCH>(&tm_do, base + C::DQ_DO_OFF, bar(C::DQB_QFULL), U.h, U.m * 128, U.b);
                 ++qn;
-                const int T = n_key_tiles(U);
+                int klo_t, khi_t;
+                key_range(U, klo_t, khi_t);
+                const int T = khi_t - klo_t;
                 for (int t = 0; ok && t < T; ++t) {
-                    const int j = T - 1 - t;
+                    const int j = khi_t - 1 - t;
                     const uint32_t ks = RK::slot(nk), vs = RV::slot(nv);
                     ok = mbar_wait(bar(C::DQB_KEMPTY + ks), RK::phase(nk) ^ 1, w, 51);
                     if (!ok) break;
@@ -396,8 +433,10 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             return mbar_wait_warp(bar(C::DQB_VFULL + RV::slot(i)), RV::phase(i), w, 62);
         };
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-            const BwdUnit U = make_bwd_unit<kCausal, false>(u, a);
-            const int T = n_key_tiles(U);
+            const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
+            int klo_t, khi_t;
+            key_range(U, klo_t, khi_t);
+            const int T = khi_t - klo_t;
             ok = mbar_wait_warp(bar(C::DQB_QFULL), qph, w, 60);
             if (!ok) break;
             qph ^= 1;
@@ -466,9 +505,18 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         uint32_t sph = 0, dpph = 0, dqph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-            const BwdUnit U = make_bwd_unit<kCausal, false>(u, a);
-            const int T = n_key_tiles(U);
+            const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
+            int klo_t, khi_t;
+            key_range(U, klo_t, khi_t);
+            const int T = khi_t - klo_t;
             const int grow = U.m * 128 + row;
+            // this row's visible keys (rows past N: any range; their P is 0)
+            int klo_r = 0, khi_r = a.N;
+            if constexpr (kWin) {
+                const int gr = min(grow, a.N - 1);
+                klo_r = win_klo(gr, a);
+                khi_r = win_khi(gr, a);
+            }
             // log2-domain LSE of this row (+inf for rows beyond N and empty
             // rows: their P is 0) and D of this row, from the workspace
             const size_t widx = (static_cast<size_t>(U.b) * a.H + U.h) * a.NP + grow;
@@ -477,7 +525,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const float2 nl2 = make_float2(-lse2, -lse2);
             const float2 nd2 = make_float2(-drow, -drow);
             for (int t = 0; t < T; ++t) {
-                const int j = T - 1 - t;
+                const int j = khi_t - 1 - t;
                 // ---- P(t) = exp2(S c - LSE2) from S(t) ----
                 ok = mbar_wait(bar(C::DQB_SFULL), sph, w, 70);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
@@ -493,12 +541,17 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (lane == 0) mbar_arrive(bar(C::DQB_SFREE));
                 int lim = min(128, a.N - j * 128) - col0;        // keys beyond N
                 if (kCausal) lim = min(lim, grow - j * 128 + 1 - col0);
+                int llo = 0;                                     // window: first visible
+                if constexpr (kWin) {
+                    lim = min(lim, khi_r - j * 128 - col0);
+                    llo = klo_r - j * 128 - col0;
+                }
                 float *pf = reinterpret_cast<float *>(sv);
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
                     const float2 x = __ffma2_rn(make_float2(pf[c], pf[c + 1]), c2, nl2);
-                    pf[c] = c < lim ? ex2_approx(x.x) : 0.f;
-                    pf[c + 1] = c + 1 < lim ? ex2_approx(x.y) : 0.f;
+                    pf[c] = (c < lim && (!kWin || c >= llo)) ? ex2_approx(x.x) : 0.f;
+                    pf[c + 1] = (c + 1 < lim && (!kWin || c + 1 >= llo)) ? ex2_approx(x.y) : 0.f;
                 }
                 // ---- dS(t) = P o (dP - D) -> TMEM dS[t%2] ----
                 ok = mbar_wait(bar(C::DQB_DPFULL), dpph, w, 71);
@@ -571,7 +624,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // dO until G3); LSE2 and D of the query columns are read from the padded
 // workspace through L1, where the producer prefetches each tile's lines.
 // ---------------------------------------------------------------------------
-template <int D, bool kCausal, bool kBF16>
+template <int D, bool kCausal, bool kBF16, bool kWin = false>
 __global__ void __launch_bounds__(320, 1)
 fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -585,7 +638,17 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     auto bar = [&](int i) -> uint32_t { return base + C::KV_BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF + 4);
-    auto first_q = [&](const BwdUnit &U) { return kCausal ? U.m : 0; };
+    // query tiles [lo, hi) that see key tile U.m
+    auto query_range = [&](const BwdUnit &U, int &lo, int &hi) {
+        if constexpr (kWin) {
+            const int k0 = U.m * 128, k1 = min(a.N, k0 + 128) - 1;
+            lo = tile_lo(win_qlo(k0, a));
+            hi = tile_hi(win_qhi(k1, a));
+        } else {
+            lo = kCausal ? U.m : 0;
+            hi = a.n_t;
+        }
+    };
     using RQ = Ring<C::QN>;
     using RO = Ring<C::DN>;
     auto q_tile = [&](uint32_t i) { return base + C::KV_Q_OFF + RQ::slot(i) * C::TILE; };
@@ -630,7 +693,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             int kvn = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-                const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
+                const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
                 ok = mbar_wait(bar(C::KVB_KVEMPTY), (kvn & 1) ^ 1, w, 80);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar(C::KVB_KVFULL), 2 * C::TILE);
@@ -638,7 +701,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 load_tile<C::NCH>(&tm_v, base + C::KV_V_OFF, bar(C::KVB_KVFULL), U.h, U.m * 128, U.b);
                 ++kvn;
                 const size_t wrow = (static_cast<size_t>(U.b) * a.H + U.h) * a.NP;
-                for (int i = first_q(U); ok && i < a.n_t; ++i, ++nq) {
+                int qlo_t, qhi_t;
+                query_range(U, qlo_t, qhi_t);
+                for (int i = qlo_t; ok && i < qhi_t; ++i, ++nq) {
                     // the elementwise warps read LSE2 and D of these 128
                     // columns: 2 x 512 B, four 128-byte lines each
 #pragma unroll
@@ -675,8 +740,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             return mbar_wait_warp(bar(C::KVB_DOFULL + RO::slot(i)), RO::phase(i), w, 96);
         };
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-            const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
-            const int Ti = a.n_t - first_q(U);
+            const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
+            int qlo_t, qhi_t;
+            query_range(U, qlo_t, qhi_t);
+            const int Ti = qhi_t - qlo_t;
             ok = mbar_wait_warp(bar(C::KVB_KVFULL), kvph, w, 90);
             if (!ok) break;
             kvph ^= 1;
@@ -748,10 +815,18 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         uint32_t stph = 0, dpph = 0, accph = 0;
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
-            const BwdUnit U = make_bwd_unit<kCausal, true>(u, a);
-            const int i0 = first_q(U);
-            const int Ti = a.n_t - i0;
+            const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
+            int i0, qhi_t;
+            query_range(U, i0, qhi_t);
+            const int Ti = qhi_t - i0;
             const int krow = U.m * 128 + row;
+            // this key row's visible queries (rows past N: any range)
+            int qlo_r = 0, qhi_r = a.N;
+            if constexpr (kWin) {
+                const int kr = min(krow, a.N - 1);
+                qlo_r = win_qlo(kr, a);
+                qhi_r = win_qhi(kr, a);
+            }
             const size_t wrow = (static_cast<size_t>(U.b) * a.H + U.h) * a.NP;
             for (int k = 0; k < Ti; ++k) {
                 const int i = i0 + k;
@@ -768,7 +843,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tmem_ld32(tST + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tmem_ld_wait();
                 // causal: query column q sees this key row iff krow <= q
-                const int lo = (kCausal ? krow - i * 128 : 0) - col0;   // first visible column
+                int lo = (kCausal ? krow - i * 128 : 0) - col0;         // first visible column
+                int hi = 1 << 30;                                       // one past the last
+                if constexpr (kWin) {
+                    lo = qlo_r - i * 128 - col0;
+                    hi = qhi_r - i * 128 - col0;
+                }
                 float *pf = reinterpret_cast<float *>(sv);
                 uint32_t pk[32];
 #pragma unroll
@@ -778,10 +858,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                                   make_float2(-l4.x, -l4.y));
                     const float2 x23 = __ffma2_rn(make_float2(pf[c + 2], pf[c + 3]), c2,
                                                   make_float2(-l4.z, -l4.w));
-                    pf[c + 0] = c + 0 >= lo ? ex2_approx(x01.x) : 0.f;
-                    pf[c + 1] = c + 1 >= lo ? ex2_approx(x01.y) : 0.f;
-                    pf[c + 2] = c + 2 >= lo ? ex2_approx(x23.x) : 0.f;
-                    pf[c + 3] = c + 3 >= lo ? ex2_approx(x23.y) : 0.f;
+                    pf[c + 0] = (c + 0 >= lo && (!kWin || c + 0 < hi)) ? ex2_approx(x01.x) : 0.f;
+                    pf[c + 1] = (c + 1 >= lo && (!kWin || c + 1 < hi)) ? ex2_approx(x01.y) : 0.f;
+                    pf[c + 2] = (c + 2 >= lo && (!kWin || c + 2 < hi)) ? ex2_approx(x23.x) : 0.f;
+                    pf[c + 3] = (c + 3 >= lo && (!kWin || c + 3 < hi)) ? ex2_approx(x23.y) : 0.f;
                     pk[c / 2] = pack2<kBF16>(pf[c], pf[c + 1]);
                     pk[c / 2 + 1] = pack2<kBF16>(pf[c + 2], pf[c + 3]);
                 }

@@ -52,6 +52,12 @@ struct BwdLaunch {
     cudaStream_t stream;
 };
 cudaError_t launch_bwd(const BwdLaunch &L);
+// The same for a local window (L.args.wl, L.args.wr; L.causal unused).
+cudaError_t launch_bwd_win(const BwdLaunch &L);
+// Gradient of per-head sink logits: dsinks[h] = -sum_{b,i} 2^(sigma_h log2 e
+// - LSE2_i) D_i over the workspace rows of the backward (one CTA per head).
+cudaError_t launch_bwd_dsink(const BwdArgs &a, const float *sinks, float *dsinks,
+                             cudaStream_t stream);
 
 // FP8 pre-pass: persistent CTAs over (b, h, 128-row tile); x arrives by
 // TMA (map {d, H, N, B}, box {d, 1, 128, 1}, no swizzle, rows >= N zero).

@@ -207,6 +207,28 @@ def test_bwd_validation_codes(lib, kw, code):
     assert _bcall(lib, **kw) == code
 
 
+def _bxcall(lib, q=A, o=A, lse=A, ws=A, dq=A, B=1, H=1, N=128, d=128, wl=64, wr=0,
+            sinks=None, dsinks=None, dtype=0):
+    return lib.fa_bwd_ext(q, A, A, o, A, lse, ws, dq, A, A, B, H, N, d, 0.088, wl, wr, sinks,
+                          dsinks, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(ws=None), fa.FA_ERR_INVALID_ARG),
+    (dict(wl=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(wr=-3), fa.FA_ERR_INVALID_ARG),
+    (dict(dsinks=A), fa.FA_ERR_INVALID_ARG),            # a sink gradient needs the sinks
+    (dict(dtype=5), fa.FA_ERR_INVALID_ARG),
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(sinks=A + 2, dsinks=A), fa.FA_ERR_MISALIGNED),
+    (dict(sinks=A, dsinks=A + 1), fa.FA_ERR_MISALIGNED),
+    (dict(dq=A + 8), fa.FA_ERR_MISALIGNED),
+])
+def test_bwd_ext_validation_codes(lib, kw, code):
+    assert _bxcall(lib, **kw) == code
+
+
 def test_bwd_noalloc_rejects_problems_beyond_its_workspace(lib):
     # 2 * B * H * ceil(N/128) * 128 floats must fit the 4 Mi-float array;
     # the check comes before any CUDA call.
