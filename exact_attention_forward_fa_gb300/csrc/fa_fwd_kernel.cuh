@@ -16,9 +16,11 @@
 //     ("FlashAttention-3 on Hopper", sec. 4.7).
 //   * 384 threads; warpgroup 2 (warps 8-11) gives registers to the two
 //     softmax warpgroups with setmaxnreg.  Warps 10-11 are spare.
-//   * Warp 8 (one lane) is the TMA producer: Q_L/Q_H once per unit, then
-//     K_j and V_j into a ring of shared-memory stages guarded by full/empty
-//     mbarriers ("FlashAttention-3 on Hopper", sec. 4.3.1).
+//   * Warp 8 (one lane) is the TMA producer: Q_L/Q_H once per unit into
+//     three rotating Q slots (the next unit's first Q tile loads while the
+//     current unit runs), then K_j and V_j into a ring of shared-memory
+//     stages guarded by full/empty mbarriers ("FlashAttention-3 on Hopper",
+//     sec. 4.3.1).
 //   * Warp 9 (one lane) issues every tcgen05.mma: S_X = Q_X K_j^T into
 //     TMEM, O_X += P_X V_j with P_X read from TMEM (TS form).  Per step the
 //     order is PV_L(j+1), QK_L(j), PV_H(j+1), QK_H(j), so each softmax group
@@ -82,7 +84,11 @@ struct FwdCfg {
     static constexpr int NCH = D * ESZ / 128;           // 128-byte column chunks
     static constexpr uint32_t CHUNK_BYTES = 128u * 128u;  // 128 rows x 128 B
     static constexpr uint32_t TILE_BYTES = NCH * CHUNK_BYTES;
-    static constexpr int NSTAGE = (kFP8 || D == 64) ? 8 : 5;
+    // K/V ring stages and Q slots.  Three Q slots rotate over the units'
+    // tiles, so the next unit's first Q tile loads while this unit still
+    // runs (two slots would make it wait for this unit's last QK).
+    static constexpr int NSTAGE = (kFP8 || D == 64) ? 8 : 4;
+    static constexpr int NQ = 3;
     static constexpr int QK_STEPS = D * ESZ / 32;       // 32 bytes of K per MMA
     static constexpr int PV_KEYS = 32 / ESZ;            // keys per PV MMA
     static constexpr int PV_STEPS = BN / PV_KEYS;
@@ -97,11 +103,11 @@ struct FwdCfg {
 
     // shared memory map (offsets from a 1024-B aligned base)
     static constexpr uint32_t Q_OFF = 0;
-    static constexpr uint32_t KV_OFF = 2 * TILE_BYTES;
+    static constexpr uint32_t KV_OFF = NQ * TILE_BYTES;
     static constexpr uint32_t BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
     // barrier indices
-    static constexpr int B_QFULL = 0, B_QEMPTY = 2, B_KVFULL = 4,
-                         B_KVEMPTY = 4 + NSTAGE, B_SFULL = 4 + 2 * NSTAGE,
+    static constexpr int B_QFULL = 0, B_QEMPTY = NQ, B_KVFULL = 2 * NQ,
+                         B_KVEMPTY = 2 * NQ + NSTAGE, B_SFULL = 2 * NQ + 2 * NSTAGE,
                          B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
                          B_OEMPTY = B_OFULL + 2, B_MMADONE = B_OEMPTY + 2,
                          NBAR = B_MMADONE + 1;
@@ -248,9 +254,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (warp == 9) tmem_alloc(base + C::MISC_OFF, C::TMEM_COLS);
     if (tid == 0) {
         *abort_flag = 0u;
+        for (int q = 0; q < C::NQ; ++q) {
+            mbar_init(bar(C::B_QFULL + q), 1);
+            mbar_init(bar(C::B_QEMPTY + q), 1);
+        }
         for (int x = 0; x < 2; ++x) {
-            mbar_init(bar(C::B_QFULL + x), 1);
-            mbar_init(bar(C::B_QEMPTY + x), 1);
             mbar_init(bar(C::B_SFULL + x), 1);
             mbar_init(bar(C::B_PFULL + x), 4);
             mbar_init(bar(C::B_OFULL + x), 1);
@@ -280,25 +288,30 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            int qn0 = 0, qn1 = 0;                   // Q loads issued per tile slot
+            uint32_t qc = 0;                        // Q loads issued (slot qc % NQ)
+            uint32_t qarmed = 0, qarmed_par = 0;    // per Q slot: ever loaded / parity
             uint32_t slot = 0, phase = 0;
             uint32_t armed = 0, armed_par = 0;      // per-slot: ever armed / parity
             bool ok = true;
-            auto load_q = [&](const int x, const Unit &U, int &qn)
-                              __attribute__((always_inline)) -> bool {
-                if (!mbar_wait(bar(C::B_QEMPTY + x), (qn & 1) ^ 1, w, 1)) return false;
-                mbar_arrive_expect_tx(bar(C::B_QFULL + x), C::TILE_BYTES);
+            // Tile x of U into the next Q slot, once the slot's previous
+            // tile has had its last QK.
+            auto load_q = [&](const int x, const Unit &U) __attribute__((always_inline)) -> bool {
+                const uint32_t qs = qc % C::NQ, qph = (qc / C::NQ) & 1u;
+                if (!mbar_wait(bar(C::B_QEMPTY + qs), qph ^ 1u, w, 1)) return false;
+                mbar_arrive_expect_tx(bar(C::B_QFULL + qs), C::TILE_BYTES);
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
-                    tma_load_4d(&tm_q, base + C::Q_OFF + x * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                bar(C::B_QFULL + x), c * (128 / C::ESZ), U.h, U.m[x] * 128, U.b);
-                ++qn;
+                    tma_load_4d(&tm_q, base + C::Q_OFF + qs * C::TILE_BYTES + c * C::CHUNK_BYTES,
+                                bar(C::B_QFULL + qs), c * (128 / C::ESZ), U.h, U.m[x] * 128, U.b);
+                qarmed |= 1u << qs;
+                qarmed_par = (qarmed_par & ~(1u << qs)) | (qph << qs);
+                ++qc;
                 return true;
             };
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
                 const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
-                if (U.act[0]) ok = ok && load_q(0, U, qn0);
-                if (U.act[1]) ok = ok && load_q(1, U, qn1);
+                if (U.act[0]) ok = ok && load_q(0, U);
+                if (U.act[1]) ok = ok && load_q(1, U);
                 const int hk = U.h / a.group;        // K/V head of this query head
                 for (int t = 0; t < U.T && ok; ++t) {
                     const int j = U.jhi - 1 - t;
@@ -320,20 +333,25 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             for (int s = 0; s < C::NSTAGE; ++s)
                 if (armed & (1u << s))
                     mbar_wait_quiet(bar(C::B_KVFULL + s), (armed_par >> s) & 1u, 500000000ull);
-            if (qn0 > 0) mbar_wait_quiet(bar(C::B_QFULL + 0), (qn0 - 1) & 1, 500000000ull);
-            if (qn1 > 0) mbar_wait_quiet(bar(C::B_QFULL + 1), (qn1 - 1) & 1, 500000000ull);
+            for (int q = 0; q < C::NQ; ++q)
+                if (qarmed & (1u << q))
+                    mbar_wait_quiet(bar(C::B_QFULL + q), (qarmed_par >> q) & 1u, 500000000ull);
         }
         __syncwarp();
     } else if (warp == 9) {
         // =================== MMA issuer (whole warp, one elected lane issues) ===================
         {
             WaitCtx w{abort_flag, a.status, kRoleMma};
-            int qn0 = 0, qn1 = 0, un0 = 0, un1 = 0;
+            uint32_t qc = 0;                        // Q slots in the producer's order
+            int un0 = 0, un1 = 0;
             uint32_t pph0 = 0, pph1 = 0;
             uint32_t slot = 0, phase = 0;
             bool ok = true;
             for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
                 const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
+                uint32_t qs0 = 0, qp0 = 0, qs1 = 0, qp1 = 0;   // Q slot and parity per tile
+                if (U.act[0]) { qs0 = qc % C::NQ; qp0 = (qc / C::NQ) & 1u; ++qc; }
+                if (U.act[1]) { qs1 = qc % C::NQ; qp1 = (qc / C::NQ) & 1u; ++qc; }
                 for (int t = 0; t <= U.T && ok; ++t) {
                     const bool has_v = t > 0, has_k = t < U.T;
                     uint32_t vslot = 0, vph = 0, kslot = 0, kph = 0;
@@ -342,8 +360,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     bool v_ready = false, k_ready = false;
                     // One Q tile's two GEMMs of this step; x is a literal at
                     // each call site, so every per-tile counter is a register.
-                    auto step_x = [&](const int x, const int t0x, const int t1x, int &qn,
-                                      int &un, uint32_t &pph) __attribute__((always_inline)) -> bool {
+                    auto step_x = [&](const int x, const int t0x, const int t1x, const uint32_t qs,
+                                      const uint32_t qp, int &un,
+                                      uint32_t &pph) __attribute__((always_inline)) -> bool {
                         // ---- O_x += P_x V_(t-1) ----
                         if (has_v && t - 1 >= t0x && (!kExt || t - 1 < t1x)) {
                             if (!v_ready) {
@@ -376,12 +395,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                 if (!mbar_wait_warp(bar(C::B_KVFULL + kslot), kph, w, 13)) return false;
                                 k_ready = true;
                             }
-                            if (t == t0x) {
-                                if (!mbar_wait_warp(bar(C::B_QFULL + x), qn & 1, w, 14)) return false;
-                                ++qn;
-                            }
+                            if (t == t0x &&
+                                !mbar_wait_warp(bar(C::B_QFULL + qs), qp, w, 14)) return false;
                             tc_fence_after();
-                            const uint64_t qd = smem_desc_sw128(base + C::Q_OFF + x * C::TILE_BYTES, 16u, 1024u);
+                            const uint64_t qd = smem_desc_sw128(base + C::Q_OFF + qs * C::TILE_BYTES, 16u, 1024u);
                             const uint64_t kd = smem_desc_sw128(base + C::KV_OFF + kslot * C::TILE_BYTES, 16u, 1024u);
 #pragma unroll
                             for (int kk = 0; kk < C::QK_STEPS; ++kk) {
@@ -394,12 +411,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                      C::IDESC_QK, kk > 0 ? 1u : 0u);
                             }
                             mma_commit_elect(bar(C::B_SFULL + x));
-                            if (t == t1x - 1) mma_commit_elect(bar(C::B_QEMPTY + x));
+                            if (t == t1x - 1) mma_commit_elect(bar(C::B_QEMPTY + qs));
                         }
                         return true;
                     };
-                    ok = step_x(0, U.t0[0], kExt ? U.t1[0] : U.T, qn0, un0, pph0) &&
-                         step_x(1, U.t0[1], kExt ? U.t1[1] : U.T, qn1, un1, pph1);
+                    ok = step_x(0, U.t0[0], kExt ? U.t1[0] : U.T, qs0, qp0, un0, pph0) &&
+                         step_x(1, U.t0[1], kExt ? U.t1[1] : U.T, qs1, qp1, un1, pph1);
                     if (!ok) break;
                     if (has_k) mma_commit_elect(bar(C::B_KVEMPTY + kslot));
                     if (has_v) mma_commit_elect(bar(C::B_KVEMPTY + vslot));
