@@ -125,14 +125,30 @@ struct BwdCfg {
                          KVB_PFULL = 4, KVB_DSFULL = 5, KVB_ACCFULL = 6, KVB_ACCEMPTY = 7,
                          KVB_MMADONE = 8, KVB_QFULL = 9, KVB_QEMPTY = KVB_QFULL + QN,
                          KVB_DOFULL = KVB_QEMPTY + QN, KVB_DOEMPTY = KVB_DOFULL + DN,
-                         KV_NBAR = KVB_DOEMPTY + DN;
+                         KVB_STFULL1 = KVB_DOEMPTY + DN, KV_NBAR = KVB_STFULL1 + 1;
     static constexpr uint32_t KV_MISC_OFF = KV_BAR_OFF + KV_NBAR * 8;
     static constexpr uint32_t KV_SMEM = KV_MISC_OFF + 16 + 1024;
     // TMEM: S^T [0,128) (P^T over its first 64), dP^T [128,256) (dS^T over
-    // its first 64), dV [256,256+D), dK [256+D,256+2D)
+    // its first 64), dV [256,256+D), dK [256+D,256+2D); at d = 64 a second
+    // S^T buffer [384,512), so the S^T of query tile i+2 is computed while
+    // tile i+1's exponentials run (d = 128 fills TMEM with one).
     static constexpr uint32_t KV_COL_ST = 0, KV_COL_DPT = 128, KV_COL_DV = 256,
-                              KV_COL_DK = 256 + D;
+                              KV_COL_DK = 256 + D, KV_COL_ST1 = 256 + 2 * D;
+    static constexpr bool KV_SDB = D == 64;
     static_assert(KV_COL_DK + D <= TMEM_COLS, "dK/dV kernel TMEM budget");
+    static_assert(!KV_SDB || KV_COL_ST1 + 128 <= TMEM_COLS, "second S^T buffer");
+    // S^T buffer and its full barrier for the n-th S^T tile of the CTA
+    __host__ __device__ static constexpr uint32_t st_buf(uint32_t n) { return KV_SDB ? (n & 1u) : 0u; }
+    __host__ __device__ static constexpr uint32_t st_col(uint32_t n) {
+        return st_buf(n) ? KV_COL_ST1 : KV_COL_ST;
+    }
+    __host__ __device__ static constexpr int st_bar(uint32_t n) {
+        return st_buf(n) ? KVB_STFULL1 : KVB_STFULL;
+    }
+    // parity of the n-th S^T tile's wait on its barrier
+    __host__ __device__ static constexpr uint32_t st_par(uint32_t n) {
+        return KV_SDB ? ((n >> 1) & 1u) : (n & 1u);
+    }
     static_assert(DQ_SMEM <= 232448 && KV_SMEM <= 232448, "shared memory");
 };
 
@@ -660,6 +676,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(bar(C::KVB_KVFULL), 1);
         mbar_init(bar(C::KVB_KVEMPTY), 1);
         mbar_init(bar(C::KVB_STFULL), 1);
+        mbar_init(bar(C::KVB_STFULL1), 1);
         mbar_init(bar(C::KVB_DPTFULL), 1);
         mbar_init(bar(C::KVB_PFULL), C::N_EW);
         mbar_init(bar(C::KVB_DSFULL), C::N_EW);
@@ -747,16 +764,25 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             ok = mbar_wait_warp(bar(C::KVB_KVFULL), kvph, w, 90);
             if (!ok) break;
             kvph ^= 1;
-            ok = wait_q(q_item);
+            // q_item counts the CTA's query tiles, and so its S^T tiles
+            auto g1 = [&](uint32_t i) __attribute__((always_inline)) -> bool {
+                if (!wait_q(i)) return false;
+                tc_fence_after();
+                gemm_ss_kmajor<D>(tbase + C::st_col(i), base + C::KV_K_OFF, q_tile(i), C::IDESC_SS);
+                mma_commit_elect(bar(C::st_bar(i)));
+                return true;
+            };
+            ok = g1(q_item);
             if (!ok) break;
-            tc_fence_after();
-            gemm_ss_kmajor<D>(tbase + C::KV_COL_ST, base + C::KV_K_OFF, q_tile(q_item), C::IDESC_SS);
-            mma_commit_elect(bar(C::KVB_STFULL));
             ok = wait_do(q_item);
             if (!ok) break;
             tc_fence_after();
             gemm_ss_kmajor<D>(tbase + C::KV_COL_DPT, base + C::KV_V_OFF, do_tile(q_item), C::IDESC_SS);
             mma_commit_elect(bar(C::KVB_DPTFULL));
+            if (C::KV_SDB && Ti > 1) {               // the second buffer starts one tile ahead
+                ok = g1(q_item + 1);
+                if (!ok) break;
+            }
             for (int k = 0; ok && k < Ti; ++k) {
                 const uint32_t ic = q_item + k, in = ic + 1;
                 const bool more = k + 1 < Ti;
@@ -767,16 +793,14 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 pph ^= 1;
                 if (k == 0) accph ^= 1;
                 tc_fence_after();
-                gemm_ts_mn(tbase + C::KV_COL_DV, tbase + C::KV_COL_ST + 32, do_tile(ic), C::IDESC_ACC,
+                gemm_ts_mn(tbase + C::KV_COL_DV, tbase + C::st_col(ic) + 32, do_tile(ic), C::IDESC_ACC,
                            k > 0);
                 mma_commit_elect(bar(C::KVB_DOEMPTY + RO::slot(ic)));
-                // ---- G1(i+1) ----
-                if (more) {
-                    ok = wait_q(in);
+                // ---- G1 into the S^T buffer G3 has just read: tile i+2
+                //      (two buffers) or i+1 (one) ----
+                if (C::KV_SDB ? k + 2 < Ti : more) {
+                    ok = g1(C::KV_SDB ? ic + 2 : in);
                     if (!ok) break;
-                    tc_fence_after();
-                    gemm_ss_kmajor<D>(tbase + C::KV_COL_ST, base + C::KV_K_OFF, q_tile(in), C::IDESC_SS);
-                    mma_commit_elect(bar(C::KVB_STFULL));
                 }
                 // ---- G4: dK += dS^T Q_i (dS^T at columns 32..95 of dP^T) ----
                 ok = mbar_wait_warp(bar(C::KVB_DSFULL), dsph, w, 95);
@@ -812,7 +836,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         WaitCtx w{abort_flag, a.status, kRoleSoftmax0};
         const float sl2 = a.scale_log2;
         const float2 c2 = make_float2(sl2, sl2);
-        uint32_t stph = 0, dpph = 0, accph = 0;
+        uint32_t stn = 0, dpph = 0, accph = 0;    // stn: S^T tiles of this CTA so far
         bool ok = true;
         for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
             const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
@@ -833,12 +857,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const float4 *lse4 = reinterpret_cast<const float4 *>(a.ws_l + wrow + i * 128 + col0);
                 const float4 *dd4 = reinterpret_cast<const float4 *>(a.ws_d + wrow + i * 128 + col0);
                 // ---- P^T = exp2(S^T c - LSE2[q]) ----
-                ok = mbar_wait(bar(C::KVB_STFULL), stph, w, 100);
+                ok = mbar_wait(bar(C::st_bar(stn)), C::st_par(stn), w, 100);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
-                stph ^= 1;
                 tc_fence_after();
                 uint32_t sv[64];
-                const uint32_t tST = tbase + lane_off + C::KV_COL_ST;
+                const uint32_t tST = tbase + lane_off + C::st_col(stn);
+                ++stn;
                 tmem_ld32(tST + col0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                 tmem_ld32(tST + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
                 tmem_ld_wait();
