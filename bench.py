@@ -274,7 +274,7 @@ def oracle_bwd_sample_rate(B, H, N, d, causal, rows, n_heads, threads, var=None)
         if var is None:
             oracle.attention_bwd_head(*t, alpha, causal)
         else:
-            oracle.attention_bwd_ext_head(*t, alpha, var["window"], 0.0,
+            oracle.attention_bwd_ext_head(*t, alpha, var["window"], var["softcap"],
                                           None if sinks is None else float(sinks[0]))
 
     t0 = time.perf_counter()
@@ -325,7 +325,7 @@ def run_bwd(args, B, H, N, d, rank, world):
             rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
         else:
             rc = fa.fa_fwd_ext(q, k, v, o, lse, B, H, H, N, d, alpha, var["window"][0],
-                               var["window"][1], 0.0, sinks_t, fa.FA_BF16, sp)
+                               var["window"][1], var["softcap"], sinks_t, fa.FA_BF16, sp)
         if rc != fa.FA_OK:
             raise fa.FaError(rc, "fa_fwd")
 
@@ -335,8 +335,8 @@ def run_bwd(args, B, H, N, d, rank, world):
                            fa.FA_BF16, sp)
         else:
             rc = fa.fa_bwd_ext(q, k, v, o, do, lse, ws, dq, dk, dv, B, H, N, d, alpha,
-                               var["window"][0], var["window"][1], sinks_t, dsinks_t,
-                               fa.FA_BF16, sp)
+                               var["window"][0], var["window"][1], var["softcap"], sinks_t,
+                               dsinks_t, fa.FA_BF16, sp)
         if rc != fa.FA_OK:
             raise fa.FaError(rc, "fa_bwd")
 
@@ -753,8 +753,6 @@ def main():
                                          or args.causal or args.d not in (64, 128)):
         ap.error("--window/--softcap/--sinks apply to BF16, d 64 or 128, without --causal "
                  "(use --window -1 0), --splits or --fp8")
-    if args.bwd and args.softcap:
-        ap.error("--softcap has no backward")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if world > 1 and args.impl == "ours":

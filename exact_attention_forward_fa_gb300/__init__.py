@@ -72,7 +72,7 @@ def load():
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_bwd.restype = i
     lib.fa_bwd_ext.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i,
-                               vp, vp, i, vp]
+                               f, vp, vp, i, vp]
     lib.fa_bwd_ext.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_bwd_noalloc.restype = i
@@ -267,20 +267,21 @@ def fa_bwd(q, k, v, o, dout, lse, workspace, dq, dk, dv, B: int, H: int, N: int,
 
 
 def fa_bwd_ext(q, k, v, o, dout, lse, workspace, dq, dk, dv, B: int, H: int, N: int, d: int,
-               alpha: float, window_left: int, window_right: int, sinks, dsinks, dtype: int,
-               stream=None) -> int:
+               alpha: float, window_left: int, window_right: int, softcap: float, sinks,
+               dsinks, dtype: int, stream=None) -> int:
     """Direct call of the C entry point: the backward of fa_fwd_ext with a
-    local window; sinks/dsinks may be None (see include/fa.h)."""
+    local window and softcap; sinks/dsinks may be None (see include/fa.h)."""
     return load().fa_bwd_ext(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                              _ptr(workspace), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H),
                              int(N), int(d), float(alpha), int(window_left), int(window_right),
-                             _ptr(sinks), _ptr(dsinks), int(dtype), _stream(stream))
+                             float(softcap), _ptr(sinks), _ptr(dsinks), int(dtype),
+                             _stream(stream))
 
 
-def attention_backward_ext(q, k, v, o, lse, dout, window=(-1, -1), sinks=None,
-                           alpha: float | None = None, stream=None):
+def attention_backward_ext(q, k, v, o, lse, dout, window=(-1, -1), softcap: float = 0.0,
+                           sinks=None, alpha: float | None = None, stream=None):
     """Gradients (dQ, dK, dV, dsinks or None) for the forward of
-    ``attention_ext`` with a window and optional sinks (no softcap)."""
+    ``attention_ext`` with a window, softcap and optional sinks."""
     import torch
     if q.dtype == torch.bfloat16:
         dt = FA_BF16
@@ -295,7 +296,7 @@ def attention_backward_ext(q, k, v, o, lse, dout, window=(-1, -1), sinks=None,
     ws = torch.empty((bwd_workspace_floats(B, H, N),), dtype=torch.float32, device=q.device)
     ds = None if sinks is None else torch.empty((H,), dtype=torch.float32, device=q.device)
     rc = fa_bwd_ext(q, k, v, o, dout, lse, ws, dq, dk, dv, B, H, N, d, alpha, int(window[0]),
-                    int(window[1]), sinks, ds, dt, stream)
+                    int(window[1]), float(softcap), sinks, ds, dt, stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_ext")
     return dq, dk, dv, ds

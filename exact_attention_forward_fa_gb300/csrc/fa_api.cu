@@ -451,12 +451,15 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
 static fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
                           const void *dout, const float *lse, float *workspace, void *dq,
                           void *dk, void *dv, int B, int H, int N, int d, float alpha,
-                          int causal, bool win, int wl, int wr, const float *sinks,
-                          float *dsinks, fa_dtype dtype, void *stream) {
+                          int causal, bool win, int wl, int wr, float softcap,
+                          const float *sinks, float *dsinks, fa_dtype dtype, void *stream) {
     // ---- host-side validation: nothing is launched on failure ----
     if (!q || !k || !v || !o || !dout || !lse || !workspace || !dq || !dk || !dv)
         return FA_ERR_INVALID_ARG;
     if (win && (wl < -1 || wr < -1)) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(softcap) || softcap < 0.f) return FA_ERR_INVALID_ARG;
+    const double cap_pre = softcap > 0.f ? static_cast<double>(alpha) / softcap : 0.0;
+    if (!std::isfinite(static_cast<float>(cap_pre))) return FA_ERR_INVALID_ARG;
     if (dsinks && !sinks) return FA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(sinks) & 3u) || (reinterpret_cast<uintptr_t>(dsinks) & 3u))
         return FA_ERR_MISALIGNED;
@@ -518,7 +521,11 @@ static fa_status bwd_impl(const void *q, const void *k, const void *v, const voi
     L.stream = static_cast<cudaStream_t>(stream);
     L.args.wl = wl;
     L.args.wr = wr;
-    cudaError_t e = win ? fa::launch_bwd_win(L) : fa::launch_bwd(L);
+    L.args.sc_pre = static_cast<float>(cap_pre);
+    L.args.sc_post = static_cast<float>(static_cast<double>(softcap) * 1.4426950408889634);
+    cudaError_t e = softcap > 0.f ? fa::launch_bwd_win_softcap(L)
+                    : win         ? fa::launch_bwd_win(L)
+                                  : fa::launch_bwd(L);
     if (e == cudaSuccess && dsinks) e = fa::launch_bwd_dsink(L.args, sinks, dsinks, L.stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -527,16 +534,16 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
                  const float *lse, float *workspace, void *dq, void *dk, void *dv, int B, int H,
                  int N, int d, float alpha, int causal, fa_dtype dtype, void *stream) {
     return bwd_impl(q, k, v, o, dout, lse, workspace, dq, dk, dv, B, H, N, d, alpha, causal,
-                    false, -1, -1, nullptr, nullptr, dtype, stream);
+                    false, -1, -1, 0.f, nullptr, nullptr, dtype, stream);
 }
 
 fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
                      const void *dout, const float *lse, float *workspace, void *dq, void *dk,
                      void *dv, int B, int H, int N, int d, float alpha, int window_left,
-                     int window_right, const float *sinks, float *dsinks, fa_dtype dtype,
-                     void *stream) {
+                     int window_right, float softcap, const float *sinks, float *dsinks,
+                     fa_dtype dtype, void *stream) {
     return bwd_impl(q, k, v, o, dout, lse, workspace, dq, dk, dv, B, H, N, d, alpha, 0, true,
-                    window_left, window_right, sinks, dsinks, dtype, stream);
+                    window_left, window_right, softcap, sinks, dsinks, dtype, stream);
 }
 
 // ---------------------------------------------------------------------------

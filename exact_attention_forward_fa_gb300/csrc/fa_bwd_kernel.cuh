@@ -62,6 +62,10 @@ struct BwdArgs {
     // Local window (kWin instantiations): key j is hidden from query i when
     // j > i + wr (wr >= 0) or j < i - wl (wl >= 0); -1 is no bound.
     int wl, wr;
+    // Softcap c (kCap instantiations): the score is c tanh(alpha s / c),
+    // t = tanh(sc_pre s) with sc_pre = alpha / c, in log2 units sc_post t
+    // with sc_post = c log2(e); dS picks up the factor 1 - t^2.
+    float sc_pre, sc_post;
 };
 
 // Visible keys [win_klo, win_khi) of query row i (0 <= i < N), and visible
@@ -332,7 +336,7 @@ __device__ __forceinline__ void store_cols(void *dst_base, const BwdArgs &a, int
 // and dP(t+1); dS is double-buffered so dQ(t) reads dS(t) while dS(t+1) is
 // written.
 // ---------------------------------------------------------------------------
-template <int D, bool kCausal, bool kBF16, bool kWin = false>
+template <int D, bool kCausal, bool kBF16, bool kWin = false, bool kCap = false>
 __global__ void __launch_bounds__(320, 1)
 fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -537,7 +541,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // rows: their P is 0) and D of this row, from the workspace
             const size_t widx = (static_cast<size_t>(U.b) * a.H + U.h) * a.NP + grow;
             const float lse2 = a.ws_l[widx], drow = a.ws_d[widx];
-            const float2 c2 = make_float2(sl2, sl2);
+            const float2 c2 = kCap ? make_float2(a.sc_post, a.sc_post) : make_float2(sl2, sl2);
             const float2 nl2 = make_float2(-lse2, -lse2);
             const float2 nd2 = make_float2(-drow, -drow);
             for (int t = 0; t < T; ++t) {
@@ -563,11 +567,17 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     llo = klo_r - j * 128 - col0;
                 }
                 float *pf = reinterpret_cast<float *>(sv);
+                if constexpr (kCap) {
+                    // keep t = tanh(alpha s / c); P comes from t in the dS step
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
-                    const float2 x = __ffma2_rn(make_float2(pf[c], pf[c + 1]), c2, nl2);
-                    pf[c] = (c < lim && (!kWin || c >= llo)) ? ex2_approx(x.x) : 0.f;
-                    pf[c + 1] = (c + 1 < lim && (!kWin || c + 1 >= llo)) ? ex2_approx(x.y) : 0.f;
+                    for (int c = 0; c < 64; ++c) pf[c] = tanh_approx(pf[c] * a.sc_pre);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 64; c += 2) {
+                        const float2 x = __ffma2_rn(make_float2(pf[c], pf[c + 1]), c2, nl2);
+                        pf[c] = (c < lim && (!kWin || c >= llo)) ? ex2_approx(x.x) : 0.f;
+                        pf[c + 1] = (c + 1 < lim && (!kWin || c + 1 >= llo)) ? ex2_approx(x.y) : 0.f;
+                    }
                 }
                 // ---- dS(t) = P o (dP - D) -> TMEM dS[t%2] ----
                 ok = mbar_wait(bar(C::DQB_DPFULL), dpph, w, 71);
@@ -584,7 +594,16 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 for (int i = 0; i < 64; i += 2) {
                     const float2 g = __fadd2_rn(
                         make_float2(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), nd2);
-                    const float2 ds = __fmul2_rn(make_float2(pf[i], pf[i + 1]), g);
+                    float2 pp = make_float2(pf[i], pf[i + 1]);
+                    if constexpr (kCap) {
+                        // P = 2^(t c log2(e) - LSE2), and dS/du = 1 - t^2
+                        const float2 x = __ffma2_rn(pp, c2, nl2);
+                        const float2 dt = __ffma2_rn(make_float2(-pp.x, -pp.y), pp,
+                                                     make_float2(1.f, 1.f));
+                        pp.x = (i < lim && (!kWin || i >= llo)) ? ex2_approx(x.x) * dt.x : 0.f;
+                        pp.y = (i + 1 < lim && (!kWin || i + 1 >= llo)) ? ex2_approx(x.y) * dt.y : 0.f;
+                    }
+                    const float2 ds = __fmul2_rn(pp, g);
                     pk[i / 2] = pack2<kBF16>(ds.x, ds.y);
                 }
                 tmem_st32(tbase + lane_off + C::DQ_COL_DS + (t & 1) * 64u + half * 32, pk);
@@ -640,7 +659,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // dO until G3); LSE2 and D of the query columns are read from the padded
 // workspace through L1, where the producer prefetches each tile's lines.
 // ---------------------------------------------------------------------------
-template <int D, bool kCausal, bool kBF16, bool kWin = false>
+template <int D, bool kCausal, bool kBF16, bool kWin = false, bool kCap = false>
 __global__ void __launch_bounds__(320, 1)
 fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -834,7 +853,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int col0 = half * 64;                          // this warp's query columns
         WaitCtx w{abort_flag, a.status, kRoleSoftmax0};
-        const float sl2 = a.scale_log2;
+        const float sl2 = kCap ? a.sc_post : a.scale_log2;
         const float2 c2 = make_float2(sl2, sl2);
         uint32_t stn = 0, dpph = 0, accph = 0;    // stn: S^T tiles of this CTA so far
         bool ok = true;
@@ -875,6 +894,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
                 float *pf = reinterpret_cast<float *>(sv);
                 uint32_t pk[32];
+                if constexpr (kCap) {
+                    // keep t = tanh(alpha s / c) in sv; P = 2^(t c log2(e) - LSE2)
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) pf[c] = tanh_approx(pf[c] * a.sc_pre);
+                }
 #pragma unroll
                 for (int c = 0; c < 64; c += 4) {
                     const float4 l4 = __ldg(lse4 + c / 4);
@@ -882,12 +906,18 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                                   make_float2(-l4.x, -l4.y));
                     const float2 x23 = __ffma2_rn(make_float2(pf[c + 2], pf[c + 3]), c2,
                                                   make_float2(-l4.z, -l4.w));
-                    pf[c + 0] = (c + 0 >= lo && (!kWin || c + 0 < hi)) ? ex2_approx(x01.x) : 0.f;
-                    pf[c + 1] = (c + 1 >= lo && (!kWin || c + 1 < hi)) ? ex2_approx(x01.y) : 0.f;
-                    pf[c + 2] = (c + 2 >= lo && (!kWin || c + 2 < hi)) ? ex2_approx(x23.x) : 0.f;
-                    pf[c + 3] = (c + 3 >= lo && (!kWin || c + 3 < hi)) ? ex2_approx(x23.y) : 0.f;
-                    pk[c / 2] = pack2<kBF16>(pf[c], pf[c + 1]);
-                    pk[c / 2 + 1] = pack2<kBF16>(pf[c + 2], pf[c + 3]);
+                    const float p0 = (c + 0 >= lo && (!kWin || c + 0 < hi)) ? ex2_approx(x01.x) : 0.f;
+                    const float p1 = (c + 1 >= lo && (!kWin || c + 1 < hi)) ? ex2_approx(x01.y) : 0.f;
+                    const float p2 = (c + 2 >= lo && (!kWin || c + 2 < hi)) ? ex2_approx(x23.x) : 0.f;
+                    const float p3 = (c + 3 >= lo && (!kWin || c + 3 < hi)) ? ex2_approx(x23.y) : 0.f;
+                    if constexpr (!kCap) {
+                        pf[c + 0] = p0;
+                        pf[c + 1] = p1;
+                        pf[c + 2] = p2;
+                        pf[c + 3] = p3;
+                    }
+                    pk[c / 2] = pack2<kBF16>(p0, p1);
+                    pk[c / 2 + 1] = pack2<kBF16>(p2, p3);
                 }
                 // 16-bit P^T of query columns [col0, col0+64) -> S^T columns
                 // 32 + col0/2 .. +32: columns this warp has read itself
@@ -915,8 +945,21 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const float2 g23 = __fadd2_rn(
                         make_float2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])),
                         make_float2(-d4.z, -d4.w));
-                    const float2 ds01 = __fmul2_rn(make_float2(pf[c], pf[c + 1]), g01);
-                    const float2 ds23 = __fmul2_rn(make_float2(pf[c + 2], pf[c + 3]), g23);
+                    float2 p01 = make_float2(pf[c], pf[c + 1]), p23 = make_float2(pf[c + 2], pf[c + 3]);
+                    if constexpr (kCap) {
+                        // P again from t, times dS/du = 1 - t^2
+                        const float4 l4 = __ldg(lse4 + c / 4);
+                        const float2 x01 = __ffma2_rn(p01, c2, make_float2(-l4.x, -l4.y));
+                        const float2 x23 = __ffma2_rn(p23, c2, make_float2(-l4.z, -l4.w));
+                        const float2 t01 = __ffma2_rn(make_float2(-p01.x, -p01.y), p01, make_float2(1.f, 1.f));
+                        const float2 t23 = __ffma2_rn(make_float2(-p23.x, -p23.y), p23, make_float2(1.f, 1.f));
+                        p01.x = (c + 0 >= lo && (!kWin || c + 0 < hi)) ? ex2_approx(x01.x) * t01.x : 0.f;
+                        p01.y = (c + 1 >= lo && (!kWin || c + 1 < hi)) ? ex2_approx(x01.y) * t01.y : 0.f;
+                        p23.x = (c + 2 >= lo && (!kWin || c + 2 < hi)) ? ex2_approx(x23.x) * t23.x : 0.f;
+                        p23.y = (c + 3 >= lo && (!kWin || c + 3 < hi)) ? ex2_approx(x23.y) * t23.y : 0.f;
+                    }
+                    const float2 ds01 = __fmul2_rn(p01, g01);
+                    const float2 ds23 = __fmul2_rn(p23, g23);
                     pk[c / 2] = pack2<kBF16>(ds01.x, ds01.y);
                     pk[c / 2 + 1] = pack2<kBF16>(ds23.x, ds23.y);
                 }

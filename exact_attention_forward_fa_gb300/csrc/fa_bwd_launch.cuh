@@ -27,13 +27,13 @@ inline cudaError_t set_smem_once(K kern, int bytes, unsigned long long &configur
 }
 
 // The three kernels of one backward, in order on the caller's stream.
-// kWin: the window instantiations (kCausal false).
-template <int D, bool kCausal, bool kBF16, bool kWin = false>
+// kWin: the window instantiations (kCausal false); kCap: with a softcap.
+template <int D, bool kCausal, bool kBF16, bool kWin = false, bool kCap = false>
 cudaError_t launch_bwd_inst(const BwdLaunch &L) {
     using C = BwdCfg<D, kBF16>;
     static unsigned long long cfg_dq = 0ull, cfg_kv = 0ull;
-    auto kdq = fa_bwd_dq_kernel<D, kCausal, kBF16, kWin>;
-    auto kkv = fa_bwd_dkdv_kernel<D, kCausal, kBF16, kWin>;
+    auto kdq = fa_bwd_dq_kernel<D, kCausal, kBF16, kWin, kCap>;
+    auto kkv = fa_bwd_dkdv_kernel<D, kCausal, kBF16, kWin, kCap>;
     cudaError_t e = set_smem_once(kdq, static_cast<int>(C::DQ_SMEM), cfg_dq);
     if (e != cudaSuccess) return e;
     e = set_smem_once(kkv, static_cast<int>(C::KV_SMEM), cfg_kv);

@@ -54,6 +54,8 @@ struct BwdLaunch {
 cudaError_t launch_bwd(const BwdLaunch &L);
 // The same for a local window (L.args.wl, L.args.wr; L.causal unused).
 cudaError_t launch_bwd_win(const BwdLaunch &L);
+// The same with a softcap (L.args.sc_pre, L.args.sc_post).
+cudaError_t launch_bwd_win_softcap(const BwdLaunch &L);
 // Gradient of per-head sink logits: dsinks[h] = -sum_{b,i} 2^(sigma_h log2 e
 // - LSE2_i) D_i over the workspace rows of the backward (one CTA per head).
 cudaError_t launch_bwd_dsink(const BwdArgs &a, const float *sinks, float *dsinks,

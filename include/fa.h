@@ -216,12 +216,17 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  int causal, fa_dtype dtype, void *stream);
 
 /*
- * fa_bwd_ext -- fa_bwd for the forward of fa_fwd_ext with a local window
- * and optional sinks ("FlashAttention-3 on Hopper", sec. 7.8: a right
- * window bounds the first query tile a key tile visits, a left window the
- * last; sec. 4.6: sinks).
+ * fa_bwd_ext -- fa_bwd for the forward of fa_fwd_ext with a local window,
+ * an optional softcap and optional sinks ("FlashAttention-3 on Hopper",
+ * sec. 7.8: a right window bounds the first query tile a key tile visits, a
+ * left window the last, and the softcap enters as a score modifier; sec.
+ * 4.6: sinks; "03 FA3", sec. 5: softcap).
  *   window_left, window_right : as for fa_fwd_ext (-1 = no bound; values
  *            below -1 return FA_ERR_INVALID_ARG).
+ *   softcap : the forward's c (0: none).  With c > 0 both kernels recompute
+ *            t = tanh(alpha s / c) (tanh.approx.f32), form P from t and the
+ *            LSE, and scale dS by dS/du = 1 - t^2.  Negative, non-finite or
+ *            alpha / c beyond FP32 returns FA_ERR_INVALID_ARG.
  *   lse    : from fa_fwd_ext with the same window and sinks.  The gradients
  *            of q, k and v need nothing else from the sinks: P is formed
  *            from that LSE, which already holds the sink term.
@@ -230,15 +235,14 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
  *            of sigma_h, -sum over batches and rows of e^(sigma_h - LSE) D
  *            (D = rowsum(dO o O)), reduced in a fixed order.  dsinks
  *            without sinks returns FA_ERR_INVALID_ARG.
- * No softcap: a forward with a softcap has no backward in this library.
  * Other arguments, results and errors as fa_bwd (H_kv = H, d in {64, 128}).
  */
 fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
                      const void *dout, const float *lse, float *workspace,
                      void *dq, void *dk, void *dv, int B, int H, int N, int d,
                      float alpha, int window_left, int window_right,
-                     const float *sinks, float *dsinks, fa_dtype dtype,
-                     void *stream);
+                     float softcap, const float *sinks, float *dsinks,
+                     fa_dtype dtype, void *stream);
 
 /*
  * fa_bwd_noalloc -- fa_bwd without a caller-provided workspace (the pages

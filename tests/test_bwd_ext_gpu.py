@@ -1,6 +1,7 @@
-"""GPU parity of the windowed backward (fa_bwd_ext, through the C ABI)
+"""GPU parity of the variants' backward (fa_bwd_ext, through the C ABI)
 against the FP64 oracle gradients of the variants ("FlashAttention-3 on
-Hopper", sec. 7.8 local attention in the backward; sec. 4.6 sinks).
+Hopper", sec. 7.8 local attention and score modifiers in the backward;
+sec. 4.6 sinks; "03 FA3" sec. 5 softcap).
 
 The forward runs first on the GPU (fa_fwd_ext gives O and LSE, with the
 sinks when given); the oracle computes dQ, dK, dV and the sink logits'
@@ -35,13 +36,13 @@ def _inputs(B, H, N, d, dtype, seed):
     return q, k, v, do
 
 
-def _gpu(fa, q, k, v, do, window, sinks, alpha):
+def _gpu(fa, q, k, v, do, window, sinks, alpha, softcap=0.0):
     dev = torch.device("cuda")
     qd, kd, vd, dod = (x.to(dev) for x in (q, k, v, do))
     sk = None if sinks is None else torch.from_numpy(np.asarray(sinks, np.float32)).to(dev)
-    o, lse = fa.attention_ext(qd, kd, vd, window=window, sinks=sk, alpha=alpha)
+    o, lse = fa.attention_ext(qd, kd, vd, window=window, softcap=softcap, sinks=sk, alpha=alpha)
     dq, dk, dv, ds = fa.attention_backward_ext(qd, kd, vd, o, lse, dod, window=window,
-                                               sinks=sk, alpha=alpha)
+                                               softcap=softcap, sinks=sk, alpha=alpha)
     assert fa.fa_check_status() == fa.FA_OK
     g = [x.float().cpu().numpy().astype(np.float64) for x in (dq, dk, dv)]
     return g, (None if ds is None else ds.cpu().numpy().astype(np.float64))
@@ -60,9 +61,9 @@ def _check(got, ref, u, rms_units=1.5):
         assert err.max() <= 4 * u * scale, f"max {err.max() / scale:.3e} of max|ref|"
 
 
-def _dsink_bound(q, k, v, do, alpha, window, sinks, u):
+def _dsink_bound(q, k, v, do, alpha, window, sinks, u, softcap=0.0):
     """4 u sum_{b,i} |P_i,sink D_i| per head, from the oracle's O and LSE."""
-    o, lse = oracle.attention_ext(q, k, v, alpha, window=window, sinks=sinks,
+    o, lse = oracle.attention_ext(q, k, v, alpha, window=window, softcap=softcap, sinks=sinks,
                                   n_threads=THREADS)
     D = np.sum(oracle._f64(do) * o, axis=-1)                  # [B, N, H]
     p = np.exp(np.asarray(sinks, np.float64)[None, :, None] - lse)   # [B, H, N]
@@ -102,6 +103,33 @@ def test_bwd_ext_parity(gpu_lib, B, H, N, d, window, sinks, dtype):
         assert np.all(np.abs(ds - dsr) <= bound + 1e-6), (ds, dsr, bound)
     else:
         assert ds is None
+
+
+SOFTCAP_CASES = [
+    # (B, H, N, d, window, softcap, sinks, dtype)
+    (2, 2, 1000, 128, (-1, -1), 50.0, False, "bf16"),  # softcap alone
+    (1, 2, 1000, 128, (-1, 0), 5.0, False, "bf16"),    # a tight softcap, causal shape
+    (1, 2, 777, 64, (256, 0), 30.0, True, "bf16"),     # with a window and sinks
+    (1, 2, 513, 128, (100, 100), 20.0, False, "fp16"),
+    (1, 3, 1000, 64, (-1, 0), 50.0, True, "bf16"),
+]
+
+
+@pytest.mark.parametrize("B,H,N,d,window,softcap,sinks,dtype", SOFTCAP_CASES)
+def test_bwd_ext_softcap_parity(gpu_lib, B, H, N, d, window, softcap, sinks, dtype):
+    # Scores pass through c tanh(s / c): dS carries 1 - t^2.  tanh.approx.f32
+    # (abs error 8e-6) moves P by at most c * 8e-6 relative, far below u.
+    q, k, v, do = _inputs(B, H, N, d, dtype, seed=synth.BASE_SEED + 3 * N + d)
+    q = (q.float() * 2.0).to(q.dtype)      # wider scores, so the cap bends them
+    sk = synth.sinks(H, seed=N + 2) if sinks else None
+    a = synth.default_alpha(d)
+    g, ds = _gpu(gpu_lib, q, k, v, do, window, sk, a, softcap)
+    dq, dk, dv, dsr = oracle.attention_bwd_ext(q, k, v, do, a, window, softcap, sk,
+                                               n_threads=THREADS)
+    _check(g, (dq, dk, dv), ULP[dtype])
+    if sinks:
+        bound = _dsink_bound(q, k, v, do, a, window, sk, ULP[dtype], softcap)
+        assert np.all(np.abs(ds - dsr) <= bound + 1e-6), (ds, dsr, bound)
 
 
 @pytest.mark.parametrize("d", [64, 128])
