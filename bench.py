@@ -306,11 +306,15 @@ def run_bwd(args, B, H, N, d, rank, world):
     alpha = synth.default_alpha(d)
     causal = int(args.causal)
     qh, kh, vh = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + rank)
+    H_kv = args.hkv or H
+    if H_kv != H:               # grouped K/V heads (variant path only)
+        kh = torch.from_numpy(synth.normal((B, N, H_kv, d), seed=synth.BASE_SEED + rank + 1)).to(qh.dtype)
+        vh = torch.from_numpy(synth.normal((B, N, H_kv, d), seed=synth.BASE_SEED + rank + 2)).to(qh.dtype)
     doh = torch.from_numpy(synth.normal((B, N, H, d), seed=synth.BASE_SEED + rank + 3)).to(qh.dtype)
     q, k, v, do = qh.to(dev), kh.to(dev), vh.to(dev), doh.to(dev)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty((fa.bwd_workspace_floats(B, H, N),), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
@@ -324,7 +328,7 @@ def run_bwd(args, B, H, N, d, rank, world):
         if var is None:
             rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
         else:
-            rc = fa.fa_fwd_ext(q, k, v, o, lse, B, H, H, N, d, alpha, var["window"][0],
+            rc = fa.fa_fwd_ext(q, k, v, o, lse, B, H, H_kv, N, d, alpha, var["window"][0],
                                var["window"][1], var["softcap"], sinks_t, fa.FA_BF16, sp)
         if rc != fa.FA_OK:
             raise fa.FaError(rc, "fa_fwd")
@@ -334,7 +338,7 @@ def run_bwd(args, B, H, N, d, rank, world):
             rc = fa.fa_bwd(q, k, v, o, do, lse, ws, dq, dk, dv, B, H, N, d, alpha, causal,
                            fa.FA_BF16, sp)
         else:
-            rc = fa.fa_bwd_ext(q, k, v, o, do, lse, ws, dq, dk, dv, B, H, N, d, alpha,
+            rc = fa.fa_bwd_ext(q, k, v, o, do, lse, ws, dq, dk, dv, B, H, H_kv, N, d, alpha,
                                var["window"][0], var["window"][1], var["softcap"], sinks_t,
                                dsinks_t, fa.FA_BF16, sp)
         if rc != fa.FA_OK:
@@ -379,7 +383,7 @@ def run_bwd(args, B, H, N, d, rank, world):
         fwd()
     stream.synchronize()
     op, lp, dop = o.cpu().pin_memory(), lse.cpu().pin_memory(), doh.pin_memory()
-    outs = [torch.empty(qh.shape, dtype=qh.dtype).pin_memory() for _ in range(3)]
+    outs = [torch.empty(x.shape, dtype=qh.dtype).pin_memory() for x in (qh, kh, vh)]
     e2e_steps = max(3, min(args.steps, 30))
 
     def e2e_step():
@@ -403,8 +407,8 @@ def run_bwd(args, B, H, N, d, rank, world):
     barrier()
     e2e_ms = reduce_max(start.elapsed_time(stop), world, dev)
     e2e_value = aggregate_value(fl, e2e_steps, e2e_ms, world)
-    h2d = 5 * qh.numel() * qh.element_size() + lse.numel() * 4
-    d2h = 3 * qh.numel() * qh.element_size()
+    h2d = (3 * qh.numel() + kh.numel() + vh.numel()) * qh.element_size() + lse.numel() * 4
+    d2h = (qh.numel() + kh.numel() + vh.numel()) * qh.element_size()
 
     if rank != 0:
         return
@@ -416,6 +420,8 @@ def run_bwd(args, B, H, N, d, rank, world):
         peak, peak_kind = burst, "burst"
     wkey = (config_name(B, H, N, d, args.causal).replace("attention fwd", "attention bwd")
             + variant_suffix(var))
+    if H_kv != H:
+        wkey = wkey.replace(f" H{H} ", f" H{H} Hkv{H_kv} ")
     line = {
         "metric": METRIC_BWD, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -745,8 +751,10 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.bwd and args.fp8:
         ap.error("--bwd and --fp8 are exclusive")
-    if args.hkv and (args.bwd or args.fp8 or args.H % args.hkv):
-        ap.error("--hkv applies to the BF16 forward and must divide --H")
+    if args.hkv and (args.fp8 or args.H % args.hkv
+                     or (args.bwd and variant_of(args) is None)):
+        ap.error("--hkv must divide --H, not with --fp8; with --bwd it needs --window "
+                 "(e.g. --window -1 -1)")
     if args.splits is not None and (args.bwd or args.fp8 or args.hkv or args.d not in (64, 128)):
         ap.error("--splits applies to the BF16 forward, d 64 or 128, without --hkv")
     if variant_of(args) is not None and (args.fp8 or args.splits is not None

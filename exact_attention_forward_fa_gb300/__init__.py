@@ -71,7 +71,7 @@ def load():
     lib.fa_fwd_fp8.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_bwd.restype = i
-    lib.fa_bwd_ext.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i,
+    lib.fa_bwd_ext.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i,
                                f, vp, vp, i, vp]
     lib.fa_bwd_ext.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
@@ -266,15 +266,15 @@ def fa_bwd(q, k, v, o, dout, lse, workspace, dq, dk, dv, B: int, H: int, N: int,
                          int(d), float(alpha), int(causal), int(dtype), _stream(stream))
 
 
-def fa_bwd_ext(q, k, v, o, dout, lse, workspace, dq, dk, dv, B: int, H: int, N: int, d: int,
-               alpha: float, window_left: int, window_right: int, softcap: float, sinks,
+def fa_bwd_ext(q, k, v, o, dout, lse, workspace, dq, dk, dv, B: int, H: int, H_kv: int, N: int,
+               d: int, alpha: float, window_left: int, window_right: int, softcap: float, sinks,
                dsinks, dtype: int, stream=None) -> int:
     """Direct call of the C entry point: the backward of fa_fwd_ext with a
     local window and softcap; sinks/dsinks may be None (see include/fa.h)."""
     return load().fa_bwd_ext(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                              _ptr(workspace), _ptr(dq), _ptr(dk), _ptr(dv), int(B), int(H),
-                             int(N), int(d), float(alpha), int(window_left), int(window_right),
-                             float(softcap), _ptr(sinks), _ptr(dsinks), int(dtype),
+                             int(H_kv), int(N), int(d), float(alpha), int(window_left),
+                             int(window_right), float(softcap), _ptr(sinks), _ptr(dsinks), int(dtype),
                              _stream(stream))
 
 
@@ -292,10 +292,11 @@ def attention_backward_ext(q, k, v, o, lse, dout, window=(-1, -1), softcap: floa
     B, N, H, d = q.shape
     if alpha is None:
         alpha = 1.0 / math.sqrt(d)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(q), torch.empty_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty((bwd_workspace_floats(B, H, N),), dtype=torch.float32, device=q.device)
     ds = None if sinks is None else torch.empty((H,), dtype=torch.float32, device=q.device)
-    rc = fa_bwd_ext(q, k, v, o, dout, lse, ws, dq, dk, dv, B, H, N, d, alpha, int(window[0]),
+    rc = fa_bwd_ext(q, k, v, o, dout, lse, ws, dq, dk, dv, B, H, k.shape[2], N, d, alpha,
+                    int(window[0]),
                     int(window[1]), float(softcap), sinks, ds, dt, stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_ext")

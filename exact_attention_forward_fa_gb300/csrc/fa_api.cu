@@ -450,13 +450,14 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
 // gradient.
 static fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o,
                           const void *dout, const float *lse, float *workspace, void *dq,
-                          void *dk, void *dv, int B, int H, int N, int d, float alpha,
+                          void *dk, void *dv, int B, int H, int H_kv, int N, int d, float alpha,
                           int causal, bool win, int wl, int wr, float softcap,
                           const float *sinks, float *dsinks, fa_dtype dtype, void *stream) {
     // ---- host-side validation: nothing is launched on failure ----
     if (!q || !k || !v || !o || !dout || !lse || !workspace || !dq || !dk || !dv)
         return FA_ERR_INVALID_ARG;
     if (win && (wl < -1 || wr < -1)) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(softcap) || softcap < 0.f) return FA_ERR_INVALID_ARG;
     const double cap_pre = softcap > 0.f ? static_cast<double>(alpha) / softcap : 0.0;
     if (!std::isfinite(static_cast<float>(cap_pre))) return FA_ERR_INVALID_ARG;
@@ -489,8 +490,8 @@ static fa_status bwd_impl(const void *q, const void *k, const void *v, const voi
     const CUtensorMapDataType dt =
         dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if ((st = encode_bshd(&L.q, q, dt, B, H, N, d, 128)) != FA_OK) return st;
-    if ((st = encode_bshd(&L.k, k, dt, B, H, N, d, 128)) != FA_OK) return st;
-    if ((st = encode_bshd(&L.v, v, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.k, k, dt, B, H_kv, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.v, v, dt, B, H_kv, N, d, 128)) != FA_OK) return st;
     if ((st = encode_bshd(&L.dout, dout, dt, B, H, N, d, 128)) != FA_OK) return st;
     L.args.lse = lse;
     L.args.ws_d = workspace;
@@ -507,6 +508,11 @@ static fa_status bwd_impl(const void *q, const void *k, const void *v, const voi
     L.args.N = N;
     L.args.n_t = static_cast<int>(n_t);
     L.args.n_units = static_cast<int>(units);
+    const uint64_t units_kv = static_cast<uint64_t>(B) * H_kv * n_t;
+    L.args.n_units_kv = static_cast<int>(units_kv);
+    L.args.group = H / H_kv;
+    L.grid_kv = static_cast<int>(units_kv < static_cast<uint64_t>(dev->sm_count) ? units_kv
+                                                                                 : dev->sm_count);
     L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
     L.args.alpha = alpha;
     L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
@@ -533,16 +539,16 @@ static fa_status bwd_impl(const void *q, const void *k, const void *v, const voi
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const void *dout,
                  const float *lse, float *workspace, void *dq, void *dk, void *dv, int B, int H,
                  int N, int d, float alpha, int causal, fa_dtype dtype, void *stream) {
-    return bwd_impl(q, k, v, o, dout, lse, workspace, dq, dk, dv, B, H, N, d, alpha, causal,
+    return bwd_impl(q, k, v, o, dout, lse, workspace, dq, dk, dv, B, H, H, N, d, alpha, causal,
                     false, -1, -1, 0.f, nullptr, nullptr, dtype, stream);
 }
 
 fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
                      const void *dout, const float *lse, float *workspace, void *dq, void *dk,
-                     void *dv, int B, int H, int N, int d, float alpha, int window_left,
-                     int window_right, float softcap, const float *sinks, float *dsinks,
-                     fa_dtype dtype, void *stream) {
-    return bwd_impl(q, k, v, o, dout, lse, workspace, dq, dk, dv, B, H, N, d, alpha, 0, true,
+                     void *dv, int B, int H, int H_kv, int N, int d, float alpha,
+                     int window_left, int window_right, float softcap, const float *sinks,
+                     float *dsinks, fa_dtype dtype, void *stream) {
+    return bwd_impl(q, k, v, o, dout, lse, workspace, dq, dk, dv, B, H, H_kv, N, d, alpha, 0, true,
                     window_left, window_right, softcap, sinks, dsinks, dtype, stream);
 }
 

@@ -56,7 +56,9 @@ struct BwdArgs {
     int B, H, N;
     int n_t;               // 128-row tiles per sequence
     int NP;                // n_t * 128: padded row count of the workspace
-    int n_units;           // B * H * n_t
+    int n_units;           // B * H * n_t (dQ kernel: query tiles)
+    int n_units_kv;        // B * (H / group) * n_t (dK/dV kernel: key tiles)
+    int group;             // query heads per K/V head (>= 1); K/V are [B][N][H/group][d]
     float scale_log2;      // alpha * log2(e)
     float alpha;
     // Local window (kWin instantiations): key j is hidden from query i when
@@ -168,7 +170,8 @@ struct BwdUnit {
 template <bool kCausal, bool kKeyTiles, bool kWin = false>
 __device__ __forceinline__ BwdUnit make_bwd_unit(int u, const BwdArgs &a) {
     BwdUnit U;
-    const int BH = a.B * a.H;
+    const int HH = kKeyTiles ? a.H / a.group : a.H;     // K/V heads for key tiles
+    const int BH = a.B * HH;
     int bh;
     const bool lpt = kWin ? (a.wl < 0 && a.wr >= 0) : kCausal;
     if (lpt) {
@@ -179,8 +182,8 @@ __device__ __forceinline__ BwdUnit make_bwd_unit(int u, const BwdArgs &a) {
         U.m = u % a.n_t;
         bh = u / a.n_t;
     }
-    U.b = bh / a.H;
-    U.h = bh % a.H;
+    U.b = bh / HH;
+    U.h = bh % HH;
     return U;
 }
 
@@ -309,11 +312,12 @@ __device__ __forceinline__ void gemm_ts_mn(uint32_t d_tmem, uint32_t a_tmem, uin
 
 // Epilogue store: columns [col0, col0 + W) of one row, v * scale -> 16 bit.
 template <int D, int W, bool kBF16>
-__device__ __forceinline__ void store_cols(void *dst_base, const BwdArgs &a, int b, int h,
-                                           int row, int col0, const uint32_t (&v)[W], float scale) {
+__device__ __forceinline__ void store_cols(void *dst_base, const BwdArgs &a, int heads, int b,
+                                           int h, int row, int col0, const uint32_t (&v)[W],
+                                           float scale) {
     if (row >= a.N) return;
     uint16_t *dst = reinterpret_cast<uint16_t *>(dst_base) +
-                    ((static_cast<size_t>(b) * a.N + row) * a.H + h) * D + col0;
+                    ((static_cast<size_t>(b) * a.N + row) * heads + h) * D + col0;
 #pragma unroll
     for (int ch = 0; ch < W / 8; ++ch) {
         uint32_t pk[4];
@@ -421,13 +425,13 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(C::DQB_KFULL + ks), C::TILE);
                     load_tile<C::NCH>(&tm_k, base + C::DQ_K_OFF + ks * C::TILE, bar(C::DQB_KFULL + ks),
-                                      U.h, j * 128, U.b);
+                                      U.h / a.group, j * 128, U.b);
                     ++nk;
                     ok = mbar_wait(bar(C::DQB_VEMPTY + vs), RV::phase(nv) ^ 1, w, 52);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(C::DQB_VFULL + vs), C::TILE);
                     load_tile<C::NCH>(&tm_v, base + C::DQ_V_OFF + vs * C::TILE, bar(C::DQB_VFULL + vs),
-                                      U.h, j * 128, U.b);
+                                      U.h / a.group, j * 128, U.b);
                     ++nv;
                 }
             }
@@ -628,7 +632,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::DQB_DQEMPTY));
-            store_cols<D, W, kBF16>(a.dq, a, U.b, U.h, grow, half * W, dq, a.alpha);
+            store_cols<D, W, kBF16>(a.dq, a, a.H, U.b, U.h, grow, half * W, dq, a.alpha);
         }
     }
 
@@ -728,7 +732,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             uint32_t nq = 0, n_qc = 0, n_dc = 0;     // tiles; Q and dO copies issued
             int kvn = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            for (int u = blockIdx.x; ok && u < a.n_units_kv; u += gridDim.x) {
                 const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
                 ok = mbar_wait(bar(C::KVB_KVEMPTY), (kvn & 1) ^ 1, w, 80);
                 if (!ok) break;
@@ -736,10 +740,13 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 load_tile<C::NCH>(&tm_k, base + C::KV_K_OFF, bar(C::KVB_KVFULL), U.h, U.m * 128, U.b);
                 load_tile<C::NCH>(&tm_v, base + C::KV_V_OFF, bar(C::KVB_KVFULL), U.h, U.m * 128, U.b);
                 ++kvn;
-                const size_t wrow = (static_cast<size_t>(U.b) * a.H + U.h) * a.NP;
                 int qlo_t, qhi_t;
                 query_range(U, qlo_t, qhi_t);
-                for (int i = qlo_t; ok && i < qhi_t; ++i, ++nq) {
+                // the query heads of this K/V head, each over its query tiles
+                for (int k = 0; ok && k < a.group * (qhi_t - qlo_t); ++k, ++nq) {
+                    const int hq = U.h * a.group + k / (qhi_t - qlo_t);
+                    const int i = qlo_t + k % (qhi_t - qlo_t);
+                    const size_t wrow = (static_cast<size_t>(U.b) * a.H + hq) * a.NP;
                     // the elementwise warps read LSE2 and D of these 128
                     // columns: 2 x 512 B, four 128-byte lines each
 #pragma unroll
@@ -750,12 +757,12 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     ok = mbar_wait(bar(C::KVB_QEMPTY + RQ::slot(nq)), RQ::phase(nq) ^ 1, w, 81);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(C::KVB_QFULL + RQ::slot(nq)), C::TILE);
-                    load_tile<C::NCH>(&tm_q, q_tile(nq), bar(C::KVB_QFULL + RQ::slot(nq)), U.h, i * 128, U.b);
+                    load_tile<C::NCH>(&tm_q, q_tile(nq), bar(C::KVB_QFULL + RQ::slot(nq)), hq, i * 128, U.b);
                     ++n_qc;
                     ok = mbar_wait(bar(C::KVB_DOEMPTY + RO::slot(nq)), RO::phase(nq) ^ 1, w, 82);
                     if (!ok) break;
                     mbar_arrive_expect_tx(bar(C::KVB_DOFULL + RO::slot(nq)), C::TILE);
-                    load_tile<C::NCH>(&tm_do, do_tile(nq), bar(C::KVB_DOFULL + RO::slot(nq)), U.h, i * 128, U.b);
+                    load_tile<C::NCH>(&tm_do, do_tile(nq), bar(C::KVB_DOFULL + RO::slot(nq)), hq, i * 128, U.b);
                     ++n_dc;
                 }
             }
@@ -775,11 +782,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         auto wait_do = [&](uint32_t i) {
             return mbar_wait_warp(bar(C::KVB_DOFULL + RO::slot(i)), RO::phase(i), w, 96);
         };
-        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+        for (int u = blockIdx.x; ok && u < a.n_units_kv; u += gridDim.x) {
             const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
             int qlo_t, qhi_t;
             query_range(U, qlo_t, qhi_t);
-            const int Ti = qhi_t - qlo_t;
+            const int Ti = a.group * (qhi_t - qlo_t);    // query tiles of all the group's heads
             ok = mbar_wait_warp(bar(C::KVB_KVFULL), kvph, w, 90);
             if (!ok) break;
             kvph ^= 1;
@@ -857,7 +864,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const float2 c2 = make_float2(sl2, sl2);
         uint32_t stn = 0, dpph = 0, accph = 0;    // stn: S^T tiles of this CTA so far
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+        for (int u = blockIdx.x; ok && u < a.n_units_kv; u += gridDim.x) {
             const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
             int i0, qhi_t;
             query_range(U, i0, qhi_t);
@@ -870,9 +877,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 qlo_r = win_qlo(kr, a);
                 qhi_r = win_qhi(kr, a);
             }
-            const size_t wrow = (static_cast<size_t>(U.b) * a.H + U.h) * a.NP;
-            for (int k = 0; k < Ti; ++k) {
-                const int i = i0 + k;
+            for (int k = 0; k < a.group * Ti; ++k) {
+                // query head of the group, then its query tile
+                const int hq = U.h * a.group + k / Ti;
+                const int i = i0 + k % Ti;
+                const size_t wrow = (static_cast<size_t>(U.b) * a.H + hq) * a.NP;
                 const float4 *lse4 = reinterpret_cast<const float4 *>(a.ws_l + wrow + i * 128 + col0);
                 const float4 *dd4 = reinterpret_cast<const float4 *>(a.ws_d + wrow + i * 128 + col0);
                 // ---- P^T = exp2(S^T c - LSE2[q]) ----
@@ -982,7 +991,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tmem_ld32(tbase + lane_off + C::KV_COL_DV + half * W + ch * 32,
                           *reinterpret_cast<uint32_t(*)[32]>(&acc[ch * 32]));
             tmem_ld_wait();
-            store_cols<D, W, kBF16>(a.dv, a, U.b, U.h, krow, half * W, acc, 1.f);
+            store_cols<D, W, kBF16>(a.dv, a, a.H / a.group, U.b, U.h, krow, half * W, acc, 1.f);
 #pragma unroll
             for (int ch = 0; ch < W / 32; ++ch)
                 tmem_ld32(tbase + lane_off + C::KV_COL_DK + half * W + ch * 32,
@@ -991,7 +1000,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::KVB_ACCEMPTY));
-            store_cols<D, W, kBF16>(a.dk, a, U.b, U.h, krow, half * W, acc, a.alpha);
+            store_cols<D, W, kBF16>(a.dk, a, a.H / a.group, U.b, U.h, krow, half * W, acc, a.alpha);
         }
     }
 

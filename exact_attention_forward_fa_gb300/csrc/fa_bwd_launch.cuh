@@ -40,7 +40,7 @@ cudaError_t launch_bwd_inst(const BwdLaunch &L) {
     if (e != cudaSuccess) return e;
     fa_bwd_delta_kernel<D, kBF16><<<L.grid_delta, 256, 0, L.stream>>>(L.args);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kkv<<<L.grid, C::NTHREADS, C::KV_SMEM, L.stream>>>(L.q, L.k, L.v, L.dout, L.args);
+    kkv<<<L.grid_kv, C::NTHREADS, C::KV_SMEM, L.stream>>>(L.q, L.k, L.v, L.dout, L.args);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     kdq<<<L.grid, C::NTHREADS, C::DQ_SMEM, L.stream>>>(L.q, L.k, L.v, L.dout, L.args);
     return cudaGetLastError();

@@ -44,7 +44,8 @@ cudaError_t launch_combine(const CombineArgs &a, int grid, cudaStream_t stream);
 struct BwdLaunch {
     CUtensorMap q, k, v, dout;
     BwdArgs args;
-    int grid;
+    int grid;              // dQ kernel
+    int grid_kv;           // dK/dV kernel (units over K/V heads)
     int grid_delta;
     int d;
     bool causal;

@@ -235,11 +235,16 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
  *            of sigma_h, -sum over batches and rows of e^(sigma_h - LSE) D
  *            (D = rowsum(dO o O)), reduced in a fixed order.  dsinks
  *            without sinks returns FA_ERR_INVALID_ARG.
- * Other arguments, results and errors as fa_bwd (H_kv = H, d in {64, 128}).
+ *   H_kv   : K/V heads (grouped-query attention, as for fa_fwd_ext): k, v,
+ *            dk, dv are [B][N][H_kv][d], query head h uses K/V head
+ *            h / (H / H_kv), and dK, dV of a K/V head sum the contributions
+ *            of all its query heads (accumulated in FP32 in one kernel, no
+ *            atomics).  H % H_kv != 0 or H_kv < 1 returns FA_ERR_INVALID_ARG.
+ * Other arguments, results and errors as fa_bwd (d in {64, 128}).
  */
 fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
                      const void *dout, const float *lse, float *workspace,
-                     void *dq, void *dk, void *dv, int B, int H, int N, int d,
+                     void *dq, void *dk, void *dv, int B, int H, int H_kv, int N, int d,
                      float alpha, int window_left, int window_right,
                      float softcap, const float *sinks, float *dsinks,
                      fa_dtype dtype, void *stream);

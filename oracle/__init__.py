@@ -268,11 +268,21 @@ def attention_bwd_ext_head(q, k, v, dout, alpha: float, window=(-1, -1),
 def attention_bwd_ext(q, k, v, dout, alpha: float, window=(-1, -1), softcap: float = 0.0,
                       sinks=None, n_threads: int = 1):
     """The variants' gradients on [B,N,H,d] tensors: (dQ, dK, dV, dsinks [H]),
-    dsinks summed over the batch (zeros without sinks).  Heads are independent
-    and run on a thread pool."""
+    dsinks summed over the batch (zeros without sinks).  k, v may have H_kv
+    heads dividing H: query head h uses K/V head h // (H / H_kv), and dK, dV
+    of a K/V head are the sums over its query heads (a shared input's
+    gradient is the sum of its uses).  Heads are independent and run on a
+    thread pool."""
     from concurrent.futures import ThreadPoolExecutor
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, N, H, d = q.shape
+    H_kv = k.shape[2]
+    if H_kv < 1 or H % H_kv:
+        raise ValueError("H_kv must divide H")
+    g = H // H_kv
+    if g > 1:
+        k = np.ascontiguousarray(np.repeat(k, g, axis=2))
+        v = np.ascontiguousarray(np.repeat(v, g, axis=2))
     dq, dk, dv = np.zeros_like(q), np.zeros_like(q), np.zeros_like(q)
     sk = None if sinks is None else _f64(sinks).reshape(H)
     dsink = np.zeros((B, H))
@@ -286,6 +296,9 @@ def attention_bwd_ext(q, k, v, dout, alpha: float, window=(-1, -1), softcap: flo
 
     with ThreadPoolExecutor(max_workers=max(1, int(n_threads))) as ex:
         list(ex.map(one, [(b, h) for b in range(B) for h in range(H)]))
+    if g > 1:
+        dk = dk.reshape(B, N, H_kv, g, d).sum(axis=3)
+        dv = dv.reshape(B, N, H_kv, g, d).sum(axis=3)
     return dq, dk, dv, dsink.sum(axis=0)
 
 

@@ -207,10 +207,10 @@ def test_bwd_validation_codes(lib, kw, code):
     assert _bcall(lib, **kw) == code
 
 
-def _bxcall(lib, q=A, o=A, lse=A, ws=A, dq=A, B=1, H=1, N=128, d=128, wl=64, wr=0,
+def _bxcall(lib, q=A, o=A, lse=A, ws=A, dq=A, B=1, H=2, H_kv=1, N=128, d=128, wl=64, wr=0,
             softcap=0.0, alpha=0.088, sinks=None, dsinks=None, dtype=0):
-    return lib.fa_bwd_ext(q, A, A, o, A, lse, ws, dq, A, A, B, H, N, d, alpha, wl, wr, softcap,
-                          sinks, dsinks, dtype, None)
+    return lib.fa_bwd_ext(q, A, A, o, A, lse, ws, dq, A, A, B, H, H_kv, N, d, alpha, wl, wr,
+                          softcap, sinks, dsinks, dtype, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -220,6 +220,8 @@ def _bxcall(lib, q=A, o=A, lse=A, ws=A, dq=A, B=1, H=1, N=128, d=128, wl=64, wr=
     (dict(wr=-3), fa.FA_ERR_INVALID_ARG),
     (dict(dsinks=A), fa.FA_ERR_INVALID_ARG),            # a sink gradient needs the sinks
     (dict(softcap=-2.0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=3, H_kv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(H_kv=0), fa.FA_ERR_INVALID_ARG),
     (dict(softcap=float("inf")), fa.FA_ERR_INVALID_ARG),
     (dict(softcap=1e-38, alpha=1e3), fa.FA_ERR_INVALID_ARG),
     (dict(dtype=5), fa.FA_ERR_INVALID_ARG),

@@ -170,3 +170,33 @@ def test_bwd_ext_b4_h16_n4096_d128_window_two_heads(gpu_lib):
         ref = oracle.attention_bwd_ext_head(q[b, :, h], k[b, :, h], v[b, :, h], do[b, :, h], a,
                                             window, 0.0, None)
         _check([x[b, :, h] for x in g], ref[:3], ULP["bf16"])
+
+
+GQA_CASES = [
+    # (B, H, H_kv, N, d, window, softcap, sinks)
+    (2, 8, 2, 1000, 128, (-1, -1), 0.0, False),
+    (1, 8, 1, 777, 64, (256, 0), 0.0, False),          # multi-query
+    (1, 4, 2, 513, 128, (-1, 0), 30.0, True),
+    (1, 6, 3, 300, 64, (64, 64), 0.0, True),
+]
+
+
+@pytest.mark.parametrize("B,H,H_kv,N,d,window,softcap,sinks", GQA_CASES)
+def test_bwd_ext_grouped_heads(gpu_lib, B, H, H_kv, N, d, window, softcap, sinks):
+    # dK, dV of a K/V head sum the gradients of its H / H_kv query heads.
+    t = torch.bfloat16
+    seed = synth.BASE_SEED + 11 * N + H_kv
+    q = torch.from_numpy(synth.normal((B, N, H, d), seed=seed)).to(t)
+    k = torch.from_numpy(synth.normal((B, N, H_kv, d), seed=seed + 1)).to(t)
+    v = torch.from_numpy(synth.normal((B, N, H_kv, d), seed=seed + 2)).to(t)
+    do = torch.from_numpy(synth.normal((B, N, H, d), seed=seed + 3)).to(t)
+    sk = synth.sinks(H, seed=N + 3) if sinks else None
+    a = synth.default_alpha(d)
+    g, ds = _gpu(gpu_lib, q, k, v, do, window, sk, a, softcap)
+    assert g[1].shape == (B, N, H_kv, d) and g[2].shape == (B, N, H_kv, d)
+    dq, dk, dv, dsr = oracle.attention_bwd_ext(q, k, v, do, a, window, softcap, sk,
+                                               n_threads=THREADS)
+    _check(g, (dq, dk, dv), ULP["bf16"])
+    if sinks:
+        bound = _dsink_bound(q, k, v, do, a, window, sk, ULP["bf16"], softcap)
+        assert np.all(np.abs(ds - dsr) <= bound + 1e-6), (ds, dsr, bound)

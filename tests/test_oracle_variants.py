@@ -310,3 +310,31 @@ def test_bwd_ext_planted_mistakes_are_caught():
     assert not _grads_agree(oracle.attention_bwd_ext_head(q, k, v, dout, a, (3, 1), c, sink), fd)
     assert not _grads_agree(oracle.attention_bwd_ext_head(q, k, v, dout, a, win, c, None), fd)
     assert not _grads_agree(oracle.attention_bwd_ext_head(q, k, v, dout, a, win, c, -0.5), fd)
+
+
+def test_bwd_ext_grouped_heads_match_finite_differences():
+    # Grouped K/V heads: the gradient of a shared K/V head is the sum over
+    # its query heads; checked by differentiating the grouped forward.
+    B, N, H, H_kv, d = 1, 4, 4, 2, 2
+    q, dout = _rand(B, N, H, d), _rand(B, N, H, d)
+    k, v = _rand(B, N, H_kv, d), _rand(B, N, H_kv, d)
+    a, win, c = 0.7, (2, 0), 1.5
+
+    def loss(kk, vv):
+        o, _ = oracle.attention_ext(q, kk, vv, a, window=win, softcap=c)
+        return float(np.sum(o * dout))
+
+    _, dk, dv, _ = oracle.attention_bwd_ext(q, k, v, dout, a, win, c, None)
+    assert dk.shape == k.shape and dv.shape == v.shape
+    eps = 1e-5
+    for x, g in ((k, dk), (v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            x0 = x[idx]
+            x[idx] = x0 + eps
+            lp = loss(k, v)
+            x[idx] = x0 - eps
+            lm = loss(k, v)
+            x[idx] = x0
+            fd[idx] = (lp - lm) / (2 * eps)
+        assert np.allclose(g, fd, rtol=1e-7, atol=1e-7)
