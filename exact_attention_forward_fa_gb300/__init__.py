@@ -31,7 +31,8 @@ FA_FP16 = 1
 # Every symbol include/fa.h declares (checked by the tests).
 EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_ext", "fa_fwd_splitkv", "fa_splitkv_workspace_floats",
            "fa_splitkv_auto", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_ext", "fa_bwd_noalloc",
-           "fa_check_status", "fa_status_detail", "fa_status_string", "fa_version")
+           "fa_check_status", "fa_status_detail", "fa_selftest_wait_timeout",
+           "fa_status_string", "fa_version")
 
 _lib = None
 
@@ -76,6 +77,8 @@ def load():
     lib.fa_bwd_ext.restype = i
     lib.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_bwd_noalloc.restype = i
+    lib.fa_selftest_wait_timeout.argtypes = [vp, vp]
+    lib.fa_selftest_wait_timeout.restype = i
     lib.fa_check_status.argtypes = [vp]
     lib.fa_check_status.restype = i
     lib.fa_status_detail.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -335,6 +338,12 @@ def attention_backward(q, k, v, o, lse, dout, causal: bool = False,
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
     return dq, dk, dv
+
+
+def fa_selftest_wait_timeout(result, stream=None) -> int:
+    """Direct call of the C entry point: a kernel whose bounded waits run
+    out (no fault); result is a device uint32 tensor of 2 elements."""
+    return load().fa_selftest_wait_timeout(_ptr(result), _stream(stream))
 
 
 def fa_check_status(stream=None) -> int:

@@ -615,6 +615,17 @@ fa_status fa_check_status(void *stream) {
     return FA_ERR_TIMEOUT;
 }
 
+fa_status fa_selftest_wait_timeout(uint32_t *result, void *stream) {
+    if (!result) return FA_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(result) & 3u) return FA_ERR_MISALIGNED;
+    DeviceInfo *dev = nullptr;
+    fa_status st = get_device(&dev);
+    if (st != FA_OK) return st;
+    cudaError_t e = fa::launch_selftest_timeout(dev->status, result,
+                                                static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 void fa_status_detail(uint32_t out[4]) {
     std::lock_guard<std::mutex> lk(g_mu);
     std::memcpy(out, g_last_detail, sizeof(g_last_detail));

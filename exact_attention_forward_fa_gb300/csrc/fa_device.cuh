@@ -21,7 +21,7 @@ enum : uint32_t {
 // Roles that may report a timeout (stored in status[1] for diagnosis).
 enum : uint32_t {
     kRoleSoftmax0 = 1, kRoleSoftmax1 = 2, kRoleProducer = 3, kRoleMma = 4,
-    kRoleDrain = 5, kRoleQuant = 6,
+    kRoleDrain = 5, kRoleQuant = 6, kRoleSelftest = 7,
 };
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.

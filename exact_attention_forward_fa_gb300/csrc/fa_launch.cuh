@@ -55,6 +55,8 @@ struct BwdLaunch {
 cudaError_t launch_bwd(const BwdLaunch &L);
 // The same for a local window (L.args.wl, L.args.wr; L.causal unused).
 cudaError_t launch_bwd_win(const BwdLaunch &L);
+// Failure-path self-test: bounded waits that run out (fa_selftest.cu).
+cudaError_t launch_selftest_timeout(uint32_t *status, uint32_t *result, cudaStream_t stream);
 // The same with a softcap (L.args.sc_pre, L.args.sc_post).
 cudaError_t launch_bwd_win_softcap(const BwdLaunch &L);
 // Gradient of per-head sink logits: dsinks[h] = -sum_{b,i} 2^(sigma_h log2 e

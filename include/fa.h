@@ -280,11 +280,27 @@ fa_status fa_check_status(void *stream);
 /*
  * fa_status_detail -- the status word captured by the last fa_check_status
  * that returned FA_ERR_TIMEOUT: out[0] code, out[1] role that gave up
- * (1/2 softmax group L/H, 3 producer, 4 MMA issuer, 6 FP8 pre-pass),
+ * (1/2 softmax group L/H, 3 producer, 4 MMA issuer, 6 FP8 pre-pass,
+ * 7 self-test),
  * out[2] wait site,
  * out[3] block index.  Zeros if no timeout was ever reported.
  */
 void fa_status_detail(uint32_t out[4]);
+
+/*
+ * fa_selftest_wait_timeout -- exercises the failure path without a fault:
+ * one CTA whose two warps wait (with the pipeline kernels' bounded wait) on
+ * valid mbarriers that nobody arrives on.  The first wait gives up after
+ * its time limit (2 s), records role 7 and its site (1 or 2) in the status
+ * word and raises the CTA's abort flag; the other then returns promptly.
+ *   result : device, uint32_t[2], 4-byte aligned (written): result[w] = 1
+ *            when warp w's wait returned false.
+ * The next fa_check_status then returns FA_ERR_TIMEOUT and
+ * fa_status_detail gives {1, 7, site, 0}; the CUDA context stays usable.
+ * Returns FA_ERR_INVALID_ARG for a null result, FA_ERR_MISALIGNED,
+ * FA_ERR_UNSUPPORTED / FA_ERR_CUDA as fa_fwd.
+ */
+fa_status fa_selftest_wait_timeout(uint32_t *result, void *stream);
 
 /* fa_status_string -- a static, human-readable name for a status code. */
 const char *fa_status_string(fa_status s);

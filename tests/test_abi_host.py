@@ -266,3 +266,8 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(mod, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         mod.load()
+
+
+def test_selftest_validation_codes(lib):
+    assert lib.fa_selftest_wait_timeout(None, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_selftest_wait_timeout(A + 2, None) == fa.FA_ERR_MISALIGNED
