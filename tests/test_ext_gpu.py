@@ -147,3 +147,19 @@ def test_sampled_b4_h16_n4096_d128_sliding_softcap_sinks(gpu_lib):
                           rng.integers(0, N, size=16).tolist()))
         o_ref, l_ref = oracle.attention_ext_rows(q, k, v, a, b, h, rows, window, softcap, sk)
         _check(o[b, rows, h, :], lse[b, h, rows], o_ref, l_ref)
+
+
+def test_sampled_long_sequence_window_and_sinks(gpu_lib):
+    # N = 2^16 + 1 with a sliding window: far-apart rows see disjoint keys.
+    B, H, N, d = 1, 2, 65537, 128
+    window = (4096, 0)
+    q, k, v = synth.qkv(B, H, N, d, seed=synth.BASE_SEED + 123)
+    sk = synth.sinks(H, seed=123)
+    a = synth.default_alpha(d)
+    o, lse = _run(gpu_lib, q, k, v, window, 0.0, sk, a)
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    rows = [0, 4095, 4096, 4097, 32768, 65535, 65536]
+    for h in range(H):
+        o_ref, l_ref = oracle.attention_ext_rows(q, k, v, a, 0, h, rows, window, 0.0, sk)
+        _check(o[0, rows, h, :], lse[0, h, rows], o_ref, l_ref)

@@ -269,3 +269,16 @@ def test_splitkv_one_split_equals_fa_fwd(gpu_lib):
         o1, l1 = gpu_lib.attention(q, k, v, causal=causal)
         o2, l2 = gpu_lib.attention_splitkv(q, k, v, causal=causal, n_splits=1)
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("N,d,causal", [(65537, 128, False), (65537, 64, True), (131072, 128, True)])
+def test_sampled_long_sequences(gpu_lib, N, d, causal):
+    # Long sequences: 64-bit row offsets, a ragged last tile (N = 2^16 + 1),
+    # 512-1024 key tiles per unit; rows sampled across the whole range.
+    _sampled(gpu_lib, 1, 2, N, d, causal, n_heads=2, n_rows=12)
+
+
+def test_sampled_many_units(gpu_lib):
+    # B32 H64 N640: 2048 heads, 6144 work units -- many waves of the
+    # persistent grid; heads sampled at both ends and in between.
+    _sampled(gpu_lib, 32, 64, 640, 64, True, n_heads=4, n_rows=8)
