@@ -475,8 +475,21 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             // exponentials (for LSE); lr: row sum of the same values rounded
             // as the P V product sees them (normalises O; 16-bit P only).
             float r = -INFINITY, le = 0.f, lr = 0.f;
+            // FP8: the K and V tile scales of the next key tile are loaded
+            // while this one waits and computes (a load at the top of each
+            // tile sat on the softmax's critical path)
+            float ks_n = 0.f, vs_n = 0.f;
+            if (kFP8 && t0 < t1) {
+                ks_n = a.k_scale[sbase + (U.jhi - 1 - t0)];
+                vs_n = a.v_scale[sbase + (U.jhi - 1 - t0)];
+            }
             for (int t = t0; t < t1; ++t) {
                 const int j = U.jhi - 1 - t;
+                const float ks_c = ks_n, vs_c = vs_n;
+                if (kFP8 && t + 1 < t1) {
+                    ks_n = a.k_scale[sbase + j - 1];
+                    vs_n = a.v_scale[sbase + j - 1];
+                }
                 ok = mbar_wait(bar(C::B_SFULL + x), sph, w, 20);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 sph ^= 1;
@@ -540,8 +553,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     // Score scale to log2 units with the q and k tile scales
                     // ("FlashAttention-3 on Hopper", sec. 6.3); the exponent
                     // offset 8 + log2(v_j / v_max) carries the V tile scale.
-                    const float sc = sl2 * qs * a.k_scale[sbase + j];
-                    vr = a.v_scale[sbase + j] / vmax;
+                    const float sc = sl2 * qs * ks_c;
+                    vr = vs_c / vmax;
                     const float voff = C::P_OFFSET + log2f(vr);
                     // e4m3 saturates above 448, so the row max comes first.
                     const float bnew = row_max() * sc;             // -inf stays -inf
