@@ -155,7 +155,9 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
                 return true;
             };
-            for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
+            const int u = unit_of_round(k, kCausal);   // longest-first: back and forth
+            if (u >= a.n_units) continue;
                 const Unit1q U = make_unit_1q<kCausal, C::BN>(u, a);
                 ok = mbar_wait(bar(C::B_QSEMPTY), (qn & 1) ^ 1, w, 1);
                 if (!ok) break;
@@ -191,7 +193,9 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             p_out = phase;
             if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
         };
-        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
+            const int u = unit_of_round(k, kCausal);   // longest-first: back and forth
+            if (u >= a.n_units) continue;
             const Unit1q U = make_unit_1q<kCausal, C::BN>(u, a);
             ok = mbar_wait_warp(bar(C::B_QTFULL), qtph, w, 30);
             if (!ok) break;
@@ -294,7 +298,9 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             return true;
         };
 
-        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
+            const int u = unit_of_round(k, kCausal);   // longest-first: back and forth
+            if (u >= a.n_units) continue;
             const Unit1q U = make_unit_1q<kCausal, C::BN>(u, a);
             // ---- copy Q (staged by TMA, 128-B swizzle) into TMEM; the last
             //      QK of the previous unit completed before its S_FULL ----

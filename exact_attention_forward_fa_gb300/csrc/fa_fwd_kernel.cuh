@@ -158,6 +158,22 @@ __device__ __forceinline__ int window_hi(int i, const FwdArgs &a) {
     return a.wr >= 0 ? i + 1 + min(a.wr, a.N - 1 - i) : a.N;
 }
 
+// Units whose length falls with their index (longest-first orders).
+template <bool kCausal, bool kExt>
+__device__ __forceinline__ bool units_longest_first(const FwdArgs &a) {
+    return kExt ? (a.wl < 0 && a.wr >= 0) : kCausal;
+}
+
+// The unit CTA blockIdx.x runs in its k-th round.  Longest-first orders go
+// back and forth over the CTAs (odd rounds in reverse), so a CTA that takes
+// one of the longest units of a round takes one of the shortest of the
+// next; striding in one direction gave CTA 0 the longest unit of every
+// round.  Every role of a CTA walks the same sequence.
+__device__ __forceinline__ int unit_of_round(int k, bool snake) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return k * G + ((snake && (k & 1)) ? G - 1 - c : c);
+}
+
 // kSplit: the key range is cut into a.n_splits parts (otherwise one part,
 // folded away at compile time).  kExt: the key range of each Q tile comes
 // from the window ("FlashAttention-3 on Hopper", sec. 4.7: local attention
@@ -172,7 +188,7 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     if (kSplit) u /= S;
     int p, bh;
     // a right bound without a left one makes later pairs longer
-    const bool lpt = kExt ? (a.wl < 0 && a.wr >= 0) : kCausal;
+    const bool lpt = units_longest_first<kCausal, kExt>(a);
     if (lpt) {              // longest-first: the last pairs of every head first
         p = a.n_pairs - 1 - u / BH;
         bh = u % BH;
@@ -245,6 +261,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const bool snake = units_longest_first<kCausal, kExt>(a);   // unit order (unit_of_round)
 
     auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
@@ -308,7 +325,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 ++qc;
                 return true;
             };
-            for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
+                const int u = unit_of_round(k, snake);
+                if (u >= a.n_units) continue;
                 const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
                 if (U.act[0]) ok = ok && load_q(0, U);
                 if (U.act[1]) ok = ok && load_q(1, U);
@@ -347,7 +366,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint32_t pph0 = 0, pph1 = 0;
             uint32_t slot = 0, phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
+                const int u = unit_of_round(k, snake);
+                if (u >= a.n_units) continue;
                 const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
                 uint32_t qs0 = 0, qp0 = 0, qs1 = 0, qp1 = 0;   // Q slot and parity per tile
                 if (U.act[0]) { qs0 = qc % C::NQ; qp0 = (qc / C::NQ) & 1u; ++qc; }
@@ -445,7 +466,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         const float sl2 = kCap ? a.sc_post : a.scale_log2;
         uint32_t sph = 0, oph = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
+                const int u = unit_of_round(k, snake);
+                if (u >= a.n_units) continue;
             const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
             const bool act = x ? U.act[1] : U.act[0];
             if (!act) continue;
