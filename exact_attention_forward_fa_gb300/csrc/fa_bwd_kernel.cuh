@@ -131,7 +131,8 @@ struct BwdCfg {
                          KVB_PFULL = 4, KVB_DSFULL = 5, KVB_ACCFULL = 6, KVB_ACCEMPTY = 7,
                          KVB_MMADONE = 8, KVB_QFULL = 9, KVB_QEMPTY = KVB_QFULL + QN,
                          KVB_DOFULL = KVB_QEMPTY + QN, KVB_DOEMPTY = KVB_DOFULL + DN,
-                         KVB_STFULL1 = KVB_DOEMPTY + DN, KV_NBAR = KVB_STFULL1 + 1;
+                         KVB_STFULL1 = KVB_DOEMPTY + DN, KVB_PFULL1 = KVB_STFULL1 + 1,
+                         KV_NBAR = KVB_PFULL1 + 1;
     static constexpr uint32_t KV_MISC_OFF = KV_BAR_OFF + KV_NBAR * 8;
     static constexpr uint32_t KV_SMEM = KV_MISC_OFF + 16 + 1024;
     // TMEM: S^T [0,128) (P^T over its first 64), dP^T [128,256) (dS^T over
@@ -151,9 +152,21 @@ struct BwdCfg {
     __host__ __device__ static constexpr int st_bar(uint32_t n) {
         return st_buf(n) ? KVB_STFULL1 : KVB_STFULL;
     }
-    // parity of the n-th S^T tile's wait on its barrier
+    // parity of the n-th S^T tile's wait on its barrier (and on p_bar(n))
     __host__ __device__ static constexpr uint32_t st_par(uint32_t n) {
         return KV_SDB ? ((n >> 1) & 1u) : (n & 1u);
+    }
+    // "P^T of the n-th tile written", one barrier per S^T buffer.  With two
+    // buffers, S^T of tile n+1 is ready before the MMA waits for P^T(n), so
+    // an elementwise warp can finish tile n and arrive for tile n+1 while
+    // another has not yet arrived for tile n.  On a single barrier counting
+    // eight arrivals, that early arrival would complete tile n's phase
+    // without the late warp; the MMA would then overwrite the late warp's
+    // S^T buffer, whose barrier would advance two phases before that warp
+    // waited on it (a lost phase: the wait never ends).  Per-buffer
+    // barriers keep every phase to one tile.
+    __host__ __device__ static constexpr int p_bar(uint32_t n) {
+        return st_buf(n) ? KVB_PFULL1 : KVB_PFULL;
     }
     static_assert(DQ_SMEM <= 232448 && KV_SMEM <= 232448, "shared memory");
 };
@@ -166,15 +179,20 @@ struct BwdUnit {
 };
 
 // kWin: the window's loop bounds; longest-first when it has a right bound
-// and no left one (the causal shape).
+// and no left one (the causal shape).  Longest-first orders are walked with
+// unit_of_round's back-and-forth over the CTAs.
+template <bool kCausal, bool kWin>
+__device__ __forceinline__ bool bwd_longest_first(const BwdArgs &a) {
+    return kWin ? (a.wl < 0 && a.wr >= 0) : kCausal;
+}
+
 template <bool kCausal, bool kKeyTiles, bool kWin = false>
 __device__ __forceinline__ BwdUnit make_bwd_unit(int u, const BwdArgs &a) {
     BwdUnit U;
     const int HH = kKeyTiles ? a.H / a.group : a.H;     // K/V heads for key tiles
     const int BH = a.B * HH;
     int bh;
-    const bool lpt = kWin ? (a.wl < 0 && a.wr >= 0) : kCausal;
-    if (lpt) {
+    if (bwd_longest_first<kCausal, kWin>(a)) {
         const int k = u / BH;
         U.m = kKeyTiles ? k : a.n_t - 1 - k;
         bh = u % BH;
@@ -351,6 +369,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool snake = bwd_longest_first<kCausal, kWin>(a);   // unit order (unit_of_round)
     auto bar = [&](int i) -> uint32_t { return base + C::DQ_BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF + 4);
@@ -407,7 +426,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t nk = 0, nv = 0;
             int qn = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
+                const int u = unit_of_round(k, snake);
+                if (u >= a.n_units) continue;
                 const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
                 ok = mbar_wait(bar(C::DQB_QEMPTY), (qn & 1) ^ 1, w, 50);
                 if (!ok) break;
@@ -456,7 +477,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         auto wait_v = [&](uint32_t i) {
             return mbar_wait_warp(bar(C::DQB_VFULL + RV::slot(i)), RV::phase(i), w, 62);
         };
-        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
+            const int u = unit_of_round(k, snake);
+            if (u >= a.n_units) continue;
             const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
             int klo_t, khi_t;
             key_range(U, klo_t, khi_t);
@@ -528,7 +551,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const float sl2 = a.scale_log2;
         uint32_t sph = 0, dpph = 0, dqph = 0;
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
+            const int u = unit_of_round(k, snake);
+            if (u >= a.n_units) continue;
             const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
             int klo_t, khi_t;
             key_range(U, klo_t, khi_t);
@@ -674,6 +699,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool snake = bwd_longest_first<kCausal, kWin>(a);   // unit order (unit_of_round)
     auto bar = [&](int i) -> uint32_t { return base + C::KV_BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF + 4);
@@ -702,6 +728,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(bar(C::KVB_STFULL1), 1);
         mbar_init(bar(C::KVB_DPTFULL), 1);
         mbar_init(bar(C::KVB_PFULL), C::N_EW);
+        mbar_init(bar(C::KVB_PFULL1), C::N_EW);
         mbar_init(bar(C::KVB_DSFULL), C::N_EW);
         mbar_init(bar(C::KVB_ACCFULL), 1);
         mbar_init(bar(C::KVB_ACCEMPTY), C::N_EW);
@@ -732,7 +759,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             uint32_t nq = 0, n_qc = 0, n_dc = 0;     // tiles; Q and dO copies issued
             int kvn = 0;
             bool ok = true;
-            for (int u = blockIdx.x; ok && u < a.n_units_kv; u += gridDim.x) {
+            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units_kv; ++k) {
+                const int u = unit_of_round(k, snake);
+                if (u >= a.n_units_kv) continue;
                 const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
                 ok = mbar_wait(bar(C::KVB_KVEMPTY), (kvn & 1) ^ 1, w, 80);
                 if (!ok) break;
@@ -774,7 +803,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     } else if (warp == 9) {
         // =================== MMA issuer ===================
         WaitCtx w{abort_flag, a.status, kRoleMma};
-        uint32_t q_item = 0, kvph = 0, pph = 0, dsph = 0, accph = 0;
+        uint32_t q_item = 0, kvph = 0, dsph = 0, accph = 0;
         bool ok = true;
         auto wait_q = [&](uint32_t i) {
             return mbar_wait_warp(bar(C::KVB_QFULL + RQ::slot(i)), RQ::phase(i), w, 91);
@@ -782,7 +811,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         auto wait_do = [&](uint32_t i) {
             return mbar_wait_warp(bar(C::KVB_DOFULL + RO::slot(i)), RO::phase(i), w, 96);
         };
-        for (int u = blockIdx.x; ok && u < a.n_units_kv; u += gridDim.x) {
+        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units_kv; ++k) {
+            const int u = unit_of_round(k, snake);
+            if (u >= a.n_units_kv) continue;
             const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
             int qlo_t, qhi_t;
             query_range(U, qlo_t, qhi_t);
@@ -813,10 +844,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const uint32_t ic = q_item + k, in = ic + 1;
                 const bool more = k + 1 < Ti;
                 // ---- G3: dV += P^T dO_i (P^T at columns 32..95 of S^T) ----
-                ok = mbar_wait_warp(bar(C::KVB_PFULL), pph, w, 92);
+                ok = mbar_wait_warp(bar(C::p_bar(ic)), C::st_par(ic), w, 92);
                 if (ok && k == 0) ok = mbar_wait_warp(bar(C::KVB_ACCEMPTY), accph ^ 1, w, 93);
                 if (!ok) break;
-                pph ^= 1;
                 if (k == 0) accph ^= 1;
                 tc_fence_after();
                 gemm_ts_mn(tbase + C::KV_COL_DV, tbase + C::st_col(ic) + 32, do_tile(ic), C::IDESC_ACC,
@@ -864,7 +894,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const float2 c2 = make_float2(sl2, sl2);
         uint32_t stn = 0, dpph = 0, accph = 0;    // stn: S^T tiles of this CTA so far
         bool ok = true;
-        for (int u = blockIdx.x; ok && u < a.n_units_kv; u += gridDim.x) {
+        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units_kv; ++k) {
+            const int u = unit_of_round(k, snake);
+            if (u >= a.n_units_kv) continue;
             const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
             int i0, qhi_t;
             query_range(U, i0, qhi_t);
@@ -890,6 +922,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tc_fence_after();
                 uint32_t sv[64];
                 const uint32_t tST = tbase + lane_off + C::st_col(stn);
+                const int pbar = C::p_bar(stn);
                 ++stn;
                 tmem_ld32(tST + col0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
                 tmem_ld32(tST + col0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
@@ -934,7 +967,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::KVB_PFULL));
+                if (lane == 0) mbar_arrive(bar(pbar));
                 // ---- dS^T = P^T o (dP^T - D[q]) ----
                 ok = mbar_wait(bar(C::KVB_DPTFULL), dpph, w, 101);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }

@@ -418,4 +418,14 @@ __device__ __forceinline__ void unpack2(uint32_t pk, float &lo, float &hi) {
     }
 }
 
+// The unit CTA blockIdx.x runs in its k-th round.  Longest-first orders go
+// back and forth over the CTAs (odd rounds in reverse), so a CTA that takes
+// one of the longest units of a round takes one of the shortest of the
+// next; striding in one direction gave CTA 0 the longest unit of every
+// round.  Every role of a CTA walks the same sequence.
+__device__ __forceinline__ int unit_of_round(int k, bool snake) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return k * G + ((snake && (k & 1)) ? G - 1 - c : c);
+}
+
 }  // namespace fa

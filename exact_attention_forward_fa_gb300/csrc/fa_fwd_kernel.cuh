@@ -164,16 +164,6 @@ __device__ __forceinline__ bool units_longest_first(const FwdArgs &a) {
     return kExt ? (a.wl < 0 && a.wr >= 0) : kCausal;
 }
 
-// The unit CTA blockIdx.x runs in its k-th round.  Longest-first orders go
-// back and forth over the CTAs (odd rounds in reverse), so a CTA that takes
-// one of the longest units of a round takes one of the shortest of the
-// next; striding in one direction gave CTA 0 the longest unit of every
-// round.  Every role of a CTA walks the same sequence.
-__device__ __forceinline__ int unit_of_round(int k, bool snake) {
-    const int G = gridDim.x, c = blockIdx.x;
-    return k * G + ((snake && (k & 1)) ? G - 1 - c : c);
-}
-
 // kSplit: the key range is cut into a.n_splits parts (otherwise one part,
 // folded away at compile time).  kExt: the key range of each Q tile comes
 // from the window ("FlashAttention-3 on Hopper", sec. 4.7: local attention
