@@ -159,3 +159,28 @@ def test_bwd_long_sequence_sampled_dq_and_dk_sum(gpu_lib):
     _check([dq[0, rows, 0]], [ref[0]], ULP["bf16"])
     s = dk[0, :, 0].sum(axis=0)
     assert np.all(np.abs(s) <= 4 * ULP["bf16"] * np.abs(dk[0, :, 0]).sum(axis=0) / np.sqrt(N) + 1e-3)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_back_to_back_launches_stay_in_step(gpu_lib, d):
+    # Many causal launches queued without a host synchronisation between
+    # them, the way a training loop issues them.  Each CTA's roles hand
+    # tiles over through barriers whose phases must each hold one tile's
+    # arrivals; a warp that ran a tile ahead onto a shared barrier once
+    # made a phase complete early and left a wait that never ended (it ran
+    # out its bound and set the status word).  Every launch must leave the
+    # status word clear and give the same bits.
+    fa = gpu_lib
+    dev = torch.device("cuda")
+    B, H, N = 4, 32 if d == 64 else 16, 4096
+    q, k, v, do = (x.to(dev) for x in _inputs(B, H, N, d, "bf16", seed=91))
+    o, lse = fa.attention(q, k, v, causal=True)
+    first = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+    same = torch.ones((), dtype=torch.bool, device=dev)
+    for _ in range(60):
+        g = fa.attention_backward(q, k, v, o, lse, do, causal=True)
+        for x, y in zip(g, first):
+            same &= (x == y).all()
+    assert fa.fa_check_status() == fa.FA_OK
+    assert bool(same.item())
+    assert all(bool(torch.isfinite(x).all()) for x in first)
