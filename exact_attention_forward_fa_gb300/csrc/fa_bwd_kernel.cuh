@@ -180,7 +180,7 @@ struct BwdUnit {
 
 // kWin: the window's loop bounds; longest-first when it has a right bound
 // and no left one (the causal shape).  Longest-first orders are walked with
-// unit_of_round's back-and-forth over the CTAs.
+// unit_stride0's back-and-forth over the CTAs.
 template <bool kCausal, bool kWin>
 __device__ __forceinline__ bool bwd_longest_first(const BwdArgs &a) {
     return kWin ? (a.wl < 0 && a.wr >= 0) : kCausal;
@@ -369,7 +369,7 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool snake = bwd_longest_first<kCausal, kWin>(a);   // unit order (unit_of_round)
+    const bool snake = bwd_longest_first<kCausal, kWin>(a);   // unit order (unit_stride0)
     auto bar = [&](int i) -> uint32_t { return base + C::DQ_BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF + 4);
@@ -426,9 +426,8 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t nk = 0, nv = 0;
             int qn = 0;
             bool ok = true;
-            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
-                const int u = unit_of_round(k, snake);
-                if (u >= a.n_units) continue;
+            for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
+                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
                 ok = mbar_wait(bar(C::DQB_QEMPTY), (qn & 1) ^ 1, w, 50);
                 if (!ok) break;
@@ -477,9 +476,8 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         auto wait_v = [&](uint32_t i) {
             return mbar_wait_warp(bar(C::DQB_VFULL + RV::slot(i)), RV::phase(i), w, 62);
         };
-        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
-            const int u = unit_of_round(k, snake);
-            if (u >= a.n_units) continue;
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
+                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
             int klo_t, khi_t;
             key_range(U, klo_t, khi_t);
@@ -551,9 +549,8 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const float sl2 = a.scale_log2;
         uint32_t sph = 0, dpph = 0, dqph = 0;
         bool ok = true;
-        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
-            const int u = unit_of_round(k, snake);
-            if (u >= a.n_units) continue;
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
+                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
             int klo_t, khi_t;
             key_range(U, klo_t, khi_t);
@@ -699,7 +696,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *gbase = smem_raw + (base - raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool snake = bwd_longest_first<kCausal, kWin>(a);   // unit order (unit_of_round)
+    const bool snake = bwd_longest_first<kCausal, kWin>(a);   // unit order (unit_stride0)
     auto bar = [&](int i) -> uint32_t { return base + C::KV_BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF + 4);
@@ -759,9 +756,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             uint32_t nq = 0, n_qc = 0, n_dc = 0;     // tiles; Q and dO copies issued
             int kvn = 0;
             bool ok = true;
-            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units_kv; ++k) {
-                const int u = unit_of_round(k, snake);
-                if (u >= a.n_units_kv) continue;
+            for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units_kv;
+                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
                 ok = mbar_wait(bar(C::KVB_KVEMPTY), (kvn & 1) ^ 1, w, 80);
                 if (!ok) break;
@@ -811,9 +807,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         auto wait_do = [&](uint32_t i) {
             return mbar_wait_warp(bar(C::KVB_DOFULL + RO::slot(i)), RO::phase(i), w, 96);
         };
-        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units_kv; ++k) {
-            const int u = unit_of_round(k, snake);
-            if (u >= a.n_units_kv) continue;
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units_kv;
+                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
             int qlo_t, qhi_t;
             query_range(U, qlo_t, qhi_t);
@@ -894,9 +889,8 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const float2 c2 = make_float2(sl2, sl2);
         uint32_t stn = 0, dpph = 0, accph = 0;    // stn: S^T tiles of this CTA so far
         bool ok = true;
-        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units_kv; ++k) {
-            const int u = unit_of_round(k, snake);
-            if (u >= a.n_units_kv) continue;
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units_kv;
+                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
             int i0, qhi_t;
             query_range(U, i0, qhi_t);

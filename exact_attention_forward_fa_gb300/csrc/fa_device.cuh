@@ -418,14 +418,20 @@ __device__ __forceinline__ void unpack2(uint32_t pk, float &lo, float &hi) {
     }
 }
 
-// The unit CTA blockIdx.x runs in its k-th round.  Longest-first orders go
-// back and forth over the CTAs (odd rounds in reverse), so a CTA that takes
-// one of the longest units of a round takes one of the shortest of the
-// next; striding in one direction gave CTA 0 the longest unit of every
-// round.  Every role of a CTA walks the same sequence.
-__device__ __forceinline__ int unit_of_round(int k, bool snake) {
+// Persistent unit order: CTA c of G runs units c, then c + s0, then
+// c + s0 + (2G - s0), ... -- strides that alternate between s0 and 2G - s0.
+// Plain orders take s0 = G (units c, c + G, c + 2G, ...).  Longest-first
+// orders go back and forth over the CTAs, s0 = 2G - 1 - 2c: round k gives
+// CTA c unit kG + c for even k and kG + G - 1 - c for odd k, so a CTA that
+// takes one of the longest units of a round takes one of the shortest of
+// the next (striding one way gave CTA 0 the longest unit of every round).
+// The units a CTA visits only grow, so the first one past the end ends its
+// sequence.  Every role of a CTA walks the same sequence:
+//   for (int u = blockIdx.x, st = unit_stride0(snake); u < n;
+//        u += st, st = 2 * gridDim.x - st)
+__device__ __forceinline__ int unit_stride0(bool snake) {
     const int G = gridDim.x, c = blockIdx.x;
-    return k * G + ((snake && (k & 1)) ? G - 1 - c : c);
+    return snake ? 2 * G - 1 - 2 * c : G;
 }
 
 }  // namespace fa

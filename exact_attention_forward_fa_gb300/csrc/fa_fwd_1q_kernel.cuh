@@ -155,9 +155,9 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
                 return true;
             };
-            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
-            const int u = unit_of_round(k, kCausal);   // longest-first: back and forth
-            if (u >= a.n_units) continue;
+            // longest-first (causal): back and forth over the CTAs
+            for (int u = blockIdx.x, st = unit_stride0(kCausal); ok && u < a.n_units;
+                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const Unit1q U = make_unit_1q<kCausal, C::BN>(u, a);
                 ok = mbar_wait(bar(C::B_QSEMPTY), (qn & 1) ^ 1, w, 1);
                 if (!ok) break;
@@ -193,9 +193,9 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             p_out = phase;
             if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
         };
-        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
-            const int u = unit_of_round(k, kCausal);   // longest-first: back and forth
-            if (u >= a.n_units) continue;
+        // longest-first (causal): back and forth over the CTAs
+        for (int u = blockIdx.x, st = unit_stride0(kCausal); ok && u < a.n_units;
+             u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const Unit1q U = make_unit_1q<kCausal, C::BN>(u, a);
             ok = mbar_wait_warp(bar(C::B_QTFULL), qtph, w, 30);
             if (!ok) break;
@@ -297,10 +297,9 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             return true;
         };
-
-        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
-            const int u = unit_of_round(k, kCausal);   // longest-first: back and forth
-            if (u >= a.n_units) continue;
+        // longest-first (causal): back and forth over the CTAs
+        for (int u = blockIdx.x, st = unit_stride0(kCausal); ok && u < a.n_units;
+             u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const Unit1q U = make_unit_1q<kCausal, C::BN>(u, a);
             // ---- copy Q (staged by TMA, 128-B swizzle) into TMEM; the last
             //      QK of the previous unit completed before its S_FULL ----

@@ -251,7 +251,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const bool snake = units_longest_first<kCausal, kExt>(a);   // unit order (unit_of_round)
+    const bool snake = units_longest_first<kCausal, kExt>(a);   // unit order (unit_stride0)
 
     auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
@@ -315,9 +315,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 ++qc;
                 return true;
             };
-            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
-                const int u = unit_of_round(k, snake);
-                if (u >= a.n_units) continue;
+            for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
+                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
                 if (U.act[0]) ok = ok && load_q(0, U);
                 if (U.act[1]) ok = ok && load_q(1, U);
@@ -356,9 +355,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint32_t pph0 = 0, pph1 = 0;
             uint32_t slot = 0, phase = 0;
             bool ok = true;
-            for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
-                const int u = unit_of_round(k, snake);
-                if (u >= a.n_units) continue;
+            for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
+                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
                 uint32_t qs0 = 0, qp0 = 0, qs1 = 0, qp1 = 0;   // Q slot and parity per tile
                 if (U.act[0]) { qs0 = qc % C::NQ; qp0 = (qc / C::NQ) & 1u; ++qc; }
@@ -456,9 +454,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         const float sl2 = kCap ? a.sc_post : a.scale_log2;
         uint32_t sph = 0, oph = 0;
         bool ok = true;
-        for (int k = 0; ok && k * static_cast<int>(gridDim.x) < a.n_units; ++k) {
-                const int u = unit_of_round(k, snake);
-                if (u >= a.n_units) continue;
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
+                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
             const bool act = x ? U.act[1] : U.act[0];
             if (!act) continue;
