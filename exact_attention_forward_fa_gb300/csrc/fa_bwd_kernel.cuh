@@ -683,7 +683,8 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // a lane quarter need no barrier; G3 and G4 read their A operand from
 // column 32.  Q_i and dO_i come through separate rings (Q is held until G4,
 // dO until G3); LSE2 and D of the query columns are read from the padded
-// workspace through L1, where the producer prefetches each tile's lines.
+// workspace through L1 (the producer prefetches them, and the elementwise
+// warps touch the next tile's sectors a tile ahead).
 // ---------------------------------------------------------------------------
 template <int D, bool kCausal, bool kBF16, bool kWin = false, bool kCap = false>
 __global__ void __launch_bounds__(320, 1)
@@ -773,7 +774,10 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     const int i = qlo_t + k % (qhi_t - qlo_t);
                     const size_t wrow = (static_cast<size_t>(U.b) * a.H + hq) * a.NP;
                     // the elementwise warps read LSE2 and D of these 128
-                    // columns: 2 x 512 B, four 128-byte lines each
+                    // columns: 2 x 512 B, four 128-byte lines each.  Measured:
+                    // at d = 128 (little L1 next to 225 KB of shared memory)
+                    // the lines are gone again by the time they are read; at
+                    // d = 64 they stay (causal d = 64 +6 %).
 #pragma unroll
                     for (int l = 0; l < 4; ++l) {
                         asm volatile("prefetch.global.L1 [%0];" :: "l"(a.ws_l + wrow + i * 128 + l * 32));
@@ -903,6 +907,17 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 qlo_r = win_qlo(kr, a);
                 qhi_r = win_qhi(kr, a);
             }
+            // LSE2 and D of a query tile are read below as broadcast loads
+            // through L1, one per four columns, each feeding the next step of
+            // a dependent loop.  At d = 128 the first read of each 32-byte
+            // sector missed L1 and waited for L2 there (measured: 1 miss per
+            // line, the producer's prefetch notwithstanding), so during tile k
+            // lanes 0-7 load one word of each of the 8 sectors of tile k+1's
+            // LSE2 [col0, col0+64) and lanes 8-15 those of D.  The word is
+            // read only at the next tile (into `touched_sum`, which a store
+            // the host rules out keeps alive), when the load has long landed.
+            // Not with a softcap: its registers are spent (the loads spilled).
+            float touched = 0.f, touched_sum = 0.f;
             for (int k = 0; k < a.group * Ti; ++k) {
                 // query head of the group, then its query tile
                 const int hq = U.h * a.group + k / Ti;
@@ -910,6 +925,24 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 const size_t wrow = (static_cast<size_t>(U.b) * a.H + hq) * a.NP;
                 const float4 *lse4 = reinterpret_cast<const float4 *>(a.ws_l + wrow + i * 128 + col0);
                 const float4 *dd4 = reinterpret_cast<const float4 *>(a.ws_d + wrow + i * 128 + col0);
+                touched_sum += touched;
+                if (!kCap && k + 1 < a.group * Ti && lane < 16) {
+                    const int hq1 = U.h * a.group + (k + 1) / Ti;
+                    const int i1 = i0 + (k + 1) % Ti;
+                    const size_t w1 = (static_cast<size_t>(U.b) * a.H + hq1) * a.NP + i1 * 128 + col0 +
+                                      (lane & 7) * 8;
+                    touched = __ldg((lane < 8 ? a.ws_l : a.ws_d) + w1);
+                }
+                // this tile's LSE2, loaded before the wait for S^T so the
+                // loads overlap it (D stays in the loop: 64 more registers
+                // would spill under the 168 a thread has with ten warps; with
+                // a softcap LSE2 is needed again in the dS step, so there it
+                // stays in the loops too)
+                float4 lse_v[16];
+                if constexpr (!kCap) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) lse_v[c] = __ldg(lse4 + c);
+                }
                 // ---- P^T = exp2(S^T c - LSE2[q]) ----
                 ok = mbar_wait(bar(C::st_bar(stn)), C::st_par(stn), w, 100);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
@@ -937,7 +970,7 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
 #pragma unroll
                 for (int c = 0; c < 64; c += 4) {
-                    const float4 l4 = __ldg(lse4 + c / 4);
+                    const float4 l4 = kCap ? __ldg(lse4 + c / 4) : lse_v[c / 4];
                     const float2 x01 = __ffma2_rn(make_float2(pf[c], pf[c + 1]), c2,
                                                   make_float2(-l4.x, -l4.y));
                     const float2 x23 = __ffma2_rn(make_float2(pf[c + 2], pf[c + 3]), c2,
@@ -1028,6 +1061,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::KVB_ACCEMPTY));
             store_cols<D, W, kBF16>(a.dk, a, a.H / a.group, U.b, U.h, krow, half * W, acc, a.alpha);
+            if constexpr (!kCap) {
+                if (a.N < 0 && touched_sum == 0.f) a.status[3] = 1u;    // never true: N >= 1
+            }
         }
     }
 
