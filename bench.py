@@ -605,8 +605,8 @@ def run_ours(args, B, H, N, d, rank, world):
             elif H_kv == H:
                 rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, causal, fa.FA_BF16, sp)
             else:
-                rc = fa.fa_fwd_gqa(q, k, v, o, lse, B, H, H_kv, N, d, alpha, causal,
-                                   fa.FA_BF16, sp)
+                call = fa.fa_fwd_gqa_packed if args.pack else fa.fa_fwd_gqa
+                rc = call(q, k, v, o, lse, B, H, H_kv, N, d, alpha, causal, fa.FA_BF16, sp)
         if rc != fa.FA_OK:
             raise fa.FaError(rc, "fa_fwd")
 
@@ -724,6 +724,8 @@ def run_ours(args, B, H, N, d, rank, world):
     wkey = config_name(B, H, N, d, args.causal, args.fp8)
     if H_kv != H:
         wkey = wkey.replace(f" H{H} ", f" H{H} Hkv{H_kv} ")
+        if args.pack:
+            wkey += " packed heads"
     if n_splits:
         wkey += f" split-KV x{n_splits}"
     wkey += variant_suffix(var)
@@ -776,6 +778,9 @@ def main():
                          "(0: the library's choice for the device)")
     ap.add_argument("--hkv", type=int, default=0,
                     help="grouped K/V heads (GQA/MQA, fa_fwd_gqa); default: H")
+    ap.add_argument("--pack", action="store_true",
+                    help="with --hkv: pack each K/V head's query heads into one Q tile "
+                         "(fa_fwd_gqa_packed)")
     ap.add_argument("--window", type=int, nargs=2, default=None, metavar=("LEFT", "RIGHT"),
                     help="local window (fa_fwd_ext): key j visible from row i when "
                          "i - LEFT <= j <= i + RIGHT; -1 = no bound on that side")
@@ -800,6 +805,9 @@ def main():
                      or (args.bwd and variant_of(args) is None)):
         ap.error("--hkv must divide --H, not with --fp8; with --bwd it needs --window "
                  "(e.g. --window -1 -1)")
+    if args.pack and (not args.hkv or args.bwd or variant_of(args) is not None
+                      or args.d not in (64, 128)):
+        ap.error("--pack needs --hkv, the plain or causal forward, d 64 or 128")
     if args.splits is not None and (args.bwd or args.fp8 or args.hkv or args.d not in (64, 128)):
         ap.error("--splits applies to the BF16 forward, d 64 or 128, without --hkv")
     if variant_of(args) is not None and (args.fp8 or args.splits is not None

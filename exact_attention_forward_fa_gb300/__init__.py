@@ -29,7 +29,7 @@ FA_BF16 = 0
 FA_FP16 = 1
 
 # Every symbol include/fa.h declares (checked by the tests).
-EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_ext", "fa_fwd_splitkv", "fa_splitkv_workspace_floats",
+EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_packed", "fa_fwd_ext", "fa_fwd_splitkv", "fa_splitkv_workspace_floats",
            "fa_splitkv_auto", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_ext", "fa_bwd_noalloc",
            "fa_check_status", "fa_status_detail", "fa_selftest_wait_timeout",
            "fa_status_string", "fa_version")
@@ -58,6 +58,8 @@ def load():
     lib.fa_fwd.restype = i
     lib.fa_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_gqa.restype = i
+    lib.fa_fwd_gqa_packed.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_gqa_packed.restype = i
     lib.fa_fwd_ext.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, f, vp, i, vp]
     lib.fa_fwd_ext.restype = i
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp, vp]
@@ -131,6 +133,15 @@ def fa_fwd_gqa(q, k, v, o, lse, B: int, H: int, H_kv: int, N: int, d: int, alpha
     return load().fa_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
                              int(H_kv), int(N), int(d), float(alpha), int(causal), int(dtype),
                              _stream(stream))
+
+
+def fa_fwd_gqa_packed(q, k, v, o, lse, B: int, H: int, H_kv: int, N: int, d: int,
+                      alpha: float, causal: int, dtype: int, stream=None) -> int:
+    """Direct call of the C entry point: fa_fwd_gqa with the query heads of
+    each K/V head packed into the rows of one Q tile (see include/fa.h)."""
+    return load().fa_fwd_gqa_packed(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                    int(H), int(H_kv), int(N), int(d), float(alpha),
+                                    int(causal), int(dtype), _stream(stream))
 
 
 def fa_fwd_ext(q, k, v, o, lse, B: int, H: int, H_kv: int, N: int, d: int, alpha: float,
@@ -361,9 +372,11 @@ def fa_version() -> int:
 
 
 def attention(q, k, v, causal: bool = False, alpha: float | None = None,
-              out=None, lse=None, want_lse: bool = True, stream=None):
+              out=None, lse=None, want_lse: bool = True, stream=None,
+              pack_gqa: bool = False):
     """Convenience wrapper over ``fa_fwd`` for torch tensors on the GPU
-    (``fa_fwd_gqa`` when K/V have fewer heads than Q).
+    (``fa_fwd_gqa`` when K/V have fewer heads than Q; ``fa_fwd_gqa_packed``
+    with ``pack_gqa``).
 
     Allocates O (and LSE) with torch when not given, launches, and raises
     FaError on a non-OK status.  Returns (O, LSE or None)."""
@@ -385,8 +398,8 @@ def attention(q, k, v, causal: bool = False, alpha: float | None = None,
     if H_kv == H:
         rc = fa_fwd(q, k, v, out, lse, B, H, N, d, alpha, int(bool(causal)), dt, stream)
     else:
-        rc = fa_fwd_gqa(q, k, v, out, lse, B, H, H_kv, N, d, alpha, int(bool(causal)), dt,
-                        stream)
+        call = fa_fwd_gqa_packed if pack_gqa else fa_fwd_gqa
+        rc = call(q, k, v, out, lse, B, H, H_kv, N, d, alpha, int(bool(causal)), dt, stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
     return out, lse

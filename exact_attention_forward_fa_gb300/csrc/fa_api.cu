@@ -89,6 +89,23 @@ fa_status encode_bshd(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, i
     return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
 }
 
+// The same map with the box {128 B, g heads, 128 / g rows, 1}: one box is
+// a Q tile of g heads packed row by row (tile row p = position p / g,
+// head p % g), 128 rows of 128 B in shared memory like an ordinary tile.
+fa_status encode_bshd_packed(CUtensorMap *m, const void *ptr, CUtensorMapDataType dt, int B,
+                             int H, int N, int d, int g) {
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {2ull * d, 2ull * d * H, 2ull * d * H * static_cast<cuuint64_t>(N)};
+    cuuint32_t box[4] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(128 / g), 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(m, dt, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -109,10 +126,12 @@ const char *fa_status_string(fa_status s) {
 }
 
 // The forward for H query heads over H_kv key/value heads (H_kv divides H;
-// query head h reads key/value head h / (H / H_kv)).
+// query head h reads key/value head h / (H / H_kv)).  pack: the g = H / H_kv
+// query heads of a key/value head share each Q tile (d in {64, 128}, g
+// dividing 128); with g = 1 that is the plain layout.
 static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
                           int B, int H, int H_kv, int N, int d, float alpha, int causal,
-                          fa_dtype dtype, void *stream) {
+                          fa_dtype dtype, void *stream, bool pack = false) {
     // ---- host-side validation: nothing is launched on failure ----
     if (!q || !k || !v || !o) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
@@ -123,14 +142,20 @@ static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, 
     if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FA_ERR_MISALIGNED;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_MISALIGNED;
+    const int g = H / H_kv;
+    if (pack && g == 1) pack = false;                  // one head per tile: the plain layout
+    if (pack && (d == 256 || 128 % g != 0)) return FA_ERR_UNSUPPORTED;
     // TMA: every global stride < 2^40 bytes; kernel indexing uses 64-bit
     // offsets, the unit counter is a 32-bit int.
     const uint64_t batch_stride = 2ull * d * H * static_cast<uint64_t>(N);
     if (batch_stride >= (1ull << 40)) return FA_ERR_TOO_LARGE;
     // Work units: pairs of 128-row Q tiles for d <= 128, single Q tiles
-    // for d = 256 (whose O accumulator alone fills half of TMEM).
+    // for d = 256 (whose O accumulator alone fills half of TMEM); packed,
+    // pairs of tiles of 128 / g positions over the key/value heads.
     const uint64_t n_qt = (static_cast<uint64_t>(N) + 127) / 128;
-    const uint64_t units = static_cast<uint64_t>(B) * H * (d == 256 ? n_qt : (n_qt + 1) / 2);
+    const uint64_t n_pt = pack ? (static_cast<uint64_t>(N) + 128 / g - 1) / (128 / g) : n_qt;
+    const uint64_t units = pack ? static_cast<uint64_t>(B) * H_kv * ((n_pt + 1) / 2)
+                                : static_cast<uint64_t>(B) * H * (d == 256 ? n_qt : (n_qt + 1) / 2);
     if (units > 0x7fffffffull || static_cast<uint64_t>(B) * H * N > 0x7fffffffffffull)
         return FA_ERR_TOO_LARGE;
 
@@ -143,7 +168,8 @@ static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, 
     const CUtensorMapDataType dt =
         dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const cuuint32_t kv_rows = d == 256 ? 64 : 128;     // key tile height
-    if ((st = encode_bshd(&L.q, q, dt, B, H, N, d, 128)) != FA_OK) return st;
+    st = pack ? encode_bshd_packed(&L.q, q, dt, B, H, N, d, g) : encode_bshd(&L.q, q, dt, B, H, N, d, 128);
+    if (st != FA_OK) return st;
     if ((st = encode_bshd(&L.k, k, dt, B, H_kv, N, d, kv_rows)) != FA_OK) return st;
     if ((st = encode_bshd(&L.v, v, dt, B, H_kv, N, d, kv_rows)) != FA_OK) return st;
     L.args.o = o;
@@ -153,7 +179,7 @@ static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, 
     L.args.H = H;
     L.args.N = N;
     L.args.n_kv = static_cast<int>(d == 256 ? (static_cast<uint64_t>(N) + 63) / 64 : n_qt);
-    L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
+    L.args.n_pairs = static_cast<int>((n_pt + 1) / 2);
     L.args.n_units = static_cast<int>(units);
     L.args.group = H / H_kv;
     L.args.n_splits = 1;
@@ -162,8 +188,10 @@ static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, 
     L.stream = static_cast<cudaStream_t>(stream);
     L.causal = causal != 0;
     L.bf16 = dtype == FA_BF16;
+    L.d64 = d == 64;
 
-    cudaError_t e = (d == 64) ? fa::launch_fwd_d64(L)
+    cudaError_t e = pack ? fa::launch_fwd_pack(L)
+                    : (d == 64) ? fa::launch_fwd_d64(L)
                     : (d == 128) ? fa::launch_fwd_d128(L) : fa::launch_fwd_d256(L);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -172,6 +200,12 @@ fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *ls
                  int H, int N, int d, float alpha, int causal, fa_dtype dtype,
                  void *stream) {
     return fwd_impl(q, k, v, o, lse, B, H, H, N, d, alpha, causal, dtype, stream);
+}
+
+fa_status fa_fwd_gqa_packed(const void *q, const void *k, const void *v, void *o, float *lse,
+                            int B, int H, int H_kv, int N, int d, float alpha, int causal,
+                            fa_dtype dtype, void *stream) {
+    return fwd_impl(q, k, v, o, lse, B, H, H_kv, N, d, alpha, causal, dtype, stream, true);
 }
 
 fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B,

@@ -169,10 +169,16 @@ __device__ __forceinline__ bool units_longest_first(const FwdArgs &a) {
 // from the window ("FlashAttention-3 on Hopper", sec. 4.7: local attention
 // bounds the loop on both sides), so a tile may also leave the pair's
 // descending key stream before its end.
-template <bool kCausal, bool kSplit, bool kExt = false>
+// kPack (grouped heads, "PackGQA"): the a.group query heads of one K/V head
+// share each Q tile -- tile row p holds query position m R + p / group of
+// query head h group + p % group, R = 128 / group -- so units run over K/V
+// heads (U.h is then the K/V head) and one K/V stream serves the whole
+// group.  R divides 128, so a tile's positions never straddle a key tile.
+template <bool kCausal, bool kSplit, bool kExt = false, bool kPack = false>
 __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     Unit U;
-    const int BH = a.B * a.H;
+    const int HH = kPack ? a.H / a.group : a.H;    // heads the units run over
+    const int BH = a.B * HH;
     const int S = kSplit ? a.n_splits : 1;
     U.s = kSplit ? u % S : 0;       // the splits of one pair are adjacent units
     if (kSplit) u /= S;
@@ -186,8 +192,8 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
         p = u % a.n_pairs;
         bh = u / a.n_pairs;
     }
-    U.b = bh / a.H;
-    U.h = bh % a.H;
+    U.b = bh / HH;
+    U.h = bh % HH;
     if constexpr (kExt) {
         int lo[2] = {0, 0}, hi[2] = {0, 0};
         for (int x = 0; x < 2; ++x) {
@@ -213,8 +219,14 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     int hi[2];
     for (int x = 0; x < 2; ++x) {
         U.m[x] = 2 * p + x;
-        U.act[x] = U.m[x] * 128 < a.N;
-        hi[x] = U.act[x] ? (kCausal ? min(a.n_kv, U.m[x] + 1) : a.n_kv) : 0;
+        if constexpr (kPack) {
+            const int q0 = U.m[x] * (128 / a.group);          // first position of the tile
+            U.act[x] = q0 < a.N;
+            hi[x] = U.act[x] ? (kCausal ? min(a.n_kv, (q0 >> 7) + 1) : a.n_kv) : 0;
+        } else {
+            U.act[x] = U.m[x] * 128 < a.N;
+            hi[x] = U.act[x] ? (kCausal ? min(a.n_kv, U.m[x] + 1) : a.n_kv) : 0;
+        }
     }
     // split s of the pair's key range [0, Tf): tiles [Tf s / S, Tf (s+1) / S)
     const int Tf = max(hi[0], hi[1]);
@@ -234,7 +246,7 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
 // 2: window, sinks and softcap; kCausal is then unused (the causal mask is
 // the window (-1, 0)).
 template <int D, bool kCausal, bool kBF16, bool kFP8 = false, bool kSplit = false,
-          int kVar = 0>
+          int kVar = 0, bool kPack = false>
 __global__ void __launch_bounds__(384, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k,
@@ -243,6 +255,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     constexpr bool kExt = kVar != 0;
     constexpr bool kCap = kVar == 2;
     static_assert(!kExt || (!kFP8 && !kSplit && !kCausal), "variants: 16-bit, one split");
+    static_assert(!kPack || (!kExt && !kFP8 && !kSplit), "packed heads: plain or causal, 16-bit");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -309,7 +322,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
                     tma_load_4d(&tm_q, base + C::Q_OFF + qs * C::TILE_BYTES + c * C::CHUNK_BYTES,
-                                bar(C::B_QFULL + qs), c * (128 / C::ESZ), U.h, U.m[x] * 128, U.b);
+                                bar(C::B_QFULL + qs), c * (128 / C::ESZ),
+                                kPack ? U.h * a.group : U.h,                 // packed: box of group heads
+                                kPack ? U.m[x] * (128 / a.group) : U.m[x] * 128, U.b);
                 qarmed |= 1u << qs;
                 qarmed_par = (qarmed_par & ~(1u << qs)) | (qph << qs);
                 ++qc;
@@ -317,10 +332,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             };
             for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
                      u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
-                const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
+                const Unit U = make_unit<kCausal, kSplit, kExt, kPack>(u, a);
                 if (U.act[0]) ok = ok && load_q(0, U);
                 if (U.act[1]) ok = ok && load_q(1, U);
-                const int hk = U.h / a.group;        // K/V head of this query head
+                const int hk = kPack ? U.h : U.h / a.group;   // K/V head of this query head
                 for (int t = 0; t < U.T && ok; ++t) {
                     const int j = U.jhi - 1 - t;
                     for (int kv = 0; kv < 2; ++kv) {
@@ -357,7 +372,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             bool ok = true;
             for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
                      u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
-                const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
+                const Unit U = make_unit<kCausal, kSplit, kExt, kPack>(u, a);
                 uint32_t qs0 = 0, qp0 = 0, qs1 = 0, qp1 = 0;   // Q slot and parity per tile
                 if (U.act[0]) { qs0 = qc % C::NQ; qp0 = (qc / C::NQ) & 1u; ++qc; }
                 if (U.act[1]) { qs1 = qc % C::NQ; qp1 = (qc / C::NQ) & 1u; ++qc; }
@@ -456,10 +471,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         bool ok = true;
         for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
                      u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
-            const Unit U = make_unit<kCausal, kSplit, kExt>(u, a);
+            const Unit U = make_unit<kCausal, kSplit, kExt, kPack>(u, a);
             const bool act = x ? U.act[1] : U.act[0];
             if (!act) continue;
             const int mt = x ? U.m[1] : U.m[0];
+            // this row's query position and head (packed: the group's heads
+            // share the tile, and its rows share one diagonal key tile)
+            const int qpos = kPack ? mt * (128 / a.group) + row / a.group : mt * 128 + row;
+            const int qh = kPack ? U.h * a.group + row % a.group : U.h;
             const int t0 = x ? U.t0[1] : U.t0[0];
             const int t1 = kExt ? (x ? U.t1[1] : U.t1[0]) : U.T;
             // this row's visible keys (rows past N: any non-empty range)
@@ -516,7 +535,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     llo = klo - j * 128;
                 } else {
                     if (j == a.n_kv - 1) lim = min(lim, a.N - j * 128);
-                    if (kCausal && j == mt) lim = min(lim, row + 1);
+                    if constexpr (kPack) {
+                        if (kCausal && j == ((mt * (128 / a.group)) >> 7)) lim = min(lim, qpos - j * 128 + 1);
+                    } else {
+                        if (kCausal && j == mt) lim = min(lim, row + 1);
+                    }
                 }
                 auto load_s = [&]() __attribute__((always_inline)) {
                     tmem_ld32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
@@ -688,9 +711,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     }
                 }
             }
-            const int grow = mt * 128 + row;
+            const int grow = qpos;
             uint16_t *orow = reinterpret_cast<uint16_t *>(a.o) +
-                             ((static_cast<size_t>(U.b) * a.N + grow) * a.H + U.h) * D;
+                             ((static_cast<size_t>(U.b) * a.N + grow) * a.H + qh) * D;
             // The whole O row comes into registers first, so the accumulator
             // is handed back to the next unit's P V before the stores.
             uint32_t ov[D];
@@ -728,7 +751,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
             }
             if (a.lse != nullptr && grow < a.N)
-                a.lse[(static_cast<size_t>(U.b) * a.H + U.h) * a.N + grow] =
+                a.lse[(static_cast<size_t>(U.b) * a.H + qh) * a.N + grow] =
                     lse2 * 0.69314718055994530942f;
         }
     }

@@ -28,6 +28,9 @@ cudaError_t launch_fwd_fp8(const FwdLaunch &L);    // e4m3 maps, 128-byte boxes
 cudaError_t launch_fwd_split(const FwdLaunch &L);  // split key ranges, d in {64, 128}
 cudaError_t launch_fwd_ext(const FwdLaunch &L);    // window / sinks, d in {64, 128}
 cudaError_t launch_fwd_ext_softcap(const FwdLaunch &L);   // the same with a softcap
+// Grouped heads packed into the Q tiles (q map box {64, group, 128 / group, 1}),
+// d in {64, 128}, plain or causal.
+cudaError_t launch_fwd_pack(const FwdLaunch &L);
 // Split-KV combine: O, LSE from S partials (o_part [S][B][N][H][d] FP32,
 // lse_part [S][B][H][N]); d in {64, 128}.
 struct CombineArgs {
@@ -85,10 +88,10 @@ cudaError_t launch_quantize(const QuantLaunch &L);
 // Shared helper: set the dynamic shared-memory limit once per device, then
 // launch one instantiation.
 template <int D, bool kCausal, bool kBF16, bool kFP8 = false, bool kSplit = false,
-          int kVar = 0>
+          int kVar = 0, bool kPack = false>
 cudaError_t launch_fwd_inst(const FwdLaunch &L) {
     using Cfg = FwdCfg<D, kCausal, kBF16, kFP8>;
-    auto kern = fa_fwd_kernel<D, kCausal, kBF16, kFP8, kSplit, kVar>;
+    auto kern = fa_fwd_kernel<D, kCausal, kBF16, kFP8, kSplit, kVar, kPack>;
     static unsigned long long configured = 0ull;   // bit per device id (< 64)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -140,6 +143,16 @@ cudaError_t launch_fwd_split_dispatch(const FwdLaunch &L) {
                       : launch_fwd_inst<D, true, false, false, true>(L);
     return L.bf16 ? launch_fwd_inst<D, false, true, false, true>(L)
                   : launch_fwd_inst<D, false, false, false, true>(L);
+}
+
+// Grouped heads packed into the Q tiles, d in {64, 128}.
+template <int D>
+cudaError_t launch_fwd_pack_dispatch(const FwdLaunch &L) {
+    if (L.causal)
+        return L.bf16 ? launch_fwd_inst<D, true, true, false, false, 0, true>(L)
+                      : launch_fwd_inst<D, true, false, false, false, 0, true>(L);
+    return L.bf16 ? launch_fwd_inst<D, false, true, false, false, 0, true>(L)
+                  : launch_fwd_inst<D, false, false, false, false, 0, true>(L);
 }
 
 // Score and mask variants, d in {64, 128}: kVar 1 (window, sinks) or 2

@@ -90,6 +90,24 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o,
                      float alpha, int causal, fa_dtype dtype, void *stream);
 
 /*
+ * fa_fwd_gqa_packed -- fa_fwd_gqa with the g = H / H_kv query heads of each
+ * key/value head packed into the rows of one Q tile ("PackGQA" of the GQA
+ * remark in "FlashAttention-3 on Hopper"): a tile holds 128 / g query
+ * positions of all g heads, so one pass over a key/value head's K and V
+ * serves the whole group and short sequences do not leave tiles half
+ * empty.  Same arguments, layouts, results (up to FP32 rounding order: the
+ * softmax's rescale decisions are taken per warp of rows) and errors as
+ * fa_fwd_gqa; additionally d must be 64 or 128 and g must divide 128
+ * (g = 1 runs fa_fwd_gqa), else FA_ERR_UNSUPPORTED.  Measured on GB300
+ * (H 32 over H_kv 2 or 8, d 128): N = 64 twice the throughput of
+ * fa_fwd_gqa, N = 256 about the same, N = 4096 2-5 % below it -- a choice
+ * for short sequences.
+ */
+fa_status fa_fwd_gqa_packed(const void *q, const void *k, const void *v, void *o,
+                            float *lse, int B, int H, int H_kv, int N, int d,
+                            float alpha, int causal, fa_dtype dtype, void *stream);
+
+/*
  * fa_fwd_ext -- fa_fwd_gqa with the score and mask variants of
  * "FlashAttention-3 on Hopper" sec. 4.6 (learnable sinks folded into the
  * row sum at finalize) and sec. 4.7 (local / sliding-window masks; a score

@@ -92,6 +92,14 @@ def test_gqa_validation_codes(lib, H, H_kv, code):
     assert lib.fa_fwd_gqa(A, A, A, A, None, 1, H, H_kv, 128, 64, 0.125, 0, 0, None) == code
 
 
+@pytest.mark.parametrize("H,H_kv,d,code", [(6, 4, 64, fa.FA_ERR_INVALID_ARG),   # H_kv must divide H
+                                           (6, 2, 64, fa.FA_ERR_UNSUPPORTED),   # group 3 does not divide 128
+                                           (8, 1, 256, fa.FA_ERR_UNSUPPORTED),  # d = 256
+                                           (8, 2, 96, fa.FA_ERR_UNSUPPORTED)])
+def test_gqa_packed_validation_codes(lib, H, H_kv, d, code):
+    assert lib.fa_fwd_gqa_packed(A, A, A, A, None, 1, H, H_kv, 128, d, 0.125, 0, 0, None) == code
+
+
 def _xcall(lib, q=A, k=A, v=A, o=A, lse=None, B=1, H=2, H_kv=1, N=128, d=128, alpha=0.088,
            wl=-1, wr=0, softcap=0.0, sinks=None, dtype=0):
     return lib.fa_fwd_ext(q, k, v, o, lse, B, H, H_kv, N, d, alpha, wl, wr, softcap, sinks,

@@ -57,6 +57,17 @@ def test_forward_variants_back_to_back(gpu_lib, window, softcap, sinks):
     _repeat_same_bits(fa, lambda: fa.attention_ext(q, k, v, window=window, softcap=softcap, sinks=s))
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_packed_gqa_back_to_back(gpu_lib, causal):
+    fa = gpu_lib
+    g = torch.Generator(device="cuda")
+    g.manual_seed(106)
+    q = torch.randn(4, 4096, 16, 128, device="cuda", dtype=torch.bfloat16, generator=g)
+    k = torch.randn(4, 4096, 2, 128, device="cuda", dtype=torch.bfloat16, generator=g)
+    v = torch.randn(4, 4096, 2, 128, device="cuda", dtype=torch.bfloat16, generator=g)
+    _repeat_same_bits(fa, lambda: fa.attention(q, k, v, causal=causal, pack_gqa=True))
+
+
 def test_fp8_back_to_back(gpu_lib):
     fa = gpu_lib
     q, k, v = _inputs(4, 16, 4096, 128, seed=103)
