@@ -278,6 +278,25 @@ def test_gqa_packed_matches_unpacked_closely(gpu_lib):
         assert float((l1 - l2).abs().max()) <= 1e-4
 
 
+def test_gqa_packed_with_one_head_per_group_is_the_plain_forward(gpu_lib):
+    # g = 1: fa_fwd_gqa_packed takes the plain layout, so its bits equal fa_fwd's.
+    fa = gpu_lib
+    B, H, N, d = 2, 3, 700, 128
+    q, k, v = (x.cuda() for x in synth.qkv(B, H, N, d, seed=17))
+    a = synth.default_alpha(d)
+    outs = []
+    for call in ("fa_fwd", "fa_fwd_gqa_packed"):
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        if call == "fa_fwd":
+            rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, a, 1, fa.FA_BF16)
+        else:
+            rc = fa.fa_fwd_gqa_packed(q, k, v, o, lse, B, H, H, N, d, a, 1, fa.FA_BF16)
+        assert rc == fa.FA_OK and fa.fa_check_status() == fa.FA_OK
+        outs.append((o, lse))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 SPLIT_CASES = [
     # (B, H, N, d, causal, n_splits)
     (1, 2, 1000, 128, True, 3),
