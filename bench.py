@@ -15,6 +15,11 @@ C ABI with pinned host buffers: host->device copies of Q/K/V, the launch and
 the device->host copy of O and LSE, every step.  ``cpu_baseline`` is the
 FP64 CPU oracle on a bounded sample of the same workload.
 ``--impl reference`` times that oracle alone, as the reference arm.
+The default run (one GPU, the workload above) also times, in the same
+process, the causal mask, d = 64 and d = 256 at N = 4096, the FP8 workload
+(kernel and pre-pass apart), the backward, and a sustained run of >= 1.2 s,
+each under ``also_measured`` with its own roofline fraction and clocks
+(``--no-extra`` skips them).
 ``--fp8`` times the FP8 forward (the quantization pre-pass reported
 separately); ``--bwd`` times the backward (fa_bwd: dQ, dK, dV from O, LSE
 and dO), counting its FLOPs as 2.5x the forward's as the pages do.
@@ -541,6 +546,156 @@ def run_reference(args, B, H, N, d, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def _timed(launch, steps, stream, dev, min_ms=0.0):
+    """Times `steps` back-to-back launches (or, with min_ms, as many as fill
+    that long) with CUDA events on `stream`, clocks sampled meanwhile.
+    Returns (ms per launch, launches timed, clock summary)."""
+    import torch
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    if min_ms > 0.0:            # size the run from a short probe
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(10):
+                launch()
+            stop.record(stream)
+        stream.synchronize()
+        steps = max(steps, int(min_ms / max(start.elapsed_time(stop) / 10, 1e-3)) + 1)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index or 0) as clk:
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(steps):
+                launch()
+            stop.record(stream)
+        stream.synchronize()
+    return start.elapsed_time(stop) / steps, steps, clk.summary()
+
+
+def extra_measurements(args, fa, dev, stream):
+    """Other workloads timed in the same process, so that they are observed
+    by the same run as the headline: the causal mask, the other head dims of
+    the sequence sweep at N = 4096, the FP8 workload (kernel and pre-pass
+    apart), the backward, and a sustained run of the headline workload
+    (>= 1.2 s of back-to-back launches, compared with the sustained peak).
+    Each entry carries its own roofline fraction and clocks."""
+    import torch
+    from exact_attention_forward_fa_gb300 import synth
+    burst, sustained, src = measured_peaks()
+    sp = stream.cuda_stream
+    steps = max(args.steps, 20)
+    out = {}
+
+    def entry(name, fl, ms, n, clocks, peak, peak_kind, extra=None):
+        ach = fl / (ms * 1e-3) / 1e12
+        out[name] = {"value": ach, "unit": "TFLOP/s", "ms_per_step": ms, "steps": n,
+                     "roofline": {"bound": "tensor", "achieved": ach, "peak": peak,
+                                  "unit": "TFLOP/s", "frac": ach / peak,
+                                  "peak_source": f"{src} {peak_kind}"},
+                     "clocks": clocks, **(extra or {})}
+
+    def check(where):
+        if fa.fa_check_status(sp) != fa.FA_OK:
+            raise RuntimeError(f"device status after {where}: {fa.fa_status_detail()}")
+
+    def fwd_case(name, B, H, N, d, causal, min_ms=0.0):
+        q, k, v = (x.to(dev) for x in synth.qkv(B, H, N, d, seed=synth.BASE_SEED))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        alpha = synth.default_alpha(d)
+
+        def launch():
+            rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, int(causal), fa.FA_BF16, sp)
+            if rc != fa.FA_OK:
+                raise fa.FaError(rc, "fa_fwd")
+        for _ in range(max(3, args.warmup)):
+            launch()
+        ms, n, clk = _timed(launch, steps, stream, dev, min_ms)
+        check(name)
+        long_run = ms * n >= 1000.0
+        peak = sustained if long_run and sustained > 0 else burst
+        kind = "bf16 sustained (cuBLAS 8192^3)" if long_run else "bf16 burst (cuBLAS 8192^3)"
+        entry(name, flops(B, H, N, d, causal), ms, n, clk, peak, kind,
+              {"workload": config_name(B, H, N, d, causal), "timed_region_ms": ms * n})
+
+    fwd_case("fwd_causal", 4, 16, 4096, 128, True)
+    fwd_case("fwd_d64_n4096", 4, 32, 4096, 64, False)
+    fwd_case("fwd_d256_n4096", 4, 8, 4096, 256, False)
+    fwd_case("fwd_sustained", 4, 16, 4096, 128, False, min_ms=1200.0)
+
+    # FP8: outlier inputs, Q and K rotated, per-tile scales
+    B, H, N, d = 4, 16, 4096, 128
+    q, k, v = (x.to(dev) for x in synth.qkv(B, H, N, d, seed=synth.BASE_SEED, outliers=True))
+    signs = torch.from_numpy(synth.hadamard_signs(d)).to(dev)
+    nt = (N + 127) // 128
+    q8, k8, v8 = (torch.empty(q.shape, dtype=torch.uint8, device=dev) for _ in range(3))
+    qs, ks, vs = (torch.empty((B, H, nt), dtype=torch.float32, device=dev) for _ in range(3))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    alpha = synth.default_alpha(d)
+
+    def quantize():
+        for x, x8, sc, sg in ((q, q8, qs, signs), (k, k8, ks, signs), (v, v8, vs, None)):
+            rc = fa.fa_quantize_fp8(x, x8, sc, sg, B, H, N, d, sp)
+            if rc != fa.FA_OK:
+                raise fa.FaError(rc, "fa_quantize_fp8")
+
+    def fp8():
+        rc = fa.fa_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, B, H, N, d, alpha, 0, sp)
+        if rc != fa.FA_OK:
+            raise fa.FaError(rc, "fa_fwd_fp8")
+    for _ in range(3):
+        quantize()
+    pre_ms, _, _ = _timed(quantize, 20, stream, dev)
+    for _ in range(max(3, args.warmup)):
+        fp8()
+    ms, n, clk = _timed(fp8, steps, stream, dev)
+    check("fp8")
+    # bytes of the pre-pass: bf16 in, e4m3 out, one FP32 scale per tile
+    pre_bytes = 3 * (q.numel() * 3 + B * H * nt * 4)
+    entry("fwd_fp8", flops(B, H, N, d, False), ms, n, clk, 2 * burst,
+          "bf16 burst (cuBLAS 8192^3) x 2 (nominal FP8/BF16 ratio)",
+          {"workload": config_name(B, H, N, d, False, fp8=True), "timed_region_ms": ms * n,
+           "prepass": {"ms": pre_ms, "tensors": 3, "rotated": 2,
+                       "algorithmic_bytes": pre_bytes,
+                       "achieved_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9,
+                       "hbm_frac": pre_bytes / (pre_ms * 1e-3) / 1e9 / measured_hbm()}})
+    del q8, k8, v8
+
+    # backward (dQ, dK, dV from O, LSE, dO), FLOPs 2.5 x the forward's
+    dout = torch.from_numpy(synth.normal((B, N, H, d), seed=synth.BASE_SEED + 3)).to(
+        torch.bfloat16).to(dev)
+    q, k, v = (x.to(dev) for x in synth.qkv(B, H, N, d, seed=synth.BASE_SEED))
+    rc = fa.fa_fwd(q, k, v, o, lse, B, H, N, d, alpha, 0, fa.FA_BF16, sp)
+    if rc != fa.FA_OK:
+        raise fa.FaError(rc, "fa_fwd")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty((fa.bwd_workspace_floats(B, H, N),), dtype=torch.float32, device=dev)
+
+    def bwd():
+        rc = fa.fa_bwd(q, k, v, o, dout, lse, ws, dq, dk, dv, B, H, N, d, alpha, 0,
+                       fa.FA_BF16, sp)
+        if rc != fa.FA_OK:
+            raise fa.FaError(rc, "fa_bwd")
+    for _ in range(max(3, args.warmup)):
+        bwd()
+    ms, n, clk = _timed(bwd, max(10, args.steps), stream, dev)
+    check("bwd")
+    entry("bwd", BWD_FACTOR * flops(B, H, N, d, False), ms, n, clk, burst,
+          "bf16 burst (cuBLAS 8192^3)",
+          {"workload": config_name(B, H, N, d, False).replace("attention fwd", "attention bwd"),
+           "timed_region_ms": ms * n, "flops": "2.5 x the forward's"})
+    return out
+
+
+def measured_hbm():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"])
+    except Exception:
+        return 6800.0
+
+
 def config_name(B, H, N, d, causal, fp8=False):
     kind = "fp8 e4m3 (outliers, Hadamard)" if fp8 else "bf16"
     return (f"attention fwd B{B} H{H} N{N} d{d} {kind} {'causal' if causal else 'non-causal'}"
@@ -758,6 +913,10 @@ def run_ours(args, B, H, N, d, rank, world):
         "gpu_launches": args.steps * (2 if n_splits else 1),
         "clocks": clk.summary(),
     }
+    plain_default = (not args.fp8 and var is None and not n_splits and H_kv == H
+                     and (B, H, N, d) == tuple(WORKLOAD.values()) and not args.causal)
+    if plain_default and world == 1 and not args.no_extra:
+        line["also_measured"] = extra_measurements(args, fa, dev, stream)
     if not args.skip_cpu:
         line["cpu_baseline"] = cpu_baseline(args, B, H, N, d)
     print(json.dumps(line), flush=True)
@@ -792,6 +951,9 @@ def main():
                     help="time the backward pass (fa_bwd) instead of the forward")
     ap.add_argument("--skip-cpu", action="store_true",
                     help="omit the cpu_baseline leg (profiling runs)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="omit the other workloads the default run also times "
+                         "(also_measured: causal, d 64/256, FP8, backward, sustained)")
     ap.add_argument("--B", type=int, default=WORKLOAD["B"])
     ap.add_argument("--H", type=int, default=WORKLOAD["H"])
     ap.add_argument("--N", type=int, default=WORKLOAD["N"])

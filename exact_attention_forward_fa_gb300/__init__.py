@@ -28,9 +28,13 @@ FA_ERR_TIMEOUT = 6
 FA_BF16 = 0
 FA_FP16 = 1
 
+FA_SCALE_TILE = 0
+FA_SCALE_HEAD = 1
+FA_SCALE_TENSOR = 2
+
 # Every symbol include/fa.h declares (checked by the tests).
 EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_packed", "fa_fwd_ext", "fa_fwd_splitkv", "fa_splitkv_workspace_floats",
-           "fa_splitkv_auto", "fa_quantize_fp8", "fa_fwd_fp8", "fa_bwd", "fa_bwd_ext", "fa_bwd_noalloc",
+           "fa_splitkv_auto", "fa_quantize_fp8", "fa_quantize_fp8_granular", "fa_fwd_fp8", "fa_bwd", "fa_bwd_ext", "fa_bwd_noalloc",
            "fa_check_status", "fa_status_detail", "fa_selftest_wait_timeout",
            "fa_status_string", "fa_version")
 
@@ -70,6 +74,8 @@ def load():
     lib.fa_splitkv_auto.restype = i
     lib.fa_quantize_fp8.argtypes = [vp, vp, vp, vp, i, i, i, i, vp]
     lib.fa_quantize_fp8.restype = i
+    lib.fa_quantize_fp8_granular.argtypes = [vp, vp, vp, vp, i, i, i, i, i, vp]
+    lib.fa_quantize_fp8_granular.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd_fp8.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
@@ -236,13 +242,27 @@ def fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B: int, H: int,
                              int(d), float(alpha), int(causal), _stream(stream))
 
 
-def quantize_fp8(x, hadamard_signs=None, stream=None):
-    """bf16 [B,N,H,d] on the GPU -> (uint8 e4m3 codes, float scales [B,H,ceil(N/128)])."""
+def fa_quantize_fp8_granular(x, x8, scales, hadamard_signs, B: int, H: int, N: int,
+                             d: int, granularity: int, stream=None) -> int:
+    """Direct call of the C entry point (see include/fa.h)."""
+    return load().fa_quantize_fp8_granular(_ptr(x), _ptr(x8), _ptr(scales),
+                                           _ptr(hadamard_signs), int(B), int(H), int(N),
+                                           int(d), int(granularity), _stream(stream))
+
+
+def quantize_fp8(x, hadamard_signs=None, stream=None, granularity: int = FA_SCALE_TILE):
+    """bf16 [B,N,H,d] on the GPU -> (uint8 e4m3 codes, float scales [B,H,ceil(N/128)]);
+    ``granularity`` FA_SCALE_HEAD / FA_SCALE_TENSOR give one scale per head /
+    per tensor, repeated over the tiles."""
     import torch
     B, N, H, d = x.shape
     x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
     sc = torch.empty((B, H, (N + 127) // 128), dtype=torch.float32, device=x.device)
-    rc = fa_quantize_fp8(x, x8, sc, hadamard_signs, B, H, N, d, stream)
+    if granularity == FA_SCALE_TILE:
+        rc = fa_quantize_fp8(x, x8, sc, hadamard_signs, B, H, N, d, stream)
+    else:
+        rc = fa_quantize_fp8_granular(x, x8, sc, hadamard_signs, B, H, N, d, granularity,
+                                      stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_quantize_fp8")
     return x8, sc

@@ -32,6 +32,24 @@ DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 uint32_t g_last_detail[4] = {0, 0, 0, 0};
 
+// The workspace of fa_bwd_noalloc: a file-scope device array in the
+// library's image, for callers that must not allocate device memory at the
+// point of the call (a program whose device memory is reserved up front, a
+// runtime that forbids allocation once a step has started).  Every device
+// that loads the library holds its own copy until the process exits.  It
+// bounds the problem: 2 * B * H * ceil(N/128) * 128 floats (D and LSE*log2 e,
+// padded to whole tiles) must fit in 4 Mi floats (16 MiB).  Every element
+// the backward reads is first written by its preprocess in the same call,
+// so nothing needs to start at zero.  All calls on a device share the
+// array: calls that overlap in time (other streams, other host threads)
+// race on it.  Its device address is resolved once per device, on the first
+// call with that device current, and cached; after a cudaDeviceReset the
+// cached address is stale, so the entry point must not be used after one in
+// the same process.
+constexpr size_t kNoallocWorkspaceFloats = size_t(1) << 22;
+static __device__ __align__(256) float g_noalloc_workspace[kNoallocWorkspaceFloats];
+float *g_noalloc_ptr[kMaxDevices] = {};
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
                                   const cuuint32_t *, CUtensorMapInterleave,
@@ -382,10 +400,11 @@ fa_status fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, f
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
-                          const float *hadamard_signs, int B, int H, int N, int d,
-                          void *stream) {
+static fa_status quantize_impl(const void *x, uint8_t *x8, float *scales,
+                               const float *hadamard_signs, int B, int H, int N, int d,
+                               int granularity, void *stream) {
     if (!x || !x8 || !scales) return FA_ERR_INVALID_ARG;
+    if (granularity < FA_SCALE_TILE || granularity > FA_SCALE_TENSOR) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(x8)) return FA_ERR_MISALIGNED;
@@ -400,6 +419,7 @@ fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
     fa_status st = get_device(&dev);
     if (st != FA_OK) return st;
     fa::QuantLaunch L;
+    std::memset(&L, 0, sizeof(L));
     // one TMA box is a whole 128-row tile: {d, 1, 128, 1}, no swizzle
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
@@ -422,9 +442,22 @@ fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
     L.args.total = static_cast<int>(static_cast<uint64_t>(B) * H * n_tiles);
     L.d = d;
     L.sm_count = dev->sm_count;
+    L.granularity = granularity;
     L.stream = static_cast<cudaStream_t>(stream);
     cudaError_t e = fa::launch_quantize(L);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
+                          const float *hadamard_signs, int B, int H, int N, int d,
+                          void *stream) {
+    return quantize_impl(x, x8, scales, hadamard_signs, B, H, N, d, FA_SCALE_TILE, stream);
+}
+
+fa_status fa_quantize_fp8_granular(const void *x, uint8_t *x8, float *scales,
+                                   const float *hadamard_signs, int B, int H, int N, int d,
+                                   int granularity, void *stream) {
+    return quantize_impl(x, x8, scales, hadamard_signs, B, H, N, d, granularity, stream);
 }
 
 fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
@@ -586,28 +619,20 @@ fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
                     window_left, window_right, softcap, sinks, dsinks, dtype, stream);
 }
 
-// ---------------------------------------------------------------------------
-// fa_bwd_noalloc: fa_bwd with a workspace that lives in the library image.
-// For callers that must not allocate device memory at the point of the call
-// (for example a host program whose device memory is reserved up front, or
-// a runtime that forbids allocation once a step has started); they still get
-// the backward without passing a workspace.  The workspace is a file-scope
-// device array of kNoallocWorkspaceFloats floats (16 MiB), which bounds the
-// problem: 2 * B * H * ceil(N/128) * 128 floats must fit.  Every element the
-// backward reads is first written by its preprocess in the same call, so
-// nothing needs to start at zero.  One array per device is shared by all
-// calls: calls that overlap in time (other streams, other host threads)
-// race on it.
-// ---------------------------------------------------------------------------
-constexpr size_t kNoallocWorkspaceFloats = size_t(1) << 22;
-static __device__ __align__(256) float g_noalloc_workspace[kNoallocWorkspaceFloats];
-float *g_noalloc_ptr[kMaxDevices] = {};
-
+// fa_bwd_noalloc: fa_bwd with the workspace taken from the library's own
+// device array (g_noalloc_workspace, declared at the top of this file).
 fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
                          const void *dout, const float *lse, void *dq, void *dk, void *dv, int B,
                          int H, int N, int d, float alpha, int causal, fa_dtype dtype,
                          void *stream) {
-    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    // The arguments fa_bwd would reject come first, so the codes match
+    // fa_bwd's; only then the limit of the library's array.
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
     const uint64_t need = 2ull * B * H * ((static_cast<uint64_t>(N) + 127) / 128) * 128;
     if (need > kNoallocWorkspaceFloats) return FA_ERR_TOO_LARGE;
     int dev = 0;

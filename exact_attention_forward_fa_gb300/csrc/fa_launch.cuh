@@ -73,6 +73,7 @@ struct QuantArgs {
     uint8_t *x8;            // e4m3 codes, [B][N][H][d]
     float *scales;          // [B][H][n_tiles]
     const float *signs;     // +-1 diagonal of the rotation, or null
+    const float *scale_in;  // given per-tile scales (kGiven pass), else unused
     uint32_t *status;       // device status word
     int B, H, N, n_tiles, total;   // total = B * H * n_tiles
 };
@@ -81,6 +82,7 @@ struct QuantLaunch {
     QuantArgs args;
     int d;
     int sm_count;
+    int granularity;        // 0 per 128-row tile, 1 per head, 2 per tensor
     cudaStream_t stream;
 };
 cudaError_t launch_quantize(const QuantLaunch &L);

@@ -17,6 +17,14 @@
 // shared memory; scale = amax / 448 (1 for an all-zero tile); codes =
 // e4m3(y * (1 / scale)), the FP32 reciprocal formed once per tile (within
 // one rounding of y / scale), round to nearest even with saturation.
+//
+// Coarser scales (the control of the FA3 numerical-error ablation, "without
+// block quantization"): one scale per head or per tensor.  Three launches:
+// the per-tile pass above, a reduction of its scales to their maximum over
+// each head (or the whole tensor), written back to every tile of the group,
+// and the same pass again with those scales given (kGiven), which rewrites
+// the codes.  The maximum of the per-tile scales is the group's amax / 448
+// exactly: x -> fl(x / 448) is monotonic.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -64,7 +72,7 @@ __device__ __forceinline__ void unpack_bf16(const typename RawWord<E>::type &w, 
     }
 }
 
-template <int D, bool kRot>
+template <int D, bool kRot, bool kGiven>
 __global__ void __launch_bounds__(256, QuantCfg<D>::min_blocks(kRot))
 fa_quantize_kernel(const __grid_constant__ CUtensorMap tm_x, const QuantArgs a) {
     using C = QuantCfg<D>;
@@ -178,9 +186,10 @@ fa_quantize_kernel(const __grid_constant__ CUtensorMap tm_x, const QuantArgs a) 
         float tmax = wa[0];
 #pragma unroll
         for (int i = 1; i < 8; ++i) tmax = fmaxf(tmax, wa[i]);
-        const float scale = tmax > 0.f ? tmax / 448.f : 1.f;
+        float scale = tmax > 0.f ? tmax / 448.f : 1.f;
+        if constexpr (kGiven) scale = a.scale_in[static_cast<size_t>(bh) * a.n_tiles + tn];
         const float inv = 1.f / scale;
-        if (tid == 0) a.scales[static_cast<size_t>(bh) * a.n_tiles + tn] = scale;
+        if (!kGiven && tid == 0) a.scales[static_cast<size_t>(bh) * a.n_tiles + tn] = scale;
 
 #pragma unroll
         for (int rr = 0; rr < ROWS; ++rr) {
@@ -213,10 +222,10 @@ fa_quantize_kernel(const __grid_constant__ CUtensorMap tm_x, const QuantArgs a) 
     }
 }
 
-template <int D, bool kRot>
+template <int D, bool kRot, bool kGiven>
 static cudaError_t launch_quantize_d(const QuantLaunch &L) {
     using C = QuantCfg<D>;
-    auto kern = fa_quantize_kernel<D, kRot>;
+    auto kern = fa_quantize_kernel<D, kRot, kGiven>;
     static unsigned long long configured = 0ull;   // bit per device id (< 64)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -233,11 +242,45 @@ static cudaError_t launch_quantize_d(const QuantLaunch &L) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_quantize(const QuantLaunch &L) {
+template <bool kGiven>
+static cudaError_t launch_quantize_pass(const QuantLaunch &L) {
     const bool rot = L.args.signs != nullptr;
-    if (L.d == 64) return rot ? launch_quantize_d<64, true>(L) : launch_quantize_d<64, false>(L);
-    if (L.d == 128) return rot ? launch_quantize_d<128, true>(L) : launch_quantize_d<128, false>(L);
-    return rot ? launch_quantize_d<256, true>(L) : launch_quantize_d<256, false>(L);
+    if (L.d == 64)
+        return rot ? launch_quantize_d<64, true, kGiven>(L) : launch_quantize_d<64, false, kGiven>(L);
+    if (L.d == 128)
+        return rot ? launch_quantize_d<128, true, kGiven>(L) : launch_quantize_d<128, false, kGiven>(L);
+    return rot ? launch_quantize_d<256, true, kGiven>(L) : launch_quantize_d<256, false, kGiven>(L);
+}
+
+// One CTA per group of n consecutive scales: all of them become the
+// group's maximum.
+__global__ void __launch_bounds__(256)
+fa_scale_group_max_kernel(float *scales, long long n) {
+    __shared__ float part[8];
+    float *g = scales + static_cast<long long>(blockIdx.x) * n;
+    float m = 0.f;
+    for (long long i = threadIdx.x; i < n; i += 256) m = fmaxf(m, g[i]);
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = part[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, part[i]);
+    for (long long i = threadIdx.x; i < n; i += 256) g[i] = m;
+}
+
+cudaError_t launch_quantize(const QuantLaunch &L) {
+    cudaError_t e = launch_quantize_pass<false>(L);
+    if (e != cudaSuccess || L.granularity == 0) return e;
+    // one group per head, or one for the whole tensor
+    const long long groups = L.granularity == 1 ? static_cast<long long>(L.args.B) * L.args.H : 1;
+    const long long n = static_cast<long long>(L.args.total) / groups;
+    fa_scale_group_max_kernel<<<static_cast<unsigned>(groups), 256, 0, L.stream>>>(L.args.scales, n);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    QuantLaunch G = L;
+    G.args.scale_in = L.args.scales;
+    return launch_quantize_pass<true>(G);
 }
 
 }  // namespace fa

@@ -59,6 +59,13 @@ typedef enum {
     FA_FP16 = 1
 } fa_dtype;
 
+/* Scale granularity of the FP8 pre-pass (fa_quantize_fp8_granular). */
+typedef enum {
+    FA_SCALE_TILE = 0,    /* one scale per 128-row tile of a head (block quantization) */
+    FA_SCALE_HEAD = 1,    /* one scale per (batch, head) */
+    FA_SCALE_TENSOR = 2   /* one scale for the whole tensor */
+} fa_scale_granularity;
+
 /*
  * fa_fwd -- exact attention forward, BF16 or FP16 in and out.
  *   q, k, v : device, [B][N][H][d] in `dtype`, 16-byte aligned.
@@ -188,6 +195,25 @@ fa_status fa_quantize_fp8(const void *x, uint8_t *x8, float *scales,
                           void *stream);
 
 /*
+ * fa_quantize_fp8_granular -- fa_quantize_fp8 with a coarser scale: the
+ * control arm of the FA3 FP8 numerical-error ablation, which compares block
+ * quantization against one scale per tensor (the FlashAttention-3 review on
+ * diycv.top, "numerical error"; "FlashAttention-3 on Hopper", sec. 6.3).
+ *   granularity : FA_SCALE_TILE (exactly fa_quantize_fp8), FA_SCALE_HEAD
+ *            (scale = amax / 448 over each (b, h)), or FA_SCALE_TENSOR (over
+ *            the whole tensor); other values give FA_ERR_INVALID_ARG.
+ *   scales : written in the per-tile layout [B][H][ceil(N/128)] whatever
+ *            the granularity (every tile of a group holds the group's
+ *            scale), so fa_fwd_fp8 consumes them unchanged.
+ * Coarser granularities run three kernels on `stream` (the per-tile pass,
+ * a maximum over each group of its tile scales, and the pass again with
+ * those scales).  Other arguments, results and errors as fa_quantize_fp8.
+ */
+fa_status fa_quantize_fp8_granular(const void *x, uint8_t *x8, float *scales,
+                                   const float *hadamard_signs, int B, int H, int N,
+                                   int d, int granularity, void *stream);
+
+/*
  * fa_fwd_fp8 -- attention forward on e4m3 Q/K/V with per-tile scales
  * (as written by fa_quantize_fp8), bf16 output ("FlashAttention-3 on
  * Hopper", sec. 6.3: descales folded into the softmax scale per tile
@@ -273,12 +299,17 @@ fa_status fa_bwd_ext(const void *q, const void *k, const void *v, const void *o,
  * For callers that must not allocate device memory at the point of the
  * call, e.g. a program whose device memory is reserved up front or a
  * runtime that forbids allocation inside a step.  The workspace is a
- * 16 MiB array in the library's device image (one per device, resolved
- * once per device); nothing is allocated, and nothing in it needs to start
- * at zero.  Limit: 2 * B * H * ceil(N/128) * 128 <= 4194304 floats, else
- * FA_ERR_TOO_LARGE before anything runs.  Calls that overlap in time (on
- * other streams or host threads) share the array and race; serialise them.
- * Other arguments, results and errors as fa_bwd.
+ * 16 MiB array in the library's device image (one per device that loads
+ * the library, held until the process exits); nothing is allocated, and
+ * nothing in it needs to start at zero.  Limit: 2 * B * H * ceil(N/128) *
+ * 128 <= 4194304 floats, else FA_ERR_TOO_LARGE before anything runs; the
+ * arguments fa_bwd rejects are checked first and give fa_bwd's codes.
+ * Calls that overlap in time (on other streams or host threads) share the
+ * array and race; serialise them.  The array's device address is looked up
+ * on the first call on each device (with that device current) and cached,
+ * so make that first call before any stream capture, and do not call this
+ * after a cudaDeviceReset in the same process (the cached address would be
+ * stale).  Other arguments, results and errors as fa_bwd.
  */
 fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v,
                          const void *o, const void *dout, const float *lse,

@@ -139,8 +139,13 @@ int oracle_attention_head(const double *q, const double *k, const double *v,
 
 /* ------------------------------------------------------------------------ */
 /* Whole tensors, [B][N][H][d] for Q/K/V/O and [B][H][N] for LSE, threaded   */
-/* over (b, h) pairs.  Each pair is independent ([FA3H] sec. 3.4.2).         */
+/* over (b, h, block of FWD_ROWS query rows).  Rows are independent          */
+/* ([FA3H] sec. 3.4.2), and each row is computed by attention_row alone, so  */
+/* the split changes no bit of the result; it only keeps every core busy     */
+/* when B * H is small (one long sequence of few heads).                     */
 /* ------------------------------------------------------------------------ */
+
+#define FWD_ROWS 256
 
 typedef struct {
     const double *q, *k, *v;
@@ -159,14 +164,21 @@ static void *fwd_worker(void *arg)
         pthread_mutex_lock(&J->mu);
         int u = J->next++;
         pthread_mutex_unlock(&J->mu);
-        if (u >= J->B * J->H) break;
-        int b = u / J->H, h = u % J->H;
+        const int nblk = (J->N + FWD_ROWS - 1) / FWD_ROWS;
+        if (u >= J->B * J->H * nblk) break;
+        int blk = u % nblk, bh = u / nblk;
+        int b = bh / J->H, h = bh % J->H;
         long ld = (long)J->H * J->d;
         long off = ((long)b * J->N * J->H + h) * J->d;
+        int r0 = blk * FWD_ROWS;
+        int nr = J->N - r0 < FWD_ROWS ? J->N - r0 : FWD_ROWS;
+        int rows[FWD_ROWS];
+        for (int t = 0; t < nr; ++t) rows[t] = r0 + t;
+        /* rows r0 .. r0+nr-1 are written at o + (r0 + t) ld, lse[r0 + t] */
         int rc = oracle_attention_head(J->q + off, J->k + off, J->v + off,
                                        J->N, J->N, J->d, ld, ld, ld, J->alpha,
-                                       J->causal, NULL, 0, J->o + off, ld,
-                                       J->lse + ((long)b * J->H + h) * J->N,
+                                       J->causal, rows, nr, J->o + off + (long)r0 * ld, ld,
+                                       J->lse + ((long)b * J->H + h) * J->N + r0,
                                        NULL);
         if (rc) {
             pthread_mutex_lock(&J->mu);

@@ -169,6 +169,22 @@ def test_quantize_validation_codes(lib, kw, code):
     assert _qcall(lib, **kw) == code
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), fa.FA_ERR_INVALID_ARG),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(sc=A + 2), fa.FA_ERR_MISALIGNED),
+    (dict(g=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(g=3), fa.FA_ERR_INVALID_ARG),
+])
+def test_quantize_granular_validation_codes(lib, kw, code):
+    g = kw.pop("g", fa.FA_SCALE_TENSOR)
+    args = dict(x=A, x8=A, sc=A, signs=None, B=1, H=1, N=128, d=128)
+    args.update(kw)
+    assert lib.fa_quantize_fp8_granular(args["x"], args["x8"], args["sc"], args["signs"],
+                                        args["B"], args["H"], args["N"], args["d"], g,
+                                        None) == code
+
+
 def _f8call(lib, q=A, k=A, v=A, qs=A, ks=A, vs=A, o=A, lse=None, B=1, H=1, N=128, d=128,
             alpha=0.088, causal=0):
     return lib.fa_fwd_fp8(q, k, v, qs, ks, vs, o, lse, B, H, N, d, alpha, causal, None)
@@ -244,10 +260,16 @@ def test_bwd_ext_validation_codes(lib, kw, code):
 
 def test_bwd_noalloc_rejects_problems_beyond_its_workspace(lib):
     # 2 * B * H * ceil(N/128) * 128 floats must fit the 4 Mi-float array;
-    # the check comes before any CUDA call.
+    # the check comes before any CUDA call, after the arguments fa_bwd
+    # itself rejects (which keep fa_bwd's codes).
     args = [A] * 9
     assert lib.fa_bwd_noalloc(*args, 1, 16, 131073, 128, 0.088, 0, 0, None) == fa.FA_ERR_TOO_LARGE
     assert lib.fa_bwd_noalloc(*args, 0, 1, 128, 128, 0.088, 0, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_bwd_noalloc(*args, 1, 16, 131073, 256, 0.088, 0, 0, None) == fa.FA_ERR_UNSUPPORTED
+    assert lib.fa_bwd_noalloc(*args, 1, 16, 131073, 128, 0.088, 2, 0, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_bwd_noalloc(*args, 1, 16, 131073, 128, 0.088, 0, 7, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_bwd_noalloc(None, *args[1:], 1, 16, 131073, 128, 0.088, 0, 0,
+                              None) == fa.FA_ERR_INVALID_ARG
 
 
 def test_valid_call_without_gpu_reports_cuda_error(lib):

@@ -33,12 +33,33 @@ pytestmark = pytest.mark.gpu
 THREADS = os.cpu_count() or 4
 
 
-def _quant(fa, x, signs):
+def _quant(fa, x, signs, granularity=0):
     dev = torch.device("cuda")
     s = None if signs is None else torch.from_numpy(signs).to(dev)
-    x8, sc = fa.quantize_fp8(x.to(dev), s)
+    x8, sc = fa.quantize_fp8(x.to(dev), s, granularity=granularity)
     assert fa.fa_check_status() == fa.FA_OK
     return x8.cpu().numpy(), sc.cpu().numpy()
+
+
+def _check_codes(got, xh, y, scale_rows, rotate):
+    """Codes of one head against the oracle's e4m3 encoding, given the
+    per-row scales the kernel used (float32 [rows, 1])."""
+    if not rotate:
+        # Same decision in the kernel's precision: the FP32 product
+        # x * (1 / scale), then round-to-nearest-even to e4m3 -> bit exact.
+        inv = np.float32(1.0) / scale_rows
+        q32 = (xh.astype(np.float32) * inv).astype(np.float64)
+        assert np.array_equal(got, oracle.e4m3_encode(q32))
+    else:
+        # The rotated values carry FP32 butterfly rounding: the code is the
+        # RNE code of y/scale, or a neighbour where y/scale lies within
+        # 2^-18 of a rounding boundary.
+        v = y / scale_rows.astype(np.float64)
+        lo = oracle.e4m3_encode(v * (1 - 2.0 ** -18) - 2.0 ** -40)
+        hi = oracle.e4m3_encode(v * (1 + 2.0 ** -18) + 2.0 ** -40)
+        mid = oracle.e4m3_encode(v)
+        ok = (got == mid) | (got == lo) | (got == hi)
+        assert np.all(ok), np.argwhere(~ok)[:5]
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
@@ -55,24 +76,39 @@ def test_quantize_matches_oracle(gpu_lib, d, rotate):
             codes_ref, sc_ref = oracle.quantize_e4m3_tiles(y, 128)
             rel = np.abs(sc[b, h] - sc_ref) / sc_ref
             assert np.all(rel <= (2.0 ** -20 if rotate else 0.0)), rel.max()
-            got = x8[b, :, h, :]
             scale_rows = np.repeat(sc[b, h], 128)[:N, None]          # float32
-            if not rotate:
-                # Same decision in the kernel's precision: the FP32 product
-                # x * (1 / scale), then round-to-nearest-even to e4m3 -> bit exact.
-                inv = np.float32(1.0) / scale_rows
-                q32 = (xh.astype(np.float32) * inv).astype(np.float64)
-                assert np.array_equal(got, oracle.e4m3_encode(q32))
+            _check_codes(x8[b, :, h, :], xh, y, scale_rows, rotate)
+
+
+@pytest.mark.parametrize("granularity", ["head", "tensor"])
+@pytest.mark.parametrize("rotate", [False, True])
+def test_quantize_granular_matches_oracle(gpu_lib, granularity, rotate):
+    # One scale per head (the oracle's block quantization with one tile of
+    # N rows) or per tensor (one tile of all B N H rows: the maximum is
+    # order-free), repeated over the per-tile layout.
+    fa = gpu_lib
+    B, H, N, d = 2, 3, 300, 128
+    g = fa.FA_SCALE_HEAD if granularity == "head" else fa.FA_SCALE_TENSOR
+    x = torch.from_numpy(synth.normal((B, N, H, d), seed=91, outliers=True)).to(torch.bfloat16)
+    signs = synth.hadamard_signs(d, seed=6) if rotate else None
+    x8, sc = _quant(fa, x, signs, g)
+    xd = x.double().numpy()
+    y = oracle.hadamard_rotate(xd, signs) if rotate else xd
+    tol = 2.0 ** -20 if rotate else 0.0
+    if g == fa.FA_SCALE_TENSOR:
+        _, s_all = oracle.quantize_e4m3_tiles(y.reshape(-1, d), B * N * H)
+    for b in range(B):
+        for h in range(H):
+            if g == fa.FA_SCALE_HEAD:
+                _, s_ref = oracle.quantize_e4m3_tiles(y[b, :, h, :], N)
             else:
-                # The rotated values carry FP32 butterfly rounding: the code
-                # is the RNE code of y/scale, or a neighbour where y/scale
-                # lies within 2^-18 of a rounding boundary.
-                v = y / scale_rows.astype(np.float64)
-                lo = oracle.e4m3_encode(v * (1 - 2.0 ** -18) - 2.0 ** -40)
-                hi = oracle.e4m3_encode(v * (1 + 2.0 ** -18) + 2.0 ** -40)
-                mid = oracle.e4m3_encode(v)
-                ok = (got == mid) | (got == lo) | (got == hi)
-                assert np.all(ok), np.argwhere(~ok)[:5]
+                s_ref = s_all
+            assert s_ref.shape == (1,)
+            rel = np.abs(sc[b, h] - s_ref[0]) / s_ref[0]
+            assert np.all(rel <= tol), rel.max()
+            assert np.all(sc[b, h] == sc[b, h, 0])
+            scale_rows = np.repeat(sc[b, h], 128)[:N, None]
+            _check_codes(x8[b, :, h, :], xd[b, :, h, :], y[b, :, h, :], scale_rows, rotate)
 
 
 def test_quantize_e4m3_ties_round_to_even(gpu_lib):
@@ -90,12 +126,12 @@ def test_quantize_e4m3_ties_round_to_even(gpu_lib):
     assert np.array_equal(x8.reshape(-1)[:len(ties)], oracle.e4m3_encode(ties))
 
 
-def _fp8_run(fa, q, k, v, causal, signs):
+def _fp8_run(fa, q, k, v, causal, signs, granularity=0):
     dev = torch.device("cuda")
     s = None if signs is None else torch.from_numpy(signs).to(dev)
-    q8, qs = fa.quantize_fp8(q.to(dev), s)
-    k8, ks = fa.quantize_fp8(k.to(dev), s)
-    v8, vs = fa.quantize_fp8(v.to(dev), None)
+    q8, qs = fa.quantize_fp8(q.to(dev), s, granularity=granularity)
+    k8, ks = fa.quantize_fp8(k.to(dev), s, granularity=granularity)
+    v8, vs = fa.quantize_fp8(v.to(dev), None, granularity=granularity)
     d = q.shape[-1]
     o, lse = fa.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, alpha=synth.default_alpha(d))
     assert fa.fa_check_status() == fa.FA_OK
@@ -150,18 +186,44 @@ def test_fp8_kernel_against_dequantized_inputs(gpu_lib, B, H, N, causal):
     assert np.abs(lse - lse_deq).max() < 5e-2
 
 
-def test_fp8_full_size_sampled_rmse(gpu_lib):
-    # B4 H16 N4096 d128 with outliers, in the bench's launch configuration.
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_full_size_rmse_every_element(gpu_lib, causal):
+    # B4 H16 N4096 d128 with outliers, in the bench's launch configuration:
+    # RMSE over every O element against FP64 attention on the unquantized
+    # inputs, the metric of the FA3 numerical-error experiment.
     B, H, N, d = 4, 16, 4096, 128
     q, k, v = synth.qkv(B, H, N, d, seed=synth.BASE_SEED, outliers=True)
-    o, _, _ = _fp8_run(gpu_lib, q, k, v, False, synth.hadamard_signs(d))
+    o, _, _ = _fp8_run(gpu_lib, q, k, v, causal, synth.hadamard_signs(d))
     a = synth.default_alpha(d)
-    rng = np.random.default_rng(9)
-    sq = []
-    for b, h in [(0, 0), (3, 15), (1, 7), (2, 3)]:
-        rows = sorted(rng.choice(N, 48, replace=False).tolist())
-        o_ref, _ = oracle.attention_rows(q, k, v, a, False, b, h, rows)
-        sq.append((o[b, rows, h, :] - o_ref) ** 2)
-    rmse = float(np.sqrt(np.mean(np.concatenate(sq))))
-    print(f"FP8 sampled RMSE B4 H16 N4096 d128: {rmse:.3e}")
+    o_ref, _ = oracle.attention(q, k, v, a, causal, n_threads=THREADS)
+    assert np.all(np.isfinite(o))
+    rmse = float(np.sqrt(np.mean((o - o_ref) ** 2)))
+    print(f"FP8 RMSE B4 H16 N4096 d128 causal={causal} (all elements): {rmse:.3e}")
     assert rmse <= 1.5e-2
+
+
+def test_fp8_ablation_block_scales_and_rotation(gpu_lib):
+    # The FA3 numerical-error ablation (the FlashAttention-3 review on
+    # diycv.top, "numerical error"): O RMSE against FP64 attention on the
+    # unquantized outlier inputs for block scales vs one scale per tensor,
+    # each with and without the Hadamard rotation, at B4 H16 N4096 d128.
+    # The pages report 9.1e-3 (block + rotation) < 9.3e-3 (per tensor +
+    # rotation) < 2.4e-2 (no rotation); the same ordering must hold here.
+    fa = gpu_lib
+    B, H, N, d = 4, 16, 4096, 128
+    q, k, v = synth.qkv(B, H, N, d, seed=synth.BASE_SEED, outliers=True)
+    a = synth.default_alpha(d)
+    o_ref, _ = oracle.attention(q, k, v, a, False, n_threads=THREADS)
+    rm = {}
+    for name, g in (("block", fa.FA_SCALE_TILE), ("tensor", fa.FA_SCALE_TENSOR)):
+        for rot in (True, False):
+            o, _, _ = _fp8_run(fa, q, k, v, False, synth.hadamard_signs(d) if rot else None, g)
+            assert np.all(np.isfinite(o))
+            rm[(name, rot)] = float(np.sqrt(np.mean((o - o_ref) ** 2)))
+    print("FP8 ablation RMSE: " + ", ".join(
+        f"{n}{'+rot' if r else ''} {x:.3e}" for (n, r), x in rm.items()))
+    assert rm[("block", True)] <= 1.5e-2
+    assert rm[("block", True)] < rm[("block", False)]
+    assert rm[("tensor", True)] < rm[("tensor", False)]
+    assert rm[("block", True)] < rm[("tensor", True)]
+    assert rm[("block", False)] < rm[("tensor", False)]

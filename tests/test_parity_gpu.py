@@ -2,10 +2,12 @@
 
 Tolerances (stated for unit-variance inputs): O max-abs <= 1e-2, O RMSE
 <= 2e-3, LSE max-abs <= 1e-3.  Small and ragged shapes are compared element
-by element in full; the full-size workloads (B4 H16 N4096 d128 and the
-16k-token sequence sweep) are compared on sampled (b, h, row) outputs that
-the oracle computes one by one, in the same launch configuration the bench
-times.  Exact pins: causal row 0 reproduces V[0] bit for bit, a constant V
+by element in full.  At full size, the N = 4096 and N = 16384 points of the
+16k-token sequence sweep (B = 16384 / N; d = 64, 128, 256; plain and causal)
+are compared element by element on every O and LSE value; N = 4096, d = 128
+is the bench's own workload (same seed, same launch configuration).  The
+other sweep points are compared on sampled (b, h, row) outputs that the
+oracle computes one by one.  Exact pins: causal row 0 reproduces V[0] bit for bit, a constant V
 gives that constant, and two launches give identical bits.
 """
 import os
@@ -108,6 +110,23 @@ def _sampled(fa, B, H, N, d, causal, n_heads=3, n_rows=24, seed=0):
 
 def test_sampled_b4_h16_n4096_d128(gpu_lib):
     _sampled(gpu_lib, 4, 16, 4096, 128, False)
+
+
+# Every element at full size: the N = 4096 and N = 16384 points of the sweep
+# at each head dim (hidden 2048, 16k tokens), plain and causal.
+FULL_SIZE = [(n, d, h, c) for n in (4096, 16384)
+             for (d, h) in ((64, 32), (128, 16), (256, 8)) for c in (False, True)]
+
+
+@pytest.mark.parametrize("N,d,H,causal", FULL_SIZE)
+def test_full_size_every_element(gpu_lib, N, d, H, causal):
+    B = 16384 // N
+    q, k, v = synth.qkv(B, H, N, d, seed=synth.BASE_SEED)
+    alpha = synth.default_alpha(d)
+    o, lse = _run(gpu_lib, q, k, v, causal, alpha)
+    o_ref, lse_ref = oracle.attention(q, k, v, alpha, causal, n_threads=THREADS)
+    mx, rmse = _check(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref)
+    print(f"full B{B} H{H} N{N} d{d} causal={causal}: O max-abs {mx:.3e} rmse {rmse:.3e}")
 
 
 SWEEP = [(n, d, h, c) for n in (512, 1024, 2048, 4096, 8192, 16384)
