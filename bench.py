@@ -16,8 +16,9 @@ the device->host copy of O and LSE, every step.  ``cpu_baseline`` is the
 FP64 CPU oracle on a bounded sample of the same workload.
 ``--impl reference`` times that oracle alone, as the reference arm.
 The default run (one GPU, the workload above) also times, in the same
-process, the causal mask, d = 64 and d = 256 at N = 4096, the FP8 workload
-(kernel and pre-pass apart), the backward, and a sustained run of >= 1.2 s,
+process, the causal mask, d = 64 and d = 256 at N = 4096 (and d = 256 at
+N = 16384), the FP8 workloads at d = 128 and d = 256 (kernel and pre-pass
+apart), the backward, and a sustained run of >= 1.2 s,
 each under ``also_measured`` with its own roofline fraction and clocks
 (``--no-extra`` skips them).
 ``--fp8`` times the FP8 forward (the quantization pre-pass reported
@@ -43,7 +44,7 @@ sys.path.insert(0, ROOT)
 
 PEAK_SPEC = 2250.0          # TFLOP/s dense BF16, the metric's denominator
 METRIC = "attention fwd TFLOP/s (BF16, d=128) and % of 2250 TFLOP/s dense peak"
-METRIC_FP8 = "attention fwd TFLOP/s (FP8 e4m3, d=128) and % of 4500 TFLOP/s dense FP8 peak"
+METRIC_FP8 = "attention fwd TFLOP/s (FP8 e4m3, d={d}) and % of 4500 TFLOP/s dense FP8 peak"
 PEAK_SPEC_FP8 = 4500.0
 METRIC_BWD = ("attention bwd TFLOP/s (BF16, d=128; FLOPs = 2.5 x forward) "
               "and % of 2250 TFLOP/s dense peak")
@@ -618,51 +619,64 @@ def extra_measurements(args, fa, dev, stream):
         entry(name, flops(B, H, N, d, causal), ms, n, clk, peak, kind,
               {"workload": config_name(B, H, N, d, causal), "timed_region_ms": ms * n})
 
+    def fp8_case(name, B, H, N, d):
+        # outlier inputs; Q and K rotated with per-tile scales, V per head
+        q, k, v = (x.to(dev) for x in synth.qkv(B, H, N, d, seed=synth.BASE_SEED, outliers=True))
+        signs = torch.from_numpy(synth.hadamard_signs(d)).to(dev)
+        nt = (N + 127) // 128
+        q8, k8, v8 = (torch.empty(q.shape, dtype=torch.uint8, device=dev) for _ in range(3))
+        qs, ks, vs = (torch.empty((B, H, nt), dtype=torch.float32, device=dev) for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        alpha = synth.default_alpha(d)
+
+        def quantize():
+            for x, x8, sc, sg, g in ((q, q8, qs, signs, fa.FA_SCALE_TILE),
+                                     (k, k8, ks, signs, fa.FA_SCALE_TILE),
+                                     (v, v8, vs, None, fa.FA_SCALE_HEAD)):
+                rc = fa.fa_quantize_fp8_granular(x, x8, sc, sg, B, H, N, d, g, sp)
+                if rc != fa.FA_OK:
+                    raise fa.FaError(rc, "fa_quantize_fp8")
+
+        def fp8():
+            rc = fa.fa_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, B, H, N, d, alpha, 0, sp)
+            if rc != fa.FA_OK:
+                raise fa.FaError(rc, "fa_fwd_fp8")
+        for _ in range(3):
+            quantize()
+        pre_ms, _, _ = _timed(quantize, 20, stream, dev)
+        for _ in range(max(3, args.warmup)):
+            fp8()
+        ms, n, clk = _timed(fp8, steps, stream, dev)
+        check(name)
+        # algorithmic bytes of the pre-pass: bf16 in, e4m3 out, one FP32
+        # scale per tile, for the three tensors
+        pre_bytes = 3 * (q.numel() * 3 + B * H * nt * 4)
+        entry(name, flops(B, H, N, d, False), ms, n, clk, 2 * burst,
+              "bf16 burst (cuBLAS 8192^3) x 2 (nominal FP8/BF16 ratio)",
+              {"workload": config_name(B, H, N, d, False, fp8=True), "timed_region_ms": ms * n,
+               "prepass": {"ms": pre_ms, "tensors": 3, "rotated": 2,
+                           "scales": "Q, K per 128-row tile; V per head",
+                           "algorithmic_bytes": pre_bytes,
+                           "achieved_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9,
+                           "hbm_frac": pre_bytes / (pre_ms * 1e-3) / 1e9 / measured_hbm()}})
+
     fwd_case("fwd_causal", 4, 16, 4096, 128, True)
     fwd_case("fwd_d64_n4096", 4, 32, 4096, 64, False)
     fwd_case("fwd_d256_n4096", 4, 8, 4096, 256, False)
     fwd_case("fwd_sustained", 4, 16, 4096, 128, False, min_ms=1200.0)
 
-    # FP8: outlier inputs, Q and K rotated, per-tile scales
-    B, H, N, d = 4, 16, 4096, 128
-    q, k, v = (x.to(dev) for x in synth.qkv(B, H, N, d, seed=synth.BASE_SEED, outliers=True))
-    signs = torch.from_numpy(synth.hadamard_signs(d)).to(dev)
-    nt = (N + 127) // 128
-    q8, k8, v8 = (torch.empty(q.shape, dtype=torch.uint8, device=dev) for _ in range(3))
-    qs, ks, vs = (torch.empty((B, H, nt), dtype=torch.float32, device=dev) for _ in range(3))
-    o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    alpha = synth.default_alpha(d)
-
-    def quantize():
-        for x, x8, sc, sg in ((q, q8, qs, signs), (k, k8, ks, signs), (v, v8, vs, None)):
-            rc = fa.fa_quantize_fp8(x, x8, sc, sg, B, H, N, d, sp)
-            if rc != fa.FA_OK:
-                raise fa.FaError(rc, "fa_quantize_fp8")
-
-    def fp8():
-        rc = fa.fa_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, B, H, N, d, alpha, 0, sp)
-        if rc != fa.FA_OK:
-            raise fa.FaError(rc, "fa_fwd_fp8")
-    for _ in range(3):
-        quantize()
-    pre_ms, _, _ = _timed(quantize, 20, stream, dev)
-    for _ in range(max(3, args.warmup)):
-        fp8()
-    ms, n, clk = _timed(fp8, steps, stream, dev)
-    check("fp8")
-    # bytes of the pre-pass: bf16 in, e4m3 out, one FP32 scale per tile
-    pre_bytes = 3 * (q.numel() * 3 + B * H * nt * 4)
-    entry("fwd_fp8", flops(B, H, N, d, False), ms, n, clk, 2 * burst,
-          "bf16 burst (cuBLAS 8192^3) x 2 (nominal FP8/BF16 ratio)",
-          {"workload": config_name(B, H, N, d, False, fp8=True), "timed_region_ms": ms * n,
-           "prepass": {"ms": pre_ms, "tensors": 3, "rotated": 2,
-                       "algorithmic_bytes": pre_bytes,
-                       "achieved_gbs": pre_bytes / (pre_ms * 1e-3) / 1e9,
-                       "hbm_frac": pre_bytes / (pre_ms * 1e-3) / 1e9 / measured_hbm()}})
-    del q8, k8, v8
+    for name, (B, H, N, d) in (("fwd_fp8", (4, 16, 4096, 128)),
+                               ("fwd_fp8_d256_n4096", (4, 8, 4096, 256)),
+                               ("fwd_fp8_d256_n16384", (1, 8, 16384, 256))):
+        fp8_case(name, B, H, N, d)
+    fwd_case("fwd_d256_n16384", 1, 8, 16384, 256, False)
 
     # backward (dQ, dK, dV from O, LSE, dO), FLOPs 2.5 x the forward's
+    B, H, N, d = 4, 16, 4096, 128
+    alpha = synth.default_alpha(d)
+    o = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     dout = torch.from_numpy(synth.normal((B, N, H, d), seed=synth.BASE_SEED + 3)).to(
         torch.bfloat16).to(dev)
     q, k, v = (x.to(dev) for x in synth.qkv(B, H, N, d, seed=synth.BASE_SEED))
@@ -740,8 +754,11 @@ def run_ours(args, B, H, N, d, rank, world):
         qs, ks, vs = (torch.empty((B, H, nt), dtype=torch.float32, device=dev) for _ in range(3))
 
     def quantize(q=q, k=k, v=v, sp=sp):
-        for x, x8, sc, sg in ((q, q8, qs, signs), (k, k8, ks, signs), (v, v8, vs, None)):
-            rc = fa.fa_quantize_fp8(x, x8, sc, sg, B, H, N, d, sp)
+        # Q, K: per-tile scales after the rotation; V: one scale per head
+        for x, x8, sc, sg, g in ((q, q8, qs, signs, fa.FA_SCALE_TILE),
+                                 (k, k8, ks, signs, fa.FA_SCALE_TILE),
+                                 (v, v8, vs, None, fa.FA_SCALE_HEAD)):
+            rc = fa.fa_quantize_fp8_granular(x, x8, sc, sg, B, H, N, d, g, sp)
             if rc != fa.FA_OK:
                 raise fa.FaError(rc, "fa_quantize_fp8")
 
@@ -885,7 +902,7 @@ def run_ours(args, B, H, N, d, rank, world):
         wkey += f" split-KV x{n_splits}"
     wkey += variant_suffix(var)
     line = {
-        "metric": METRIC_FP8 if args.fp8 else METRIC, "value": value, "unit": "TFLOP/s",
+        "metric": METRIC_FP8.format(d=d) if args.fp8 else METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -963,6 +980,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.bwd and args.fp8:
         ap.error("--bwd and --fp8 are exclusive")
+    if args.fp8 and args.d not in (128, 256):
+        ap.error("--fp8 needs --d 128 or 256")
     if args.hkv and (args.fp8 or args.H % args.hkv
                      or (args.bwd and variant_of(args) is None)):
         ap.error("--hkv must divide --H, not with --fp8; with --bwd it needs --window "

@@ -468,15 +468,17 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
-    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o)) return FA_ERR_MISALIGNED;
     if ((reinterpret_cast<uintptr_t>(q_scale) & 3u) || (reinterpret_cast<uintptr_t>(k_scale) & 3u) ||
         (reinterpret_cast<uintptr_t>(v_scale) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return FA_ERR_MISALIGNED;
     const uint64_t batch_stride = 1ull * d * H * static_cast<uint64_t>(N);
     if (batch_stride >= (1ull << 40)) return FA_ERR_TOO_LARGE;
+    // work units: pairs of 128-row Q tiles at d = 128, single Q tiles at
+    // d = 256 (whose O accumulator alone fills half of TMEM)
     const uint64_t n_qt = (static_cast<uint64_t>(N) + 127) / 128;
-    const uint64_t units = static_cast<uint64_t>(B) * H * ((n_qt + 1) / 2);
+    const uint64_t units = static_cast<uint64_t>(B) * H * (d == 256 ? n_qt : (n_qt + 1) / 2);
     if (units > 0x7fffffffull || static_cast<uint64_t>(B) * H * N > 0x7fffffffffffull)
         return FA_ERR_TOO_LARGE;
     DeviceInfo *dev = nullptr;
@@ -508,7 +510,7 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     L.stream = static_cast<cudaStream_t>(stream);
     L.causal = causal != 0;
     L.bf16 = true;
-    cudaError_t e = fa::launch_fwd_fp8(L);
+    cudaError_t e = d == 256 ? fa::launch_fwd_fp8_d256(L) : fa::launch_fwd_fp8(L);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -7,6 +7,7 @@
 
 #include "fa_bwd_kernel.cuh"
 #include "fa_fwd_1q_kernel.cuh"
+#include "fa_fwd_fp8_1q_kernel.cuh"
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -25,6 +26,7 @@ cudaError_t launch_fwd_d64(const FwdLaunch &L);
 cudaError_t launch_fwd_d128(const FwdLaunch &L);
 cudaError_t launch_fwd_d256(const FwdLaunch &L);   // K/V maps with 64-row boxes
 cudaError_t launch_fwd_fp8(const FwdLaunch &L);    // e4m3 maps, 128-byte boxes
+cudaError_t launch_fwd_fp8_d256(const FwdLaunch &L);   // the same at head dim 256
 cudaError_t launch_fwd_split(const FwdLaunch &L);  // split key ranges, d in {64, 128}
 cudaError_t launch_fwd_ext(const FwdLaunch &L);    // window / sinks, d in {64, 128}
 cudaError_t launch_fwd_ext_softcap(const FwdLaunch &L);   // the same with a softcap
@@ -114,6 +116,26 @@ template <int D, bool kCausal, bool kBF16>
 cudaError_t launch_fwd_1q_inst(const FwdLaunch &L) {
     using Cfg = Fwd1qCfg<D, kCausal, kBF16>;
     auto kern = fa_fwd_1q_kernel<D, kCausal, kBF16>;
+    static unsigned long long configured = 0ull;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(Cfg::SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        __atomic_fetch_or(&configured, bit, __ATOMIC_ACQ_REL);
+    }
+    kern<<<L.grid, Cfg::NTHREADS, Cfg::SMEM_BYTES, L.stream>>>(L.q, L.k, L.v, L.args);
+    return cudaGetLastError();
+}
+
+// Same, for the FP8 one-Q-tile kernel (head dim 256).
+template <int D, bool kCausal>
+cudaError_t launch_fwd_fp8_1q_inst(const FwdLaunch &L) {
+    using Cfg = Fp8Fwd1qCfg<D, kCausal>;
+    auto kern = fa_fwd_fp8_1q_kernel<D, kCausal>;
     static unsigned long long configured = 0ull;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

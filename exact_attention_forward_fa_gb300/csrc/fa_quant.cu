@@ -18,13 +18,14 @@
 // e4m3(y * (1 / scale)), the FP32 reciprocal formed once per tile (within
 // one rounding of y / scale), round to nearest even with saturation.
 //
-// Coarser scales (the control of the FA3 numerical-error ablation, "without
-// block quantization"): one scale per head or per tensor.  Three launches:
-// the per-tile pass above, a reduction of its scales to their maximum over
-// each head (or the whole tensor), written back to every tile of the group,
-// and the same pass again with those scales given (kGiven), which rewrites
-// the codes.  The maximum of the per-tile scales is the group's amax / 448
-// exactly: x -> fl(x / 448) is monotonic.
+// Coarser scales (one per head: the per-(batch, head) descale that the FP8
+// forward takes for V; one per tensor: the control of the FA3 numerical-error
+// ablation, "without block quantization").  Three launches: the per-tile
+// pass above writing only the scales (kScalesOnly), a reduction of those
+// scales to their maximum over each head (or the whole tensor), written back
+// to every tile of the group, and the pass again with those scales given
+// (kGiven), which writes the codes.  The maximum of the per-tile scales is
+// the group's amax / 448 exactly: x -> fl(x / 448) is monotonic.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -72,7 +73,11 @@ __device__ __forceinline__ void unpack_bf16(const typename RawWord<E>::type &w, 
     }
 }
 
-template <int D, bool kRot, bool kGiven>
+// kMode: 0 per-tile scales and codes, kGiven (1) codes from given scales,
+// kScalesOnly (2) per-tile scales without codes.
+constexpr int kGiven = 1, kScalesOnly = 2;
+
+template <int D, bool kRot, int kMode>
 __global__ void __launch_bounds__(256, QuantCfg<D>::min_blocks(kRot))
 fa_quantize_kernel(const __grid_constant__ CUtensorMap tm_x, const QuantArgs a) {
     using C = QuantCfg<D>;
@@ -187,9 +192,10 @@ fa_quantize_kernel(const __grid_constant__ CUtensorMap tm_x, const QuantArgs a) 
 #pragma unroll
         for (int i = 1; i < 8; ++i) tmax = fmaxf(tmax, wa[i]);
         float scale = tmax > 0.f ? tmax / 448.f : 1.f;
-        if constexpr (kGiven) scale = a.scale_in[static_cast<size_t>(bh) * a.n_tiles + tn];
+        if constexpr (kMode == kGiven) scale = a.scale_in[static_cast<size_t>(bh) * a.n_tiles + tn];
         const float inv = 1.f / scale;
-        if (!kGiven && tid == 0) a.scales[static_cast<size_t>(bh) * a.n_tiles + tn] = scale;
+        if (kMode != kGiven && tid == 0) a.scales[static_cast<size_t>(bh) * a.n_tiles + tn] = scale;
+        if constexpr (kMode == kScalesOnly) continue;
 
 #pragma unroll
         for (int rr = 0; rr < ROWS; ++rr) {
@@ -222,10 +228,10 @@ fa_quantize_kernel(const __grid_constant__ CUtensorMap tm_x, const QuantArgs a) 
     }
 }
 
-template <int D, bool kRot, bool kGiven>
+template <int D, bool kRot, int kMode>
 static cudaError_t launch_quantize_d(const QuantLaunch &L) {
     using C = QuantCfg<D>;
-    auto kern = fa_quantize_kernel<D, kRot, kGiven>;
+    auto kern = fa_quantize_kernel<D, kRot, kMode>;
     static unsigned long long configured = 0ull;   // bit per device id (< 64)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -242,14 +248,14 @@ static cudaError_t launch_quantize_d(const QuantLaunch &L) {
     return cudaGetLastError();
 }
 
-template <bool kGiven>
+template <int kMode>
 static cudaError_t launch_quantize_pass(const QuantLaunch &L) {
     const bool rot = L.args.signs != nullptr;
     if (L.d == 64)
-        return rot ? launch_quantize_d<64, true, kGiven>(L) : launch_quantize_d<64, false, kGiven>(L);
+        return rot ? launch_quantize_d<64, true, kMode>(L) : launch_quantize_d<64, false, kMode>(L);
     if (L.d == 128)
-        return rot ? launch_quantize_d<128, true, kGiven>(L) : launch_quantize_d<128, false, kGiven>(L);
-    return rot ? launch_quantize_d<256, true, kGiven>(L) : launch_quantize_d<256, false, kGiven>(L);
+        return rot ? launch_quantize_d<128, true, kMode>(L) : launch_quantize_d<128, false, kMode>(L);
+    return rot ? launch_quantize_d<256, true, kMode>(L) : launch_quantize_d<256, false, kMode>(L);
 }
 
 // One CTA per group of n consecutive scales: all of them become the
@@ -271,8 +277,9 @@ fa_scale_group_max_kernel(float *scales, long long n) {
 }
 
 cudaError_t launch_quantize(const QuantLaunch &L) {
-    cudaError_t e = launch_quantize_pass<false>(L);
-    if (e != cudaSuccess || L.granularity == 0) return e;
+    if (L.granularity == 0) return launch_quantize_pass<0>(L);
+    cudaError_t e = launch_quantize_pass<kScalesOnly>(L);
+    if (e != cudaSuccess) return e;
     // one group per head, or one for the whole tensor
     const long long groups = L.granularity == 1 ? static_cast<long long>(L.args.B) * L.args.H : 1;
     const long long n = static_cast<long long>(L.args.total) / groups;
@@ -280,7 +287,7 @@ cudaError_t launch_quantize(const QuantLaunch &L) {
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     QuantLaunch G = L;
     G.args.scale_in = L.args.scales;
-    return launch_quantize_pass<true>(G);
+    return launch_quantize_pass<kGiven>(G);
 }
 
 }  // namespace fa

@@ -221,9 +221,15 @@ fa_status fa_quantize_fp8_granular(const void *x, uint8_t *x8, float *scales,
  *   q8, k8, v8 : device, uint8 e4m3 [B][N][H][d], 16-byte aligned.
  *   q_scale, k_scale, v_scale : device, float [B][H][ceil(N/128)].
  *   o   : device, bf16 [B][N][H][d] (written).  lse : as for fa_fwd.
- *   d = 128 (others return FA_ERR_UNSUPPORTED).  alpha, causal as fa_fwd.
+ *   d in {128, 256} (others return FA_ERR_UNSUPPORTED; d = 256 runs one
+ *   128-row Q tile per work unit).  alpha, causal as fa_fwd.
  * P is rounded to e4m3 before the P V product with the V tile scale
- * folded in; accumulation is FP32.
+ * folded in (P'_j = P_j v_j / max_j v_j); accumulation is FP32, and O is
+ * normalised by the FP32 row sum of the unrounded P.  Per-tile V scales
+ * are accepted, but the fold then rounds the dominant terms of P' (ratios
+ * below 1 are not powers of two), which the row sum does not see; one V
+ * scale per head (fa_quantize_fp8_granular with FA_SCALE_HEAD, repeated
+ * over the tiles) makes every ratio 1 and is the measured better choice.
  */
 fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
                      const float *q_scale, const float *k_scale, const float *v_scale,

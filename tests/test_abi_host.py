@@ -196,7 +196,7 @@ def _f8call(lib, q=A, k=A, v=A, qs=A, ks=A, vs=A, o=A, lse=None, B=1, H=1, N=128
     (dict(causal=3), fa.FA_ERR_INVALID_ARG),
     (dict(alpha=float("nan")), fa.FA_ERR_INVALID_ARG),
     (dict(d=64), fa.FA_ERR_UNSUPPORTED),
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(k=A + 4), fa.FA_ERR_MISALIGNED),
     (dict(qs=A + 2), fa.FA_ERR_MISALIGNED),
 ])
