@@ -5,11 +5,18 @@
 //
 // What it computes is the FP8 forward of fa_fwd_kernel.cuh ("FlashAttention-3
 // on Hopper", sec. 6.3: e4m3 operands with one FP32 scale per 128-row tile;
-// "03 FA3", sec. 4: the exponent of P shifted by +8 so that P uses the e4m3
+// "03 FA3", sec. 4: the exponent of P shifted so that P uses the e4m3
 // range): for each row, S_j = (alpha log2 e) q_s k_s (Q K_j^T) in log2
-// units, P'_j = 2^(S_j - r + 8) (v_j / v_max) rounded to e4m3, O += P'_j V_j,
-// the row sum l counts 2^(S_j - r + 8) without the V factor, and finally
-// O = acc v_max / l, LSE = (r - 8 + log2 l) ln 2.
+// units, P'_j = 2^(S_j - r + c) (v_j / v_max) rounded to e4m3, O += P'_j V_j,
+// the row sum l counts 2^(S_j - r + c) without the V factor, and finally
+// O = acc v_max / l, LSE = (r - c + log2 l) ln 2.  The reference r moves
+// only when a tile's row max exceeds it by more than tau (conditional
+// rescale, "FlashAttention v1-v4", FA4), so P' <= 2^(c + tau); here c = 4
+// and tau = 4.8 (2^8.8 < 448, the largest e4m3 value).  The pages' shift of
+// 8 with tau = 0.8 meets the same bound, but on the outlier inputs a warp
+// then rescales its O rows on 31-63 % of key tiles, at ~2000 cycles each;
+// with c = 4 that falls to about a sixth, and the terms of P' that lose
+// precision (subnormal e4m3) are those below 2^-10 of the reference.
 //
 // Why a kernel of its own: at d = 256 the O accumulator of one Q tile takes
 // 256 of the 512 TMEM columns, so the two-Q-tile schedule does not fit; and
@@ -76,9 +83,10 @@ struct Fp8Fwd1qCfg {
 
     static constexpr uint32_t IDESC_QK = idesc_e4m3(128, BN, false, false);
     static constexpr uint32_t IDESC_PV = idesc_e4m3(128, D, false, true);
-    // "03 FA3", sec. 4: Max_offset 8; tau = 0.8 keeps P' <= 2^8.8 < 448.
-    static constexpr float TAU = 0.8f;
-    static constexpr float P_OFFSET = 8.0f;
+    // exponent offset c and rescale threshold tau: P' <= 2^(c + tau) =
+    // 2^8.8 < 448 (see the header)
+    static constexpr float TAU = 4.8f;
+    static constexpr float P_OFFSET = 4.0f;
 };
 
 // Work unit: one 128-row Q tile m of one (b, h); key tiles jhi-1 down to 0.
@@ -339,9 +347,19 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
             for (int m = 16; m > 0; m >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, m));
             const float vmax = vm;
-            // The K and V scales of the next key tile load while this one
-            // waits and computes.
-            float ks_n = a.k_scale[sbase + (U.T - 1)], vs_n = a.v_scale[sbase + (U.T - 1)];
+            // Per key tile: the score scale to log2 units with the q and k
+            // tile scales ("FlashAttention-3 on Hopper", sec. 6.3), the
+            // exponent offset c + log2(v_j / v_max) that carries the V tile
+            // scale, and v_max / v_j for the row sum.  Formed one tile ahead,
+            // off the path from S to P'.
+            float sc_n, voff_n, ivr_n;
+            auto tile_consts = [&](const int j) __attribute__((always_inline)) {
+                const float ks = a.k_scale[sbase + j], vs = a.v_scale[sbase + j];
+                sc_n = sl2 * qsc * ks;
+                voff_n = C::P_OFFSET + log2f(vs / vmax);
+                ivr_n = vmax / vs;
+            };
+            tile_consts(U.T - 1);
             // ---- epilogue of the previous unit, overlapped with this unit's
             //      first score tile ----
             if (pending_epi) {
@@ -352,11 +370,7 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             float r = -INFINITY, le = 0.f;
             for (int t = 0; t < U.T; ++t) {
                 const int j = U.T - 1 - t;
-                const float ks_c = ks_n, vs_c = vs_n;
-                if (t + 1 < U.T) {
-                    ks_n = a.k_scale[sbase + j - 1];
-                    vs_n = a.v_scale[sbase + j - 1];
-                }
+                const float sc = sc_n, voff = voff_n, ivr = ivr_n;
                 const uint32_t sb = t & 1;
                 ok = mbar_wait(bar(C::B_SFULL + sb), sb ? sph1 : sph0, w, 42);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
@@ -387,12 +401,6 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                     m2 = max3(m2, sf[c + 2], sf[c + 6]);
                     m3 = max3(m3, sf[c + 3], sf[c + 7]);
                 }
-                // score scale to log2 units with the q and k tile scales
-                // ("FlashAttention-3 on Hopper", sec. 6.3); the exponent
-                // offset 8 + log2(v_j / v_max) carries the V tile scale
-                const float sc = sl2 * qsc * ks_c;
-                const float vr = vs_c / vmax;
-                const float voff = C::P_OFFSET + log2f(vr);
                 const float bnew = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * sc;   // -inf stays -inf
                 float rn = r, corr = 1.f;
                 if (r == -INFINITY) rn = bnew;
@@ -403,7 +411,7 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const float2 nr2 = make_float2(voff - rs, voff - rs);
                 float2 e_a = make_float2(0.f, 0.f), e_b = e_a;
                 uint32_t p[32];
-                // ---- P' = 2^(x - r + 8) (v_j / v_max) as e4m3 ----
+                // ---- P' = 2^(x - r + c) (v_j / v_max) as e4m3 ----
 #pragma unroll
                 for (int c = 0; c < 128; c += 4) {
                     const float2 x01 = __ffma2_rn(make_float2(sf[c + 0], sf[c + 1]), c2, nr2);
@@ -415,6 +423,7 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                     e_b = __fadd2_rn(e_b, e23);
                 }
                 tmem_st32(tS + 0, p);
+                if (t + 1 < U.T) tile_consts(j - 1);
                 // ---- O correction: PV(t-1) must have completed first ----
                 const bool fix = __any_sync(0xffffffffu, need);
                 bool waited = false;
@@ -450,8 +459,8 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                     ok = wait_pv(t - 1, 44);
                     if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 }
-                // the row sum counts 2^(x - r + 8) without the V factor
-                le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y)) / vr;
+                // the row sum counts 2^(x - r + c) without the V factor
+                le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y)) * ivr;
                 r = rn;
             }
             if (!ok) break;
