@@ -420,17 +420,38 @@ static fa_status quantize_impl(const void *x, uint8_t *x8, float *scales,
     if (st != FA_OK) return st;
     fa::QuantLaunch L;
     std::memset(&L, 0, sizeof(L));
-    // one TMA box is a whole 128-row tile: {d, 1, 128, 1}, no swizzle
-    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                          static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
-    cuuint64_t strides[3] = {2ull * d, 2ull * d * H, 2ull * d * H * static_cast<cuuint64_t>(N)};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1, 128, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    if (g_encode(&L.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides,
-                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return FA_ERR_CUDA;
+    // Without rotation one TMA box is a whole 128-row tile, {d, 1, 128, 1},
+    // no swizzle.  With it, 128-byte column chunks {64, 1, 128, 1} in the
+    // 128-byte swizzle (rows read by one thread each without conflicts), and
+    // the codes leave through TMA stores of {128, 1, 128, 1} (64-byte swizzle
+    // and {64, 1, 128, 1} at d = 64).
+    if (hadamard_signs) {
+        if ((st = encode_bshd(&L.x, x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, H, N, d, 128)) != FA_OK)
+            return st;
+        const cuuint32_t w8 = d == 64 ? 64 : 128;
+        cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+        cuuint64_t strides[3] = {1ull * d, 1ull * d * H, 1ull * d * H * static_cast<cuuint64_t>(N)};
+        cuuint32_t box[4] = {w8, 1, 128, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (g_encode(&L.x8, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, x8, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     d == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return FA_ERR_CUDA;
+    } else {
+        cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+        cuuint64_t strides[3] = {2ull * d, 2ull * d * H, 2ull * d * H * static_cast<cuuint64_t>(N)};
+        cuuint32_t box[4] = {static_cast<cuuint32_t>(d), 1, 128, 1};
+        cuuint32_t estr[4] = {1, 1, 1, 1};
+        if (g_encode(&L.x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return FA_ERR_CUDA;
+    }
     L.args.x8 = x8;
     L.args.scales = scales;
     L.args.signs = hadamard_signs;

@@ -81,6 +81,7 @@ struct QuantArgs {
 };
 struct QuantLaunch {
     CUtensorMap x;
+    CUtensorMap x8;         // rotated pass: codes {d, H, N, B}, box {128, 1, 128, 1}, 128-B swizzle
     QuantArgs args;
     int d;
     int sm_count;
