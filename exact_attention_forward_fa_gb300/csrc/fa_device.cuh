@@ -144,6 +144,14 @@ __device__ __forceinline__ void tma_load_4d(const CUtensorMap *m, uint32_t dst,
         : "memory");
 }
 
+// 32-byte store of eight 32-bit words (the address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]),
+                    "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
 // 4-D tiled store of a box from shared memory (bulk-group completion).  Out-of-
 // range parts of the box are not written; every coordinate is >= 0 and c0
 // is 16-byte aligned in bytes.

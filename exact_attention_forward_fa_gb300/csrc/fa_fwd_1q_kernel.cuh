@@ -391,8 +391,8 @@ fa_fwd_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                     add_pair<kBF16>(r_a.x, r_a.y, pk0);
                     add_pair<kBF16>(r_b.x, r_b.y, pk1);
                 }
-                le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y));
-                lr = lr * corr + ((r_a.x + r_a.y) + (r_b.x + r_b.y));
+                le = __fmaf_rn(le, corr, (e_a.x + e_a.y) + (e_b.x + e_b.y));
+                lr = __fmaf_rn(lr, corr, (r_a.x + r_a.y) + (r_b.x + r_b.y));
 #pragma unroll
                 for (int c = 0; c < BN / 2; c += 32)
                     tmem_st32(tS + c, *reinterpret_cast<uint32_t(*)[32]>(&p[c]));

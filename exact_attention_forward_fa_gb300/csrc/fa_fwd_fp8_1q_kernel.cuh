@@ -460,7 +460,7 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                     if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 }
                 // the row sum counts 2^(x - r + c) without the V factor
-                le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y)) * ivr;
+                le = __fmaf_rn(le, corr, ((e_a.x + e_a.y) + (e_b.x + e_b.y)) * ivr);
                 r = rn;
             }
             if (!ok) break;

@@ -32,7 +32,8 @@
 //     accumulates the row sum of those rounded values in FP32, writes P back
 //     over its S columns with tcgen05.st,
 //     and rescales its O row in TMEM when the reference point moved.  After
-//     the last tile it normalises O by 1/l and stores O and LSE.
+//     the last tile it normalises O by 1/l and stores O (32-byte stores, so
+//     each store fills whole sectors of its row) and LSE.
 //   * TMEM (512 columns): S_L [0,128), S_H [128,256), O_L [256,256+D),
 //     O_H [256+D, 256+2D); P_X (64 columns of packed pairs) overlays the
 //     first half of S_X.
@@ -113,6 +114,7 @@ struct FwdCfg {
                          NBAR = B_MMADONE + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
     static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;   // + align slack
+    static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
     // TMEM columns
     static constexpr uint32_t TMEM_COLS = 512;
@@ -471,6 +473,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         const float sc_pre = kCap ? a.sc_pre : 0.f;
         const float sl2 = kCap ? a.sc_post : a.scale_log2;
         uint32_t sph = 0, oph = 0;
+        // O rows are D * 2 (partials D * 4) bytes apart, a multiple of 32, so
+        // 32-byte stores are aligned everywhere when the base is; the API
+        // promises only 16 bytes, and 16-byte stores serve that case.
+        const bool v8ok =
+            ((reinterpret_cast<uintptr_t>(kSplit ? static_cast<const void *>(a.o_part) : a.o) & 31u) == 0);
         bool ok = true;
         for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
                      u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
@@ -674,7 +681,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (lane == 0) mbar_arrive(bar(C::B_PFULL + x));
                 // ---- row sums, after P is published ----
                 // (FP8: the row sum counts 2^(x - r + c) without the V factor)
-                le = le * corr + ((e_a.x + e_a.y) + (e_b.x + e_b.y)) * ivr_c;
+                // (the row-sum updates are explicit fused multiply-adds: every
+                // instantiation then rounds them alike, whatever the compiler
+                // would contract)
+                le = __fmaf_rn(le, corr, ((e_a.x + e_a.y) + (e_b.x + e_b.y)) * ivr_c);
                 if constexpr (!kFP8) {
                     float2 r_a = make_float2(0.f, 0.f), r_b = r_a;
 #pragma unroll
@@ -682,16 +692,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         add_pair<kBF16>(r_a.x, r_a.y, p[i]);
                         add_pair<kBF16>(r_b.x, r_b.y, p[i + 1]);
                     }
-                    lr = lr * corr + ((r_a.x + r_a.y) + (r_b.x + r_b.y));
+                    lr = __fmaf_rn(lr, corr, (r_a.x + r_a.y) + (r_b.x + r_b.y));
                 }
                 r = rn;
             }
             if (!ok) break;
-            // ---- epilogue: O / l -> global, LSE ----
-            ok = mbar_wait(bar(C::B_OFULL + x), oph, w, 21);
-            if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
-            oph ^= 1;
-            tc_fence_after();
+            // ---- the row's normaliser and LSE ----
             // 16-bit P: O / l_r.  FP8: O v_max / l (O accumulated P' = P v_j/v_max).
             const bool live = (le > 0.f) && (kFP8 || lr > 0.f);
             float inv = live ? (kFP8 ? vmax / le : 1.f / lr) : 0.f;
@@ -707,49 +713,84 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         lse2 = sg;
                     } else {
                         const float M = fmaxf(r, sg);
-                        lse2 = M + log2f(le * ex2_approx(r - M) + ex2_approx(sg - M));
+                        lse2 = M + log2f(__fmaf_rn(le, ex2_approx(r - M), ex2_approx(sg - M)));
                         inv = 1.f / (lr + ex2_approx(sg - r));    // 2^+big -> inf -> 0
                     }
                 }
             }
             const int grow = qpos;
-            uint16_t *orow = reinterpret_cast<uint16_t *>(a.o) +
-                             ((static_cast<size_t>(U.b) * a.N + grow) * a.H + qh) * D;
-            // The whole O row comes into registers first, so the accumulator
-            // is handed back to the next unit's P V before the stores.
-            uint32_t ov[D];
+            {
+                // ---- epilogue: O / l -> global ----
+                ok = mbar_wait(bar(C::B_OFULL + x), oph, w, 21);
+                if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
+                oph ^= 1;
+                tc_fence_after();
+                // The whole O row comes into registers first, so the
+                // accumulator is handed back to the next unit's P V before
+                // the stores.
+                uint32_t ov[D];
 #pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch)
-                tmem_ld32(tO + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[ch * 32]));
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + x));
-            if constexpr (kSplit) {
-                // split key range: FP32 partial O and its LSE
+                for (int ch = 0; ch < D / 32; ++ch)
+                    tmem_ld32(tO + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[ch * 32]));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + x));
                 if (grow < a.N) {
-                    float *prow = a.o_part +
-                        (((static_cast<size_t>(U.s) * a.B + U.b) * a.N + grow) * a.H + U.h) * D;
+                    if constexpr (kSplit) {
+                        // split key range: FP32 partial O
+                        float *prow = a.o_part +
+                            (((static_cast<size_t>(U.s) * a.B + U.b) * a.N + grow) * a.H + U.h) * D;
+                        if (v8ok) {
 #pragma unroll
-                    for (int ch = 0; ch < D / 4; ++ch)
-                        reinterpret_cast<float4 *>(prow)[ch] = make_float4(
-                            __uint_as_float(ov[4 * ch]) * inv, __uint_as_float(ov[4 * ch + 1]) * inv,
-                            __uint_as_float(ov[4 * ch + 2]) * inv, __uint_as_float(ov[4 * ch + 3]) * inv);
+                            for (int ch = 0; ch < D / 8; ++ch) {
+                                uint32_t pv[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    pv[i] = __float_as_uint(__uint_as_float(ov[8 * ch + i]) * inv);
+                                st_global_v8(prow + 8 * ch, pv);
+                            }
+                        } else {
+#pragma unroll
+                            for (int ch = 0; ch < D / 4; ++ch)
+                                reinterpret_cast<float4 *>(prow)[ch] = make_float4(
+                                    __uint_as_float(ov[4 * ch]) * inv, __uint_as_float(ov[4 * ch + 1]) * inv,
+                                    __uint_as_float(ov[4 * ch + 2]) * inv,
+                                    __uint_as_float(ov[4 * ch + 3]) * inv);
+                        }
+                    } else {
+                        uint16_t *orow = reinterpret_cast<uint16_t *>(a.o) +
+                                         ((static_cast<size_t>(U.b) * a.N + grow) * a.H + qh) * D;
+                        if (v8ok) {
+#pragma unroll
+                            for (int ch = 0; ch < D / 16; ++ch) {
+                                uint32_t pk[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    pk[i] = pack2<kBF16>(__uint_as_float(ov[16 * ch + 2 * i]) * inv,
+                                                         __uint_as_float(ov[16 * ch + 2 * i + 1]) * inv);
+                                st_global_v8(orow + 16 * ch, pk);
+                            }
+                        } else {
+#pragma unroll
+                            for (int ch = 0; ch < D / 8; ++ch) {
+                                uint32_t pk[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    pk[i] = pack2<kBF16>(__uint_as_float(ov[8 * ch + 2 * i]) * inv,
+                                                         __uint_as_float(ov[8 * ch + 2 * i + 1]) * inv);
+                                reinterpret_cast<uint4 *>(orow)[ch] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            }
+                        }
+                    }
+                }
+            }
+            if constexpr (kSplit) {
+                // split key range: the partial's LSE
+                if (grow < a.N)
                     a.lse_part[((static_cast<size_t>(U.s) * a.B + U.b) * a.H + U.h) * a.N + grow] =
                         live ? (r + log2f(le)) * 0.69314718055994530942f : -INFINITY;
-                }
                 continue;
-            }
-            if (grow < a.N) {
-#pragma unroll
-                for (int ch = 0; ch < D / 8; ++ch) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        pk[i] = pack2<kBF16>(__uint_as_float(ov[8 * ch + 2 * i]) * inv,
-                                             __uint_as_float(ov[8 * ch + 2 * i + 1]) * inv);
-                    reinterpret_cast<uint4 *>(orow)[ch] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                }
             }
             if (a.lse != nullptr && grow < a.N)
                 a.lse[(static_cast<size_t>(U.b) * a.H + qh) * a.N + grow] =

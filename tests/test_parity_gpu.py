@@ -181,6 +181,41 @@ def test_deterministic_bits_lse_optional_and_side_stream(gpu_lib):
     assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
 
 
+def _offset16(n, dtype):
+    """A device buffer of n elements that starts 16 bytes past a 32-byte
+    boundary (torch allocations are 256-byte aligned)."""
+    shift = 16 // torch.empty((), dtype=dtype).element_size()
+    buf = torch.empty((n + shift,), dtype=dtype, device="cuda")
+    out = buf[shift:]
+    assert out.data_ptr() % 32 == 16
+    return out
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_outputs_at_16_byte_offsets_match_aligned_bits(gpu_lib, causal):
+    # The API promises 16-byte alignment only: the O stores and the split
+    # partials must give the same bits there as at a 256-byte boundary.
+    fa = gpu_lib
+    B, H, N, d = 2, 3, 700, 64
+    q, k, v = (x.cuda() for x in synth.qkv(B, H, N, d, seed=12))
+    a = synth.default_alpha(d)
+    o1, l1 = fa.attention(q, k, v, causal=causal, alpha=a)
+    o2 = _offset16(q.numel(), q.dtype).view(q.shape)
+    l2 = torch.empty_like(l1)
+    assert fa.fa_fwd(q, k, v, o2, l2, B, H, N, d, a, int(causal), fa.FA_BF16) == fa.FA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    S = 2
+    ws = _offset16(fa.fa_splitkv_workspace_floats(B, H, N, d, S), torch.float32)
+    o3 = torch.empty_like(q)
+    l3 = torch.empty_like(l1)
+    assert fa.fa_fwd_splitkv(q, k, v, o3, l3, B, H, N, d, a, int(causal), fa.FA_BF16, S,
+                             ws) == fa.FA_OK
+    o4, l4 = fa.attention_splitkv(q, k, v, causal=causal, alpha=a, n_splits=S)
+    assert fa.fa_check_status() == fa.FA_OK
+    assert torch.equal(o3, o4) and torch.equal(l3, l4)
+
+
 @pytest.mark.parametrize("alpha", [0.03, 0.5])
 def test_other_scales_and_wide_scores(gpu_lib, alpha):
     # Scores with a wide spread move the reference point often (tau = 8).
