@@ -350,16 +350,22 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             // Per key tile: the score scale to log2 units with the q and k
             // tile scales ("FlashAttention-3 on Hopper", sec. 6.3), the
             // exponent offset c + log2(v_j / v_max) that carries the V tile
-            // scale, and v_max / v_j for the row sum.  Formed one tile ahead,
-            // off the path from S to P'.
-            float sc_n, voff_n, ivr_n;
-            auto tile_consts = [&](const int j) __attribute__((always_inline)) {
-                const float ks = a.k_scale[sbase + j], vs = a.v_scale[sbase + j];
-                sc_n = sl2 * qsc * ks;
-                voff_n = C::P_OFFSET + log2f(vs / vmax);
-                ivr_n = vmax / vs;
+            // scale, and v_max / v_j for the row sum.  The next tile's scales
+            // are loaded at the top of a tile (they land during the wait for
+            // S) and turned into its constants after this tile's row sum:
+            // neither sits on the path from S to P'.
+            float ks_n, vs_n, sc_n, voff_n, ivr_n;
+            auto tile_load = [&](const int j) __attribute__((always_inline)) {
+                ks_n = a.k_scale[sbase + j];
+                vs_n = a.v_scale[sbase + j];
             };
-            tile_consts(U.T - 1);
+            auto tile_consts = [&]() __attribute__((always_inline)) {
+                sc_n = sl2 * qsc * ks_n;
+                voff_n = C::P_OFFSET + log2f(vs_n / vmax);
+                ivr_n = vmax / vs_n;
+            };
+            tile_load(U.T - 1);
+            tile_consts();
             // ---- epilogue of the previous unit, overlapped with this unit's
             //      first score tile ----
             if (pending_epi) {
@@ -371,6 +377,7 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             for (int t = 0; t < U.T; ++t) {
                 const int j = U.T - 1 - t;
                 const float sc = sc_n, voff = voff_n, ivr = ivr_n;
+                if (t + 1 < U.T) tile_load(j - 1);
                 const uint32_t sb = t & 1;
                 ok = mbar_wait(bar(C::B_SFULL + sb), sb ? sph1 : sph0, w, 42);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
@@ -423,7 +430,6 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                     e_b = __fadd2_rn(e_b, e23);
                 }
                 tmem_st32(tS + 0, p);
-                if (t + 1 < U.T) tile_consts(j - 1);
                 // ---- O correction: PV(t-1) must have completed first ----
                 const bool fix = __any_sync(0xffffffffu, need);
                 bool waited = false;
@@ -462,6 +468,7 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // the row sum counts 2^(x - r + c) without the V factor
                 le = __fmaf_rn(le, corr, ((e_a.x + e_a.y) + (e_b.x + e_b.y)) * ivr);
                 r = rn;
+                if (t + 1 < U.T) tile_consts();
             }
             if (!ok) break;
             P = U;

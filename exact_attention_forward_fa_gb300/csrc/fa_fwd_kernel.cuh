@@ -517,20 +517,30 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             // FP8, per key tile: the score scale to log2 units with the q and
             // k tile scales ("FlashAttention-3 on Hopper", sec. 6.3), the
             // exponent offset c + log2(v_j / v_max) that carries the V tile
-            // scale, and v_max / v_j for the row sum -- formed one tile
-            // ahead, off the path from S to P' (loads, a division and a
-            // logarithm at the top of each tile sat on that path)
+            // scale, and v_max / v_j for the row sum.  The next tile's scales
+            // are loaded at the top of a tile (they land during the wait for
+            // S) and turned into its constants after this tile's row sums:
+            // neither the loads nor the division and logarithm sit on the
+            // path from S to P'.
+            float ks_n = 0.f, vs_n = 0.f;
             float sc_n = 0.f, voff_n = 0.f, ivr_n = 1.f;
-            auto tile_consts = [&](const int jj) __attribute__((always_inline)) {
-                const float ks = a.k_scale[sbase + jj], vs = a.v_scale[sbase + jj];
-                sc_n = sl2 * qs * ks;
-                voff_n = C::P_OFFSET + log2f(vs / vmax);
-                ivr_n = vmax / vs;
+            auto tile_load = [&](const int jj) __attribute__((always_inline)) {
+                ks_n = a.k_scale[sbase + jj];
+                vs_n = a.v_scale[sbase + jj];
             };
-            if (kFP8 && t0 < t1) tile_consts(U.jhi - 1 - t0);
+            auto tile_consts = [&]() __attribute__((always_inline)) {
+                sc_n = sl2 * qs * ks_n;
+                voff_n = C::P_OFFSET + log2f(vs_n / vmax);
+                ivr_n = vmax / vs_n;
+            };
+            if (kFP8 && t0 < t1) {
+                tile_load(U.jhi - 1 - t0);
+                tile_consts();
+            }
             for (int t = t0; t < t1; ++t) {
                 const int j = U.jhi - 1 - t;
                 const float sc_c = sc_n, voff_c = voff_n, ivr_c = ivr_n;
+                if (kFP8 && t + 1 < t1) tile_load(j - 1);
                 ok = mbar_wait(bar(C::B_SFULL + x), sph, w, 20);
                 if (__any_sync(0xffffffffu, !ok)) { ok = false; break; }
                 sph ^= 1;
@@ -618,7 +628,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         e_b = __fadd2_rn(e_b, e23);
                     }
                     tmem_st32(tS + 0, *reinterpret_cast<uint32_t(*)[32]>(&p[0]));
-                    if (t + 1 < t1) tile_consts(j - 1);
                 } else {
                     // ---- 16-bit P = 2^(x - r): first against the current r;
                     //      the max is formed only on the first tile or when
@@ -695,6 +704,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     lr = __fmaf_rn(lr, corr, (r_a.x + r_a.y) + (r_b.x + r_b.y));
                 }
                 r = rn;
+                if (kFP8 && t + 1 < t1) tile_consts();
             }
             if (!ok) break;
             // ---- the row's normaliser and LSE ----
