@@ -147,6 +147,21 @@ const char *fa_status_string(fa_status s) {
 // query head h reads key/value head h / (H / H_kv)).  pack: the g = H / H_kv
 // query heads of a key/value head share each Q tile (d in {64, 128}, g
 // dividing 128); with g = 1 that is the plain layout.
+// Causal units of the two-tile kernel (unsplit, unpacked) run in the
+// kernel's dynamic order: one CTA per unit (CTAs that have not started yet
+// are taken over by running ones), and a.chunk query heads per group of the
+// order, as many as keep the group's K and V within 32 MiB of L2.
+static void set_dynamic_order(fa::FwdLaunch &L, uint64_t units, int B, int H, int N, int d,
+                              int elem_bytes, int group) {
+    L.grid = static_cast<int>(units);
+    const uint64_t kv_head = 2ull * static_cast<uint64_t>(N) * d * elem_bytes;
+    uint64_t c = (32ull << 20) / (kv_head > 0 ? kv_head : 1) * static_cast<uint64_t>(group);
+    const uint64_t bh = static_cast<uint64_t>(B) * H;
+    if (c < 1) c = 1;
+    if (c > bh) c = bh;
+    L.args.chunk = static_cast<int>(c);
+}
+
 static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse,
                           int B, int H, int H_kv, int N, int d, float alpha, int causal,
                           fa_dtype dtype, void *stream, bool pack = false) {
@@ -203,6 +218,8 @@ static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, 
     L.args.n_splits = 1;
     L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
     L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
+    L.args.chunk = 1;
+    if (causal && !pack && d != 256) set_dynamic_order(L, units, B, H, N, d, 2, g);
     L.stream = static_cast<cudaStream_t>(stream);
     L.causal = causal != 0;
     L.bf16 = dtype == FA_BF16;
@@ -528,6 +545,8 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     L.args.k_scale = k_scale;
     L.args.v_scale = v_scale;
     L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
+    L.args.chunk = 1;
+    if (causal && d == 128) set_dynamic_order(L, units, B, H, N, d, 1, 1);
     L.stream = static_cast<cudaStream_t>(stream);
     L.causal = causal != 0;
     L.bf16 = true;

@@ -152,6 +152,30 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *v) {
                  : "memory");
 }
 
+// Cluster launch control (dynamic persistent scheduling): ask the hardware
+// to cancel one not-yet-launched CTA of this grid; the 16-byte response
+// lands in shared memory at resp and completes 16 transaction bytes on bar
+// (armed by the caller with mbar_arrive_expect_tx).  A CTA that was
+// cancelled never runs, so its block index becomes this CTA's work.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+        "[%0], [%1];" :: "r"(resp), "r"(bar) : "memory");
+}
+// The block index a completed response names, or -1 when nothing was
+// cancelled (every CTA of the grid has been launched).
+__device__ __forceinline__ int clc_block(uint32_t resp) {
+    uint32_t ok, cx;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+        "ld.shared.b128 r, [%2];\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(cx) : "r"(resp) : "memory");
+    return ok ? static_cast<int>(cx) : -1;
+}
+
 // 4-D tiled store of a box from shared memory (bulk-group completion).  Out-of-
 // range parts of the box are not written; every coordinate is >= 0 and c0
 // is 16-byte aligned in bytes.

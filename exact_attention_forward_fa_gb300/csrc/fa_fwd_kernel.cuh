@@ -56,8 +56,13 @@ struct FwdArgs {
     // Split key ranges (d <= 128, 16-bit): n_splits >= 1; with o_part set,
     // split s of a unit writes its partial O (FP32, normalised by its own
     // row sum) to o_part [S][B][N][H][D] and its LSE to lse_part [S][B][H][N]
-    // instead of O and LSE.
-    int n_splits;
+    // instead of O and LSE.  Causal units without splits or packing take
+    // the dynamic order of make_unit instead, whose groups hold chunk heads
+    // (>= 1); the two never meet in one launch.
+    union {
+        int n_splits;
+        int chunk;
+    };
     float *o_part, *lse_part;
     float scale_log2;    // alpha * log2(e)
     // Score and mask variants (kExt instantiations only).  Key j is hidden
@@ -111,9 +116,17 @@ struct FwdCfg {
                          B_KVEMPTY = 2 * NQ + NSTAGE, B_SFULL = 2 * NQ + 2 * NSTAGE,
                          B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
                          B_OEMPTY = B_OFULL + 2, B_MMADONE = B_OEMPTY + 2,
-                         NBAR = B_MMADONE + 1;
+                         // dynamic order: the hardware's answer for the next
+                         // unit landed, its block index published, slot free
+                         B_CLCFULL = B_MMADONE + 1, B_UNIT = B_CLCFULL + 4,
+                         B_CLCEMPTY = B_UNIT + 4, NBAR = B_CLCEMPTY + 4;
+    static constexpr int CLC_DEPTH = 4;          // units the producer may run ahead
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;   // + align slack
+    // 16 B per answer, 16-byte aligned (the answer's store and its 128-bit load)
+    static constexpr uint32_t CLC_OFF = (MISC_OFF + 16 + 15) & ~15u;
+    static_assert(CLC_OFF % 16 == 0, "cluster launch control answers: 16-byte aligned");
+    static constexpr uint32_t UNIT_OFF = CLC_OFF + CLC_DEPTH * 16;   // int per answer
+    static constexpr uint32_t SMEM_BYTES = UNIT_OFF + CLC_DEPTH * 4 + 1024;   // + align slack
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
     // TMEM columns
@@ -179,6 +192,18 @@ __device__ __forceinline__ bool units_longest_first(const FwdArgs &a) {
 // query head h group + p % group, R = 128 / group -- so units run over K/V
 // heads (U.h is then the K/V head) and one K/V stream serves the whole
 // group.  R divides 128, so a tile's positions never straddle a key tile.
+// Causal units without splits or packing are taken in a dynamic order:
+// each CTA asks the hardware for its next unit when it needs it (cluster
+// launch control), so a CTA that finishes early takes more.  The order
+// keeps a group of a.chunk heads together, longest pair first within the
+// group, so the group's K/V stay in L2 while its units run; the shortest
+// pair of every head (one or two key tiles) comes last, over all heads,
+// so that the CTAs finish together.
+template <bool kCausal, bool kSplit, bool kExt, bool kPack>
+__device__ __forceinline__ constexpr bool dynamic_units() {
+    return kCausal && !kSplit && !kExt && !kPack;
+}
+
 template <bool kCausal, bool kSplit, bool kExt = false, bool kPack = false>
 __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     Unit U;
@@ -190,7 +215,20 @@ __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     int p, bh;
     // a right bound without a left one makes later pairs longer
     const bool lpt = units_longest_first<kCausal, kExt>(a);
-    if (lpt) {              // longest-first: the last pairs of every head first
+    if (dynamic_units<kCausal, kSplit, kExt, kPack>()) {
+        const int P1 = a.n_pairs - 1;              // pairs per head before the tail
+        const int grouped = BH * P1;
+        if (u < grouped) {
+            const int g = u / (a.chunk * P1);
+            const int r = u - g * a.chunk * P1;
+            const int cg = min(a.chunk, BH - g * a.chunk);   // heads in this group
+            p = P1 - r / cg;
+            bh = g * a.chunk + r % cg;
+        } else {
+            p = 0;
+            bh = u - grouped;
+        }
+    } else if (lpt) {       // longest-first: the last pairs of every head first
         p = a.n_pairs - 1 - u / BH;
         bh = u % BH;
     } else {                // consecutive units share a head's K/V in L2
@@ -270,6 +308,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const bool snake = units_longest_first<kCausal, kExt>(a);   // unit order (unit_stride0)
+    // Dynamic order: the grid has one CTA per unit; a CTA starts with its
+    // own unit and then takes the units of CTAs it cancels before they
+    // launch.  The producer asks for the next unit once it has issued the
+    // loads of the current one; the k-th answer goes to slot k % CLC_DEPTH,
+    // the producer publishes its block index there (-1: none left), and the
+    // MMA warp and the 8 softmax warps read it and release the slot.
+    // Static order: the persistent stride walk.
+    volatile int *unit_slot = reinterpret_cast<volatile int *>(gbase + C::UNIT_OFF);
+    constexpr bool kDyn = dynamic_units<kCausal, kSplit, kExt, kPack>();
 
     auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
@@ -294,6 +341,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             mbar_init(bar(C::B_KVEMPTY + s), 1);
         }
         mbar_init(bar(C::B_MMADONE), 1);
+        for (int q = 0; kDyn && q < C::CLC_DEPTH; ++q) {
+            mbar_init(bar(C::B_CLCFULL + q), 1);
+            mbar_init(bar(C::B_UNIT + q), 1);
+            mbar_init(bar(C::B_CLCEMPTY + q), 9);
+        }
         fence_barrier_init();
     }
     tc_fence_before();
@@ -335,8 +387,27 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 ++qc;
                 return true;
             };
-            for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
-                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+            // dynamic order: the k-th request (k = 0, 1, ...) uses slot
+            // k % CLC_DEPTH, once its readers have released answer k - CLC_DEPTH
+            uint32_t kq = 0;                        // requests issued
+            bool clc_pending = false;               // a request without its answer
+            auto next_dyn = [&]() __attribute__((always_inline)) -> int {
+                if (!ok) return -1;
+                const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+                ++kq;
+                if (!mbar_wait(bar(C::B_CLCEMPTY + q), ph ^ 1u, w, 3)) { ok = false; return -1; }
+                mbar_arrive_expect_tx(bar(C::B_CLCFULL + q), 16u);
+                clc_try_cancel(base + C::CLC_OFF + 16u * q, bar(C::B_CLCFULL + q));
+                clc_pending = true;
+                if (!mbar_wait(bar(C::B_CLCFULL + q), ph, w, 4)) { ok = false; return -1; }
+                clc_pending = false;
+                const int nu = clc_block(base + C::CLC_OFF + 16u * q);
+                unit_slot[q] = nu;
+                mbar_arrive(bar(C::B_UNIT + q));        // release: the index is visible
+                return nu;
+            };
+            for (int u = blockIdx.x, st = unit_stride0(snake); ok && (!kDyn || u >= 0) && u < a.n_units;
+                     u = kDyn ? next_dyn() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const Unit U = make_unit<kCausal, kSplit, kExt, kPack>(u, a);
                 if (U.act[0]) ok = ok && load_q(0, U);
                 if (U.act[1]) ok = ok && load_q(1, U);
@@ -358,6 +429,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
             }
             // Let every copy this lane issued land before the CTA can exit.
+            if (kDyn && clc_pending)
+                mbar_wait_quiet(bar(C::B_CLCFULL + (kq - 1) % C::CLC_DEPTH),
+                                ((kq - 1) / C::CLC_DEPTH) & 1u, 500000000ull);
             for (int s = 0; s < C::NSTAGE; ++s)
                 if (armed & (1u << s))
                     mbar_wait_quiet(bar(C::B_KVFULL + s), (armed_par >> s) & 1u, 500000000ull);
@@ -375,8 +449,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint32_t pph0 = 0, pph1 = 0;
             uint32_t slot = 0, phase = 0;
             bool ok = true;
-            for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
-                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+            uint32_t kq = 0;                        // dynamic order: answers read
+            auto next_dyn = [&]() __attribute__((always_inline)) -> int {
+                if (!ok) return -1;
+                const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+                ++kq;
+                if (!mbar_wait_warp(bar(C::B_UNIT + q), ph, w, 15)) { ok = false; return -1; }
+                const int nu = unit_slot[q];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(C::B_CLCEMPTY + q));
+                return nu;
+            };
+            for (int u = blockIdx.x, st = unit_stride0(snake); ok && (!kDyn || u >= 0) && u < a.n_units;
+                     u = kDyn ? next_dyn() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const Unit U = make_unit<kCausal, kSplit, kExt, kPack>(u, a);
                 uint32_t qs0 = 0, qp0 = 0, qs1 = 0, qp1 = 0;   // Q slot and parity per tile
                 if (U.act[0]) { qs0 = qc % C::NQ; qp0 = (qc / C::NQ) & 1u; ++qc; }
@@ -479,8 +564,20 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         const bool v8ok =
             ((reinterpret_cast<uintptr_t>(kSplit ? static_cast<const void *>(a.o_part) : a.o) & 31u) == 0);
         bool ok = true;
-        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
-                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+        uint32_t kq = 0;                            // dynamic order: answers read
+        // (a failed wait leaves this loop by break, so ok holds here)
+        auto next_dyn = [&]() __attribute__((always_inline)) -> int {
+            const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+            ++kq;
+            ok = mbar_wait(bar(C::B_UNIT + q), ph, w, 23);
+            if (__any_sync(0xffffffffu, !ok)) { ok = false; return -1; }
+            const int nu = unit_slot[q];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_CLCEMPTY + q));
+            return nu;
+        };
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && (!kDyn || u >= 0) && u < a.n_units;
+                     u = kDyn ? next_dyn() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const Unit U = make_unit<kCausal, kSplit, kExt, kPack>(u, a);
             const bool act = x ? U.act[1] : U.act[0];
             if (!act) continue;
