@@ -147,10 +147,10 @@ const char *fa_status_string(fa_status s) {
 // query head h reads key/value head h / (H / H_kv)).  pack: the g = H / H_kv
 // query heads of a key/value head share each Q tile (d in {64, 128}, g
 // dividing 128); with g = 1 that is the plain layout.
-// Causal units of the two-tile kernel (unsplit, unpacked) run in the
-// kernel's dynamic order: one CTA per unit (CTAs that have not started yet
-// are taken over by running ones), and a.chunk query heads per group of the
-// order, as many as keep the group's K and V within 32 MiB of L2.
+// Causal units (unsplit, unpacked; every head dim) run in the kernels'
+// dynamic order: one CTA per unit (CTAs that have not started yet are taken
+// over by running ones), and a.chunk query heads per group of the order, as
+// many as keep the group's K and V within 32 MiB of L2.
 static void set_dynamic_order(fa::FwdLaunch &L, uint64_t units, int B, int H, int N, int d,
                               int elem_bytes, int group) {
     L.grid = static_cast<int>(units);
@@ -219,7 +219,7 @@ static fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, 
     L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
     L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
     L.args.chunk = 1;
-    if (causal && !pack && d != 256) set_dynamic_order(L, units, B, H, N, d, 2, g);
+    if (causal && !pack) set_dynamic_order(L, units, B, H, N, d, 2, g);
     L.stream = static_cast<cudaStream_t>(stream);
     L.causal = causal != 0;
     L.bf16 = dtype == FA_BF16;
@@ -546,7 +546,7 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     L.args.v_scale = v_scale;
     L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
     L.args.chunk = 1;
-    if (causal && d == 128) set_dynamic_order(L, units, B, H, N, d, 1, 1);
+    if (causal) set_dynamic_order(L, units, B, H, N, d, 1, 1);
     L.stream = static_cast<cudaStream_t>(stream);
     L.causal = causal != 0;
     L.bf16 = true;

@@ -71,9 +71,14 @@ struct Fp8Fwd1qCfg {
                          B_KVEMPTY = B_KVFULL + NSTAGE, B_SFULL = B_KVEMPTY + NSTAGE,
                          B_PFULL = B_SFULL + 2, B_PVDONE = B_PFULL + 2,
                          B_OEMPTY = B_PVDONE + 2, B_MMADONE = B_OEMPTY + 1,
-                         NBAR = B_MMADONE + 1;
+                         // causal: the dynamic order's answers (see the kernel)
+                         B_CLCFULL = B_MMADONE + 1, B_UNIT = B_CLCFULL + 4,
+                         B_CLCEMPTY = B_UNIT + 4, NBAR = B_CLCEMPTY + 4;
+    static constexpr int CLC_DEPTH = 4;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NBAR * 8;
-    static constexpr uint32_t SMEM_BYTES = MISC_OFF + 16 + 1024;   // + align slack
+    static constexpr uint32_t CLC_OFF = (MISC_OFF + 16 + 15) & ~15u;   // 16-byte aligned
+    static constexpr uint32_t UNIT_OFF = CLC_OFF + CLC_DEPTH * 16;
+    static constexpr uint32_t SMEM_BYTES = UNIT_OFF + CLC_DEPTH * 4 + 1024;   // + align slack
     static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
     static constexpr uint32_t TMEM_COLS = 512;
@@ -99,9 +104,8 @@ __device__ __forceinline__ UnitF8 make_unit_f8(int u, const FwdArgs &a) {
     UnitF8 U;
     const int BH = a.B * a.H;
     int bh;
-    if (kCausal) {            // longest first
-        U.m = a.n_kv - 1 - u / BH;
-        bh = u % BH;
+    if (kCausal) {            // the dynamic order of fa_fwd_kernel.cuh
+        dynamic_order(u, BH, a.n_kv, a.chunk, U.m, bh);
     } else {                  // consecutive units share a head's K/V in L2
         U.m = u % a.n_kv;
         bh = u / a.n_kv;
@@ -130,7 +134,12 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
     auto bar = [&](int i) -> uint32_t { return base + C::BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::MISC_OFF + 4);
-
+    // Causal: the dynamic order of fa_fwd_kernel.cuh (one CTA per unit).  The
+    // producer asks for the next unit once it has issued the loads of the
+    // current one; the k-th answer goes to slot k % CLC_DEPTH, the producer
+    // publishes its block index there (-1: none left), and the MMA warp and
+    // the 4 softmax warps read it and release the slot.
+    volatile int *unit_slot = reinterpret_cast<volatile int *>(gbase + C::UNIT_OFF);
     if (warp == 5) tmem_alloc(base + C::MISC_OFF, C::TMEM_COLS);
     if (tid == 0) {
         *abort_flag = 0u;
@@ -149,6 +158,11 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         mbar_init(bar(C::B_OEMPTY), 4);
         mbar_init(bar(C::B_MMADONE), 1);
+        for (int q = 0; kCausal && q < C::CLC_DEPTH; ++q) {
+            mbar_init(bar(C::B_CLCFULL + q), 1);
+            mbar_init(bar(C::B_UNIT + q), 1);
+            mbar_init(bar(C::B_CLCEMPTY + q), 5);
+        }
         fence_barrier_init();
     }
     tc_fence_before();
@@ -178,8 +192,25 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
                 return true;
             };
-            for (int u = blockIdx.x, st = unit_stride0(kCausal); ok && u < a.n_units;
-                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+            uint32_t kq = 0;                        // causal: requests issued
+            bool clc_pending = false;
+            auto next_u = [&]() __attribute__((always_inline)) -> int {
+                    if (!ok) return -1;
+                const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+                ++kq;
+                if (!mbar_wait(bar(C::B_CLCEMPTY + q), ph ^ 1u, w, 3)) { ok = false; return -1; }
+                mbar_arrive_expect_tx(bar(C::B_CLCFULL + q), 16u);
+                clc_try_cancel(base + C::CLC_OFF + 16u * q, bar(C::B_CLCFULL + q));
+                clc_pending = true;
+                if (!mbar_wait(bar(C::B_CLCFULL + q), ph, w, 4)) { ok = false; return -1; }
+                clc_pending = false;
+                const int nu = clc_block(base + C::CLC_OFF + 16u * q);
+                unit_slot[q] = nu;
+                mbar_arrive(bar(C::B_UNIT + q));        // release: the index is visible
+                return nu;
+            };
+            for (int u = blockIdx.x, st = unit_stride0(kCausal); ok && (!kCausal || u >= 0) && u < a.n_units;
+                 u = kCausal ? next_u() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const UnitF8 U = make_unit_f8<kCausal>(u, a);
                 const uint32_t qs = qc % C::NQ, qph = (qc / C::NQ) & 1u;
                 ok = mbar_wait(bar(C::B_QEMPTY + qs), qph ^ 1u, w, 1);
@@ -202,6 +233,9 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
                 if (ok) ok = load_kv(&tm_v, U, 0);
             }
             // Let every copy this lane issued land before the CTA can exit.
+            if (kCausal && clc_pending)
+                mbar_wait_quiet(bar(C::B_CLCFULL + (kq - 1) % C::CLC_DEPTH),
+                                ((kq - 1) / C::CLC_DEPTH) & 1u, 500000000ull);
             for (int s = 0; s < C::NSTAGE; ++s)
                 if (armed & (1u << s))
                     mbar_wait_quiet(bar(C::B_KVFULL + s), (armed_par >> s) & 1u, 500000000ull);
@@ -221,8 +255,19 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             p_out = phase;
             if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
         };
-        for (int u = blockIdx.x, st = unit_stride0(kCausal); ok && u < a.n_units;
-             u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+        uint32_t kq = 0;                            // causal: answers read
+        auto next_u = [&]() __attribute__((always_inline)) -> int {
+            if (!ok) return -1;
+            const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+            ++kq;
+            if (!mbar_wait_warp(bar(C::B_UNIT + q), ph, w, 35)) { ok = false; return -1; }
+            const int nu = unit_slot[q];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_CLCEMPTY + q));
+            return nu;
+        };
+        for (int u = blockIdx.x, st = unit_stride0(kCausal); ok && (!kCausal || u >= 0) && u < a.n_units;
+                 u = kCausal ? next_u() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const UnitF8 U = make_unit_f8<kCausal>(u, a);
             const uint32_t qs = qc % C::NQ, qph = (qc / C::NQ) & 1u;
             ++qc;
@@ -335,8 +380,20 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             return true;
         };
 
-        for (int u = blockIdx.x, st = unit_stride0(kCausal); ok && u < a.n_units;
-             u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+        uint32_t kq = 0;                            // causal: answers read
+        // (a failed wait leaves this loop by break, so ok holds here)
+        auto next_u = [&]() __attribute__((always_inline)) -> int {
+            const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+            ++kq;
+            ok = mbar_wait(bar(C::B_UNIT + q), ph, w, 45);
+            if (__any_sync(0xffffffffu, !ok)) { ok = false; return -1; }
+            const int nu = unit_slot[q];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_CLCEMPTY + q));
+            return nu;
+        };
+        for (int u = blockIdx.x, st = unit_stride0(kCausal); ok && (!kCausal || u >= 0) && u < a.n_units;
+                 u = kCausal ? next_u() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const UnitF8 U = make_unit_f8<kCausal>(u, a);
             // The Q tile's scale and the largest V scale of the head (the
             // per-tile V scales are folded into P' relative to it).
