@@ -78,6 +78,10 @@ typedef enum {
  * Accumulation is FP32; P is rounded to `dtype` before the P V product and
  * the softmax denominator sums those same rounded values; O is rounded to
  * `dtype` round-to-nearest-even.
+ * Causal launches have one CTA per work unit and let running CTAs take over
+ * those not yet started (cluster launch control), in an order that keeps
+ * groups of heads together for L2 reuse of K and V; which CTA computes a
+ * tile varies from launch to launch, the results do not.
  */
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o,
                  float *lse, int B, int H, int N, int d, float alpha,

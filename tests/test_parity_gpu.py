@@ -181,6 +181,23 @@ def test_deterministic_bits_lse_optional_and_side_stream(gpu_lib):
     assert torch.equal(o1, o2) and torch.equal(l1, l2) and torch.equal(o1, o3)
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_causal_dynamic_order_repeats_bits(gpu_lib, d):
+    # Causal launches hand units to CTAs dynamically (which CTA runs which
+    # tile differs between launches); every launch must give the same bits,
+    # with one K/V head per query head and with grouped K/V heads.
+    B, H, N = 3, 8, 1300
+    q, k, v = (x.cuda() for x in synth.qkv(B, H, N, d, seed=21))
+    a = synth.default_alpha(d)
+    runs = [gpu_lib.attention(q, k, v, causal=True, alpha=a) for _ in range(3)]
+    kg, vg = k[:, :, :2].contiguous(), v[:, :, :2].contiguous()
+    runs_g = [gpu_lib.attention(q, kg, vg, causal=True, alpha=a) for _ in range(3)]
+    assert gpu_lib.fa_check_status() == gpu_lib.FA_OK
+    for rs in (runs, runs_g):
+        for o, l in rs[1:]:
+            assert torch.equal(o, rs[0][0]) and torch.equal(l, rs[0][1])
+
+
 def _offset16(n, dtype):
     """A device buffer of n elements that starts 16 bytes past a 32-byte
     boundary (torch allocations are 256-byte aligned)."""
