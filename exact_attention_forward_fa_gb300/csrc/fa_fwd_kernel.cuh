@@ -9,11 +9,13 @@
 // How (the Blackwell forward schedule of "FlashAttention v1-v4", FA4
 // sections "TMEM", "forward schedule: two Q tiles, two softmax groups" and
 // "conditional rescale", re-planned for GB300):
-//   * Persistent grid, one CTA per SM.  A work unit is a pair of 128-row Q
-//     tiles (tile L = 2p, tile H = 2p+1) of one (b, h); both share one
-//     stream of 128-key K/V tiles, visited in descending order so that the
-//     masked tiles (sequence tail, causal diagonal) come first
-//     ("FlashAttention-3 on Hopper", sec. 4.7).
+//   * A work unit is a pair of 128-row Q tiles (tile L = 2p, tile H = 2p+1)
+//     of one (b, h); both share one stream of 128-key K/V tiles, visited in
+//     descending order so that the masked tiles (sequence tail, causal
+//     diagonal) come first ("FlashAttention-3 on Hopper", sec. 4.7).
+//     Persistent grid, one CTA per SM, except for causal units, which are
+//     scheduled dynamically (make_unit): one CTA per unit, running CTAs
+//     taking over those not yet started.
 //   * 384 threads; warpgroup 2 (warps 8-11) gives registers to the two
 //     softmax warpgroups with setmaxnreg.  Warps 10-11 are spare.
 //   * Warp 8 (one lane) is the TMA producer: Q_L/Q_H once per unit into
