@@ -1,7 +1,8 @@
 // fa_fwd_fp8_1q_kernel.cuh -- FP8 (e4m3) attention forward with one
 // 128-row Q tile per work unit, used at head dim 256, on sm_103a.  (The
 // template also compiles for d = 128, where it measured slower than the
-// two-Q-tile kernel: 1123 against 1524 TFLOP/s at B4 H16 N4096.)
+// two-Q-tile kernel: 1123 against 1524 TFLOP/s at B4 H16 N4096 when both
+// used the shift of 8.)
 //
 // What it computes is the FP8 forward of fa_fwd_kernel.cuh ("FlashAttention-3
 // on Hopper", sec. 6.3: e4m3 operands with one FP32 scale per 128-row tile;

@@ -223,8 +223,9 @@ fa_status fa_quantize_fp8_granular(const void *x, uint8_t *x8, float *scales,
  * Hopper", sec. 6.3: descales folded into the softmax scale per tile
  * pair; "03 FA3", sec. 4: the exponent of the FP8 probabilities shifted
  * into the e4m3 range: P' = 2^(s - r + c) with the reference r moved when
- * a tile's row max exceeds it by more than tau; c = 8, tau = 0.8 at
- * d = 128 and c = 4, tau = 4.8 at d = 256, so P' <= 2^8.8 < 448).
+ * a tile's row max exceeds it by more than tau; c = 4, tau = 4.8, so
+ * P' <= 2^8.8 < 448: the pages' c = 8 would leave tau = 0.8 and a rescale
+ * on about half of the steps of outlier inputs).
  *   q8, k8, v8 : device, uint8 e4m3 [B][N][H][d], 16-byte aligned.
  *   q_scale, k_scale, v_scale : device, float [B][H][ceil(N/128)].
  *   o   : device, bf16 [B][N][H][d] (written).  lse : as for fa_fwd.
