@@ -638,6 +638,20 @@ static fa_status bwd_impl(const void *q, const void *k, const void *v, const voi
     L.args.wr = wr;
     L.args.sc_pre = static_cast<float>(cap_pre);
     L.args.sc_post = static_cast<float>(static_cast<double>(softcap) * 1.4426950408889634);
+    if (causal && !win) {
+        // (chunk shares wl's storage: set only here, where no window is read)
+        // the forward's dynamic order (set_dynamic_order): one CTA per unit in
+        // both main kernels, groups of heads whose streamed inputs (K and V
+        // for dQ, Q and dO for dK/dV) fit 32 MiB
+        L.grid = static_cast<int>(units);
+        L.grid_kv = static_cast<int>(units_kv);
+        const uint64_t per_head = 4ull * static_cast<uint64_t>(N) * d;
+        uint64_t c = (32ull << 20) / per_head;
+        const uint64_t bh = static_cast<uint64_t>(B) * H;
+        if (c < 1) c = 1;
+        if (c > bh) c = bh;
+        L.args.chunk = static_cast<int>(c);
+    }
     cudaError_t e = softcap > 0.f ? fa::launch_bwd_win_softcap(L)
                     : win         ? fa::launch_bwd_win(L)
                                   : fa::launch_bwd(L);

@@ -62,8 +62,15 @@ struct BwdArgs {
     float scale_log2;      // alpha * log2(e)
     float alpha;
     // Local window (kWin instantiations): key j is hidden from query i when
-    // j > i + wr (wr >= 0) or j < i - wl (wl >= 0); -1 is no bound.
-    int wl, wr;
+    // j > i + wr (wr >= 0) or j < i - wl (wl >= 0); -1 is no bound.  Causal
+    // without a window: both main kernels take their units in the dynamic
+    // order of the forward (make_bwd_unit), whose groups hold chunk heads;
+    // chunk shares wl's storage (the two never meet in one launch).
+    union {
+        int wl;
+        int chunk;
+    };
+    int wr;
     // Softcap c (kCap instantiations): the score is c tanh(alpha s / c),
     // t = tanh(sc_pre s) with sc_pre = alpha / c, in log2 units sc_post t
     // with sc_post = c log2(e); dS picks up the factor 1 - t^2.
@@ -97,6 +104,7 @@ struct BwdCfg {
     static constexpr uint32_t TILE = NCH * CHUNK;        // one 128 x D tile
     static constexpr int NTHREADS = 320;
     static constexpr int N_EW = 8;                        // elementwise warps
+    static constexpr int CLC_DEPTH = 4;                   // causal: answers in flight
     static constexpr uint32_t TMEM_COLS = 512;
     // S = Q K^T style: both operands K-major, M = N = 128
     static constexpr uint32_t IDESC_SS = idesc_f16(128, 128, kBF16, false, false);
@@ -114,9 +122,14 @@ struct BwdCfg {
                          DQB_SFREE = 4, DQB_DSFULL = 5 /* x2 */, DQB_DQFULL = 7,
                          DQB_DQEMPTY = 8, DQB_MMADONE = 9, DQB_KFULL = 10,
                          DQB_KEMPTY = DQB_KFULL + KN, DQB_VFULL = DQB_KEMPTY + KN,
-                         DQB_VEMPTY = DQB_VFULL + VN, DQ_NBAR = DQB_VEMPTY + VN;
+                         DQB_VEMPTY = DQB_VFULL + VN,
+                         // causal: the dynamic order's answers (see the kernel)
+                         DQB_CLCFULL = DQB_VEMPTY + VN, DQB_UNIT = DQB_CLCFULL + 4,
+                         DQB_CLCEMPTY = DQB_UNIT + 4, DQ_NBAR = DQB_CLCEMPTY + 4;
     static constexpr uint32_t DQ_MISC_OFF = DQ_BAR_OFF + DQ_NBAR * 8;
-    static constexpr uint32_t DQ_SMEM = DQ_MISC_OFF + 16 + 1024;
+    static constexpr uint32_t DQ_CLC_OFF = (DQ_MISC_OFF + 16 + 15) & ~15u;   // 16-byte aligned
+    static constexpr uint32_t DQ_UNIT_OFF = DQ_CLC_OFF + 4 * 16;
+    static constexpr uint32_t DQ_SMEM = DQ_UNIT_OFF + 4 * 4 + 1024;
     // TMEM: S [0,128), dP [128,256), dQ [256,256+D), dS0, dS1 (64 columns each)
     static constexpr uint32_t DQ_COL_S = 0, DQ_COL_DP = 128, DQ_COL_DQ = 256,
                               DQ_COL_DS = 256 + D;
@@ -132,9 +145,13 @@ struct BwdCfg {
                          KVB_MMADONE = 8, KVB_QFULL = 9, KVB_QEMPTY = KVB_QFULL + QN,
                          KVB_DOFULL = KVB_QEMPTY + QN, KVB_DOEMPTY = KVB_DOFULL + DN,
                          KVB_STFULL1 = KVB_DOEMPTY + DN, KVB_PFULL1 = KVB_STFULL1 + 1,
-                         KV_NBAR = KVB_PFULL1 + 1;
+                         // causal: the dynamic order's answers (see the kernel)
+                         KVB_CLCFULL = KVB_PFULL1 + 1, KVB_UNIT = KVB_CLCFULL + 4,
+                         KVB_CLCEMPTY = KVB_UNIT + 4, KV_NBAR = KVB_CLCEMPTY + 4;
     static constexpr uint32_t KV_MISC_OFF = KV_BAR_OFF + KV_NBAR * 8;
-    static constexpr uint32_t KV_SMEM = KV_MISC_OFF + 16 + 1024;
+    static constexpr uint32_t KV_CLC_OFF = (KV_MISC_OFF + 16 + 15) & ~15u;   // 16-byte aligned
+    static constexpr uint32_t KV_UNIT_OFF = KV_CLC_OFF + 4 * 16;
+    static constexpr uint32_t KV_SMEM = KV_UNIT_OFF + 4 * 4 + 1024;
     // TMEM: S^T [0,128) (P^T over its first 64), dP^T [128,256) (dS^T over
     // its first 64), dV [256,256+D), dK [256+D,256+2D); at d = 64 a second
     // S^T buffer [384,512), so the S^T of query tile i+2 is computed while
@@ -192,7 +209,13 @@ __device__ __forceinline__ BwdUnit make_bwd_unit(int u, const BwdArgs &a) {
     const int HH = kKeyTiles ? a.H / a.group : a.H;     // K/V heads for key tiles
     const int BH = a.B * HH;
     int bh;
-    if (bwd_longest_first<kCausal, kWin>(a)) {
+    if (kCausal && !kWin) {
+        // the forward's dynamic order (fa_fwd_kernel.cuh): unit i of a head
+        // is its (i+1)-th longest; dQ: query tile i, dK/dV: key tile n_t-1-i
+        int i;
+        dynamic_order(u, BH, a.n_t, a.chunk, i, bh);
+        U.m = kKeyTiles ? a.n_t - 1 - i : i;
+    } else if (bwd_longest_first<kCausal, kWin>(a)) {
         const int k = u / BH;
         U.m = kKeyTiles ? k : a.n_t - 1 - k;
         bh = u % BH;
@@ -373,6 +396,13 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     auto bar = [&](int i) -> uint32_t { return base + C::DQ_BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::DQ_MISC_OFF + 4);
+    // Causal without a window: one CTA per unit, running CTAs take over those
+    // not yet started (clc_try_cancel).  The producer asks for the next unit
+    // once it has issued the current one's loads; the k-th answer goes to
+    // slot k % CLC_DEPTH, the producer publishes its block index there (-1:
+    // none left), and the MMA warp and the 8 elementwise warps read it.
+    constexpr bool kDyn = kCausal && !kWin;
+    volatile int *unit_slot = reinterpret_cast<volatile int *>(gbase + C::DQ_UNIT_OFF);
     // key tiles [lo, hi) of query tile U.m, visited from hi - 1 down
     auto key_range = [&](const BwdUnit &U, int &lo, int &hi) {
         if constexpr (kWin) {
@@ -398,6 +428,11 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_init(bar(C::DQB_DQFULL), 1);
         mbar_init(bar(C::DQB_DQEMPTY), C::N_EW);
         mbar_init(bar(C::DQB_MMADONE), 1);
+        for (int q = 0; kDyn && q < C::CLC_DEPTH; ++q) {
+            mbar_init(bar(C::DQB_CLCFULL + q), 1);
+            mbar_init(bar(C::DQB_UNIT + q), 1);
+            mbar_init(bar(C::DQB_CLCEMPTY + q), 1 + C::N_EW);
+        }
         for (int s = 0; s < C::KN; ++s) {
             mbar_init(bar(C::DQB_KFULL + s), 1);
             mbar_init(bar(C::DQB_KEMPTY + s), 1);
@@ -426,8 +461,25 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t nk = 0, nv = 0;
             int qn = 0;
             bool ok = true;
-            for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
-                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+            uint32_t kq = 0;                        // causal: requests issued
+            bool clc_pending = false;               // a request without its answer
+            auto next_dyn = [&]() __attribute__((always_inline)) -> int {
+                if (!ok) return -1;
+                const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+                ++kq;
+                if (!mbar_wait(bar(C::DQB_CLCEMPTY + q), ph ^ 1u, w, 53)) { ok = false; return -1; }
+                mbar_arrive_expect_tx(bar(C::DQB_CLCFULL + q), 16u);
+                clc_try_cancel(base + C::DQ_CLC_OFF + 16u * q, bar(C::DQB_CLCFULL + q));
+                clc_pending = true;
+                if (!mbar_wait(bar(C::DQB_CLCFULL + q), ph, w, 54)) { ok = false; return -1; }
+                clc_pending = false;
+                const int nu = clc_block(base + C::DQ_CLC_OFF + 16u * q);
+                unit_slot[q] = nu;
+                mbar_arrive(bar(C::DQB_UNIT + q));    // release: the index is visible
+                return nu;
+            };
+            for (int u = blockIdx.x, st = unit_stride0(snake); ok && (!kDyn || u >= 0) && u < a.n_units;
+                     u = kDyn ? next_dyn() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
                 ok = mbar_wait(bar(C::DQB_QEMPTY), (qn & 1) ^ 1, w, 50);
                 if (!ok) break;
@@ -455,6 +507,9 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     ++nv;
                 }
             }
+            if (kDyn && clc_pending)
+                mbar_wait_quiet(bar(C::DQB_CLCFULL + (kq - 1) % C::CLC_DEPTH),
+                                ((kq - 1) / C::CLC_DEPTH) & 1u, 500000000ull);
             RK::drain(nk, C::DQB_KFULL, base + C::DQ_BAR_OFF);
             RV::drain(nv, C::DQB_VFULL, base + C::DQ_BAR_OFF);
             if (qn > 0) mbar_wait_quiet(bar(C::DQB_QFULL), (qn - 1) & 1, 500000000ull);
@@ -476,8 +531,19 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         auto wait_v = [&](uint32_t i) {
             return mbar_wait_warp(bar(C::DQB_VFULL + RV::slot(i)), RV::phase(i), w, 62);
         };
-        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
-                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+        uint32_t kq = 0;                            // causal: answers read
+        auto next_dyn = [&]() __attribute__((always_inline)) -> int {
+            if (!ok) return -1;
+            const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+            ++kq;
+            if (!mbar_wait_warp(bar(C::DQB_UNIT + q), ph, w, 64)) { ok = false; return -1; }
+            const int nu = unit_slot[q];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::DQB_CLCEMPTY + q));
+            return nu;
+        };
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && (!kDyn || u >= 0) && u < a.n_units;
+                 u = kDyn ? next_dyn() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
             int klo_t, khi_t;
             key_range(U, klo_t, khi_t);
@@ -549,8 +615,20 @@ fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const float sl2 = a.scale_log2;
         uint32_t sph = 0, dpph = 0, dqph = 0;
         bool ok = true;
-        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units;
-                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+        uint32_t kq = 0;                            // causal: answers read
+        auto next_dyn = [&]() __attribute__((always_inline)) -> int {
+            if (!ok) return -1;
+            const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+            ++kq;
+            ok = mbar_wait(bar(C::DQB_UNIT + q), ph, w, 73);
+            if (__any_sync(0xffffffffu, !ok)) { ok = false; return -1; }
+            const int nu = unit_slot[q];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::DQB_CLCEMPTY + q));
+            return nu;
+        };
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && (!kDyn || u >= 0) && u < a.n_units;
+                 u = kDyn ? next_dyn() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const BwdUnit U = make_bwd_unit<kCausal, false, kWin>(u, a);
             int klo_t, khi_t;
             key_range(U, klo_t, khi_t);
@@ -701,6 +779,13 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     auto bar = [&](int i) -> uint32_t { return base + C::KV_BAR_OFF + 8u * i; };
     volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF);
     volatile uint32_t *abort_flag = reinterpret_cast<volatile uint32_t *>(gbase + C::KV_MISC_OFF + 4);
+    // Causal without a window: one CTA per unit, running CTAs take over those
+    // not yet started (clc_try_cancel).  The producer asks for the next unit
+    // once it has issued the current one's loads; the k-th answer goes to
+    // slot k % CLC_DEPTH, the producer publishes its block index there (-1:
+    // none left), and the MMA warp and the 8 elementwise warps read it.
+    constexpr bool kDyn = kCausal && !kWin;
+    volatile int *unit_slot = reinterpret_cast<volatile int *>(gbase + C::KV_UNIT_OFF);
     // query tiles [lo, hi) that see key tile U.m
     auto query_range = [&](const BwdUnit &U, int &lo, int &hi) {
         if constexpr (kWin) {
@@ -731,6 +816,11 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_init(bar(C::KVB_ACCFULL), 1);
         mbar_init(bar(C::KVB_ACCEMPTY), C::N_EW);
         mbar_init(bar(C::KVB_MMADONE), 1);
+        for (int q = 0; kDyn && q < C::CLC_DEPTH; ++q) {
+            mbar_init(bar(C::KVB_CLCFULL + q), 1);
+            mbar_init(bar(C::KVB_UNIT + q), 1);
+            mbar_init(bar(C::KVB_CLCEMPTY + q), 1 + C::N_EW);
+        }
         for (int s = 0; s < C::QN; ++s) {
             mbar_init(bar(C::KVB_QFULL + s), 1);
             mbar_init(bar(C::KVB_QEMPTY + s), 1);
@@ -757,8 +847,25 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             uint32_t nq = 0, n_qc = 0, n_dc = 0;     // tiles; Q and dO copies issued
             int kvn = 0;
             bool ok = true;
-            for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units_kv;
-                     u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+            uint32_t kq = 0;                        // causal: requests issued
+            bool clc_pending = false;               // a request without its answer
+            auto next_dyn = [&]() __attribute__((always_inline)) -> int {
+                if (!ok) return -1;
+                const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+                ++kq;
+                if (!mbar_wait(bar(C::KVB_CLCEMPTY + q), ph ^ 1u, w, 83)) { ok = false; return -1; }
+                mbar_arrive_expect_tx(bar(C::KVB_CLCFULL + q), 16u);
+                clc_try_cancel(base + C::KV_CLC_OFF + 16u * q, bar(C::KVB_CLCFULL + q));
+                clc_pending = true;
+                if (!mbar_wait(bar(C::KVB_CLCFULL + q), ph, w, 84)) { ok = false; return -1; }
+                clc_pending = false;
+                const int nu = clc_block(base + C::KV_CLC_OFF + 16u * q);
+                unit_slot[q] = nu;
+                mbar_arrive(bar(C::KVB_UNIT + q));    // release: the index is visible
+                return nu;
+            };
+            for (int u = blockIdx.x, st = unit_stride0(snake); ok && (!kDyn || u >= 0) && u < a.n_units_kv;
+                     u = kDyn ? next_dyn() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
                 const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
                 ok = mbar_wait(bar(C::KVB_KVEMPTY), (kvn & 1) ^ 1, w, 80);
                 if (!ok) break;
@@ -795,6 +902,9 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     ++n_dc;
                 }
             }
+            if (kDyn && clc_pending)
+                mbar_wait_quiet(bar(C::KVB_CLCFULL + (kq - 1) % C::CLC_DEPTH),
+                                ((kq - 1) / C::CLC_DEPTH) & 1u, 500000000ull);
             RQ::drain(n_qc, C::KVB_QFULL, base + C::KV_BAR_OFF);
             RO::drain(n_dc, C::KVB_DOFULL, base + C::KV_BAR_OFF);
             if (kvn > 0) mbar_wait_quiet(bar(C::KVB_KVFULL), (kvn - 1) & 1, 500000000ull);
@@ -811,8 +921,19 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         auto wait_do = [&](uint32_t i) {
             return mbar_wait_warp(bar(C::KVB_DOFULL + RO::slot(i)), RO::phase(i), w, 96);
         };
-        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units_kv;
-                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+        uint32_t kq = 0;                            // causal: answers read
+        auto next_dyn = [&]() __attribute__((always_inline)) -> int {
+            if (!ok) return -1;
+            const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+            ++kq;
+            if (!mbar_wait_warp(bar(C::KVB_UNIT + q), ph, w, 94)) { ok = false; return -1; }
+            const int nu = unit_slot[q];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::KVB_CLCEMPTY + q));
+            return nu;
+        };
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && (!kDyn || u >= 0) && u < a.n_units_kv;
+                 u = kDyn ? next_dyn() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
             int qlo_t, qhi_t;
             query_range(U, qlo_t, qhi_t);
@@ -893,8 +1014,20 @@ fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const float2 c2 = make_float2(sl2, sl2);
         uint32_t stn = 0, dpph = 0, accph = 0;    // stn: S^T tiles of this CTA so far
         bool ok = true;
-        for (int u = blockIdx.x, st = unit_stride0(snake); ok && u < a.n_units_kv;
-                 u += st, st = 2 * static_cast<int>(gridDim.x) - st) {
+        uint32_t kq = 0;                            // causal: answers read
+        auto next_dyn = [&]() __attribute__((always_inline)) -> int {
+            if (!ok) return -1;
+            const uint32_t q = kq % C::CLC_DEPTH, ph = (kq / C::CLC_DEPTH) & 1u;
+            ++kq;
+            ok = mbar_wait(bar(C::KVB_UNIT + q), ph, w, 103);
+            if (__any_sync(0xffffffffu, !ok)) { ok = false; return -1; }
+            const int nu = unit_slot[q];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::KVB_CLCEMPTY + q));
+            return nu;
+        };
+        for (int u = blockIdx.x, st = unit_stride0(snake); ok && (!kDyn || u >= 0) && u < a.n_units_kv;
+                 u = kDyn ? next_dyn() : u + st, st = 2 * static_cast<int>(gridDim.x) - st) {
             const BwdUnit U = make_bwd_unit<kCausal, true, kWin>(u, a);
             int i0, qhi_t;
             query_range(U, i0, qhi_t);

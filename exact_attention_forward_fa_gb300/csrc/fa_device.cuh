@@ -176,6 +176,25 @@ __device__ __forceinline__ int clc_block(uint32_t resp) {
     return ok ? static_cast<int>(cx) : -1;
 }
 
+// The dynamic causal order (clc_try_cancel schedules it): groups of chunk
+// heads, longest unit first within a group, every head's shortest unit last.
+// Position u over BH heads of n units each (unit i of a head is its
+// (i+1)-th shortest): the unit index i and the head bh.
+__device__ __forceinline__ void dynamic_order(int u, int BH, int n, int chunk, int &i, int &bh) {
+    const int n1 = n - 1;                          // units per head before the tail
+    const int grouped = BH * n1;
+    if (u < grouped) {
+        const int g = u / (chunk * n1);
+        const int r = u - g * chunk * n1;
+        const int cg = min(chunk, BH - g * chunk); // heads in this group
+        i = n1 - r / cg;
+        bh = g * chunk + r % cg;
+    } else {
+        i = 0;
+        bh = u - grouped;
+    }
+}
+
 // 4-D tiled store of a box from shared memory (bulk-group completion).  Out-of-
 // range parts of the box are not written; every coordinate is >= 0 and c0
 // is 16-byte aligned in bytes.

@@ -207,24 +207,6 @@ __device__ __forceinline__ constexpr bool dynamic_units() {
     return kCausal && !kSplit && !kExt && !kPack;
 }
 
-// Position u of that order over BH heads of n causal units each (the
-// one-Q-tile kernels: unit i of a head is its i-th Q tile): the unit index
-// i and the head bh.
-__device__ __forceinline__ void dynamic_order(int u, int BH, int n, int chunk, int &i, int &bh) {
-    const int n1 = n - 1;                          // units per head before the tail
-    const int grouped = BH * n1;
-    if (u < grouped) {
-        const int g = u / (chunk * n1);
-        const int r = u - g * chunk * n1;
-        const int cg = min(chunk, BH - g * chunk); // heads in this group
-        i = n1 - r / cg;
-        bh = g * chunk + r % cg;
-    } else {
-        i = 0;
-        bh = u - grouped;
-    }
-}
-
 template <bool kCausal, bool kSplit, bool kExt = false, bool kPack = false>
 __device__ __forceinline__ Unit make_unit(int u, const FwdArgs &a) {
     Unit U;
