@@ -198,6 +198,44 @@ def test_causal_dynamic_order_repeats_bits(gpu_lib, d):
             assert torch.equal(o, rs[0][0]) and torch.equal(l, rs[0][1])
 
 
+@pytest.mark.parametrize("B,H,N,d", [(32, 64, 640, 64), (4, 16, 4096, 128), (2, 8, 2000, 256)])
+def test_dynamic_order_writes_every_row(gpu_lib, B, H, N, d):
+    # Causal launches have one CTA per unit and let running CTAs take over
+    # the others (up to 6144 here).  O and LSE start as NaN: a unit that no
+    # CTA ran would leave NaN rows, one that ran twice would still give the
+    # same values, so every row must come out finite and equal to a
+    # launch's own bits on the second run.
+    fa = gpu_lib
+    q, k, v = (x.cuda() for x in synth.qkv(B, H, N, d, seed=33))
+    a = synth.default_alpha(d)
+    outs = []
+    for _ in range(2):
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+        assert fa.fa_fwd(q, k, v, o, lse, B, H, N, d, a, 1, fa.FA_BF16) == fa.FA_OK
+        outs.append((o, lse))
+    assert fa.fa_check_status() == fa.FA_OK
+    for o, lse in outs:
+        assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+def test_dynamic_order_backward_writes_every_row(gpu_lib):
+    # The causal backward's two main kernels take the same dynamic order:
+    # dQ, dK, dV start as NaN and must come out finite everywhere.
+    fa = gpu_lib
+    B, H, N, d = 8, 16, 1500, 128
+    q, k, v = (x.cuda() for x in synth.qkv(B, H, N, d, seed=34))
+    do = torch.from_numpy(synth.normal((B, N, H, d), seed=35)).to(q.dtype).cuda()
+    a = synth.default_alpha(d)
+    o, lse = fa.attention(q, k, v, causal=True, alpha=a)
+    g = [torch.full_like(q, float("nan")) for _ in range(3)]
+    ws = torch.empty((fa.bwd_workspace_floats(B, H, N),), dtype=torch.float32, device="cuda")
+    assert fa.fa_bwd(q, k, v, o, do, lse, ws, *g, B, H, N, d, a, 1, fa.FA_BF16) == fa.FA_OK
+    assert fa.fa_check_status() == fa.FA_OK
+    assert all(bool(torch.isfinite(x).all()) for x in g)
+
+
 def _offset16(n, dtype):
     """A device buffer of n elements that starts 16 bytes past a 32-byte
     boundary (torch allocations are 256-byte aligned)."""
