@@ -509,7 +509,11 @@ def run_reference(args, B, H, N, d, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": config_name(B, H, N, d, args.causal).replace(
                 "attention fwd", "attention bwd") + variant_suffix(var), "B": B,
-                       "H": H, "N": N, "d": d, "causal": args.causal},
+                       "H": H, "N": N, "d": d, "causal": bool(args.causal),
+                       **({"variant": var, "flops": "2.5 x 4 d per visible (row, key) pair"}
+                          if var else {}),
+                       "l2": "no flush: 320 MiB of inputs exceed the 126 MB L2",
+                       "parallelism": f"replicas x{world}"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -536,8 +540,11 @@ def run_reference(args, B, H, N, d, rank, world):
         "ms_per_step": 1e3 * secs / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": config_name(B, H, N, d, args.causal) + variant_suffix(var),
-                   "B": B, "H": H, "N": N, "d": d, "causal": args.causal,
-                   **({"variant": var} if var else {})},
+                   "B": B, "H": H, "H_kv": args.hkv or H, "N": N, "d": d,
+                   "causal": bool(args.causal), **({"variant": var,
+                   "flops": "4 d per visible (row, key) pair"} if var else {}),
+                   "l2": "no flush: 192 MiB of inputs exceed the 126 MB L2",
+                   "parallelism": f"replicas x{world}"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
                          "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
