@@ -109,10 +109,18 @@ struct FwdCfg {
     static constexpr uint32_t REGS_LOW = 96, REGS_HIGH = 200;
     static_assert(128 * REGS_LOW + 256 * REGS_HIGH <= 384 * 168, "register budget");
 
-    // shared memory map (offsets from a 1024-B aligned base)
+    // d = 64: the row sum of the rounded P comes from the tensor core, as a
+    // 16-column accumulator L_X += P_X 1 next to O_X (TMEM has room at d = 64;
+    // at d = 128 S and O fill it), which takes 128 additions per tile off
+    // the softmax warps.
+    static constexpr bool kLMMA = D == 64 && !kFP8;
+    // shared memory map (offsets from a 1024-B aligned base); ONES: a 2 KB
+    // block of 16-bit ones, the B operand of the L product (every element
+    // it reads is 1, so one descriptor serves every key step)
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t KV_OFF = NQ * TILE_BYTES;
-    static constexpr uint32_t BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
+    static constexpr uint32_t ONES_OFF = KV_OFF + NSTAGE * TILE_BYTES;
+    static constexpr uint32_t BAR_OFF = ONES_OFF + (kLMMA ? 2048u : 0u);
     // barrier indices
     static constexpr int B_QFULL = 0, B_QEMPTY = NQ, B_KVFULL = 2 * NQ,
                          B_KVEMPTY = 2 * NQ + NSTAGE, B_SFULL = 2 * NQ + 2 * NSTAGE,
@@ -135,11 +143,14 @@ struct FwdCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     __host__ __device__ static constexpr uint32_t col_s(int x) { return x ? 128u : 0u; }
     __host__ __device__ static constexpr uint32_t col_o(int x) { return 256u + (x ? D : 0u); }
+    __host__ __device__ static constexpr uint32_t col_l(int x) { return 256u + 2u * D + (x ? 16u : 0u); }
+    static_assert(!kLMMA || col_l(1) + 16 <= TMEM_COLS, "TMEM budget of L");
 
     static constexpr uint32_t IDESC_QK =
         kFP8 ? idesc_e4m3(128, 128, false, false) : idesc_f16(128, 128, kBF16, false, false);
     static constexpr uint32_t IDESC_PV =
         kFP8 ? idesc_e4m3(128, D, false, true) : idesc_f16(128, D, kBF16, false, true);
+    static constexpr uint32_t IDESC_L = idesc_f16(128, 16, kBF16, false, true);
     // Conditional-rescale threshold (log2 units).  16-bit P: tau = 8, so
     // P <= 2^8.  FP8 P ("03 FA3", sec. 4, Max_offset): the exponent is
     // shifted by c = 4 into the e4m3 range and tau = 4.8 keeps
@@ -351,6 +362,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         fence_barrier_init();
     }
+    if constexpr (C::kLMMA) {
+        // the ones block (2048 B of 16-bit 1.0), written here and read by the
+        // tensor core: made visible to the async proxy before the barrier
+        const uint32_t one2 = kBF16 ? 0x3F803F80u : 0x3C003C00u;
+        for (int i = tid; i < 512; i += C::NTHREADS)
+            reinterpret_cast<uint32_t *>(gbase + C::ONES_OFF)[i] = one2;
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -502,6 +521,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                                 else
                                     mma_ts_f16_elect(tbase + C::col_o(x), tbase + C::col_s(x) + kk * 8u,
                                                      bd, C::IDESC_PV, (acc | kk) ? 1u : 0u);
+                                if constexpr (C::kLMMA)     // L_X += P_X 1 (row sums of P)
+                                    mma_ts_f16_elect(tbase + C::col_l(x), tbase + C::col_s(x) + kk * 8u,
+                                                     smem_desc_sw128(base + C::ONES_OFF, 16u, 1024u),
+                                                     C::IDESC_L, (acc | kk) ? 1u : 0u);
                             }
                             pph ^= 1;
                             if (t == t1x) mma_commit_elect(bar(C::B_OFULL + x));
@@ -555,6 +578,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tbase + lane_off + C::col_s(x);
         const uint32_t tO = tbase + lane_off + C::col_o(x);
+        const uint32_t tL = tbase + lane_off + (C::kLMMA ? C::col_l(x) : 0u);
         WaitCtx w{abort_flag, a.status, x ? kRoleSoftmax1 : kRoleSoftmax0};
         // With a softcap the scores reaching the softmax are tanh values in
         // [-1, 1], scaled to log2 units by c log2(e).
@@ -783,6 +807,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                         }
                         tmem_st32(tO + ch * 32, ov);
                     }
+                    if constexpr (C::kLMMA) {            // L holds the rounded-P row sum
+                        uint32_t lv[16];
+                        tmem_ld16(tL, lv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            lv[i] = __float_as_uint(__uint_as_float(lv[i]) * corr);
+                        tmem_st16(tL, lv);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -794,7 +827,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                 // instantiation then rounds them alike, whatever the compiler
                 // would contract)
                 le = __fmaf_rn(le, corr, ((e_a.x + e_a.y) + (e_b.x + e_b.y)) * ivr_c);
-                if constexpr (!kFP8) {
+                if constexpr (!kFP8 && !C::kLMMA) {
                     float2 r_a = make_float2(0.f, 0.f), r_b = r_a;
 #pragma unroll
                     for (int i = 0; i < 64; i += 2) {
@@ -809,25 +842,30 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (!ok) break;
             // ---- the row's normaliser and LSE ----
             // 16-bit P: O / l_r.  FP8: O v_max / l (O accumulated P' = P v_j/v_max).
-            const bool live = (le > 0.f) && (kFP8 || lr > 0.f);
-            float inv = live ? (kFP8 ? vmax / le : 1.f / lr) : 0.f;
-            // LSE in log2 units
-            float lse2 = live ? r - C::P_OFFSET + log2f(le) : -INFINITY;
-            if constexpr (kExt) {
-                // Sink ("FlashAttention-3 on Hopper", sec. 4.6): one more
-                // term 2^(sigma log2 e - r) in both row sums, no value.
-                if (a.sinks != nullptr) {
-                    const float sg = a.sinks[U.h] * 1.44269504088896340736f;
-                    if (!live) {
-                        inv = 0.f;
-                        lse2 = sg;
-                    } else {
-                        const float M = fmaxf(r, sg);
-                        lse2 = M + log2f(__fmaf_rn(le, ex2_approx(r - M), ex2_approx(sg - M)));
-                        inv = 1.f / (lr + ex2_approx(sg - r));    // 2^+big -> inf -> 0
+            // (d = 64: l_r is the L accumulator, read with O below.)
+            bool live = false;
+            float inv = 0.f, lse2 = -INFINITY;      // LSE in log2 units
+            auto normalise = [&]() __attribute__((always_inline)) {
+                live = (le > 0.f) && (kFP8 || lr > 0.f);
+                inv = live ? (kFP8 ? vmax / le : 1.f / lr) : 0.f;
+                lse2 = live ? r - C::P_OFFSET + log2f(le) : -INFINITY;
+                if constexpr (kExt) {
+                    // Sink ("FlashAttention-3 on Hopper", sec. 4.6): one more
+                    // term 2^(sigma log2 e - r) in both row sums, no value.
+                    if (a.sinks != nullptr) {
+                        const float sg = a.sinks[U.h] * 1.44269504088896340736f;
+                        if (!live) {
+                            inv = 0.f;
+                            lse2 = sg;
+                        } else {
+                            const float M = fmaxf(r, sg);
+                            lse2 = M + log2f(__fmaf_rn(le, ex2_approx(r - M), ex2_approx(sg - M)));
+                            inv = 1.f / (lr + ex2_approx(sg - r));    // 2^+big -> inf -> 0
+                        }
                     }
                 }
-            }
+            };
+            if constexpr (!C::kLMMA) normalise();
             const int grow = qpos;
             {
                 // ---- epilogue: O / l -> global ----
@@ -842,7 +880,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int ch = 0; ch < D / 32; ++ch)
                     tmem_ld32(tO + ch * 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[ch * 32]));
-                tmem_ld_wait();
+                if constexpr (C::kLMMA) {
+                    uint32_t lv[16];
+                    tmem_ld16(tL, lv);
+                    tmem_ld_wait();
+                    lr = __uint_as_float(lv[0]);
+                    normalise();
+                } else {
+                    tmem_ld_wait();
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(C::B_OEMPTY + x));
