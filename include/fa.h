@@ -266,7 +266,9 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
  * and dP (sec. 7.2, first option), so no atomics are used and the results
  * are identical from run to run.  P and dS are rounded to `dtype` for the
  * GEMMs that consume them; accumulation is FP32; outputs are rounded to
- * `dtype`.  Nothing is allocated.  Errors as fa_fwd.
+ * `dtype`.  Nothing is allocated.  Errors as fa_fwd.  With causal = 1 both
+ * main kernels schedule their units as fa_fwd's causal launches do (one CTA
+ * per unit, head groups kept together for L2 reuse).
  */
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o,
                  const void *dout, const float *lse, float *workspace, void *dq,
