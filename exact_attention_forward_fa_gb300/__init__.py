@@ -34,7 +34,7 @@ FA_SCALE_TENSOR = 2
 
 # Every symbol include/fa.h declares (checked by the tests).
 EXPORTS = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_packed", "fa_fwd_ext", "fa_fwd_splitkv", "fa_splitkv_workspace_floats",
-           "fa_splitkv_auto", "fa_quantize_fp8", "fa_quantize_fp8_granular", "fa_fwd_fp8", "fa_bwd", "fa_bwd_ext", "fa_bwd_noalloc",
+           "fa_splitkv_auto", "fa_quantize_fp8", "fa_quantize_fp8_granular", "fa_fwd_fp8", "fa_fwd_fp8_gqa", "fa_bwd", "fa_bwd_ext", "fa_bwd_noalloc",
            "fa_check_status", "fa_status_detail", "fa_selftest_wait_timeout",
            "fa_status_string", "fa_version")
 
@@ -78,6 +78,8 @@ def load():
     lib.fa_quantize_fp8_granular.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
     lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_fp8_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_fp8_gqa.restype = i
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
     lib.fa_bwd.restype = i
     lib.fa_bwd_ext.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i,
@@ -268,20 +270,35 @@ def quantize_fp8(x, hadamard_signs=None, stream=None, granularity: int = FA_SCAL
     return x8, sc
 
 
+def fa_fwd_fp8_gqa(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B: int, H: int, H_kv: int,
+                   N: int, d: int, alpha: float, causal: int, stream=None) -> int:
+    """Direct call of the C entry point: fa_fwd_fp8 with K/V (codes and
+    scales) over H_kv heads (see include/fa.h)."""
+    return load().fa_fwd_fp8_gqa(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(q_scale), _ptr(k_scale),
+                                 _ptr(v_scale), _ptr(o), _ptr(lse), int(B), int(H), int(H_kv),
+                                 int(N), int(d), float(alpha), int(causal), _stream(stream))
+
+
 def attention_fp8(q8, k8, v8, q_scale, k_scale, v_scale, causal: bool = False,
                   alpha: float | None = None, out=None, lse=None, want_lse: bool = True,
                   stream=None):
-    """FP8 forward on quantized inputs; returns (O bf16, LSE or None)."""
+    """FP8 forward on quantized inputs; returns (O bf16, LSE or None).  K/V
+    may have fewer heads than Q (fa_fwd_fp8_gqa)."""
     import torch
     B, N, H, d = q8.shape
+    H_kv = k8.shape[2]
     if alpha is None:
         alpha = 1.0 / math.sqrt(d)
     if out is None:
         out = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device)
     if lse is None and want_lse:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q8.device)
-    rc = fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, out, lse, B, H, N, d, alpha,
-                    int(bool(causal)), stream)
+    if H_kv == H:
+        rc = fa_fwd_fp8(q8, k8, v8, q_scale, k_scale, v_scale, out, lse, B, H, N, d, alpha,
+                        int(bool(causal)), stream)
+    else:
+        rc = fa_fwd_fp8_gqa(q8, k8, v8, q_scale, k_scale, v_scale, out, lse, B, H, H_kv, N, d,
+                            alpha, int(bool(causal)), stream)
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_fp8")
     return out, lse

@@ -498,12 +498,13 @@ fa_status fa_quantize_fp8_granular(const void *x, uint8_t *x8, float *scales,
     return quantize_impl(x, x8, scales, hadamard_signs, B, H, N, d, granularity, stream);
 }
 
-fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
-                     const float *q_scale, const float *k_scale, const float *v_scale,
-                     void *o, float *lse, int B, int H, int N, int d, float alpha,
-                     int causal, void *stream) {
+static fa_status fwd_fp8_impl(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                              const float *q_scale, const float *k_scale, const float *v_scale,
+                              void *o, float *lse, int B, int H, int H_kv, int N, int d,
+                              float alpha, int causal, void *stream) {
     if (!q8 || !k8 || !v8 || !q_scale || !k_scale || !v_scale || !o) return FA_ERR_INVALID_ARG;
     if (B < 1 || H < 1 || N < 1 || d < 1) return FA_ERR_INVALID_ARG;
+    if (H_kv < 1 || H % H_kv != 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(alpha)) return FA_ERR_INVALID_ARG;
     if (d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
@@ -527,8 +528,8 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     std::memset(&L, 0, sizeof(L));
     const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
     if ((st = encode_bshd(&L.q, q8, dt, B, H, N, d, 128)) != FA_OK) return st;
-    if ((st = encode_bshd(&L.k, k8, dt, B, H, N, d, 128)) != FA_OK) return st;
-    if ((st = encode_bshd(&L.v, v8, dt, B, H, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.k, k8, dt, B, H_kv, N, d, 128)) != FA_OK) return st;
+    if ((st = encode_bshd(&L.v, v8, dt, B, H_kv, N, d, 128)) != FA_OK) return st;
     L.args.o = o;
     L.args.lse = lse;
     L.args.status = dev->status;
@@ -538,7 +539,7 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     L.args.n_kv = static_cast<int>(n_qt);
     L.args.n_pairs = static_cast<int>((n_qt + 1) / 2);
     L.args.n_units = static_cast<int>(units);
-    L.args.group = 1;
+    L.args.group = H / H_kv;
     L.args.n_splits = 1;
     L.args.scale_log2 = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634);
     L.args.q_scale = q_scale;
@@ -546,12 +547,28 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
     L.args.v_scale = v_scale;
     L.grid = static_cast<int>(units < static_cast<uint64_t>(dev->sm_count) ? units : dev->sm_count);
     L.args.chunk = 1;
-    if (causal) set_dynamic_order(L, units, B, H, N, d, 1, 1);
+    if (causal) set_dynamic_order(L, units, B, H, N, d, 1, H / H_kv);
     L.stream = static_cast<cudaStream_t>(stream);
     L.causal = causal != 0;
     L.bf16 = true;
     cudaError_t e = d == 256 ? fa::launch_fwd_fp8_d256(L) : fa::launch_fwd_fp8(L);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                     const float *q_scale, const float *k_scale, const float *v_scale,
+                     void *o, float *lse, int B, int H, int N, int d, float alpha,
+                     int causal, void *stream) {
+    return fwd_fp8_impl(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, H, N, d, alpha,
+                        causal, stream);
+}
+
+fa_status fa_fwd_fp8_gqa(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                         const float *q_scale, const float *k_scale, const float *v_scale,
+                         void *o, float *lse, int B, int H, int H_kv, int N, int d,
+                         float alpha, int causal, void *stream) {
+    return fwd_fp8_impl(q8, k8, v8, q_scale, k_scale, v_scale, o, lse, B, H, H_kv, N, d, alpha,
+                        causal, stream);
 }
 
 // The backward with the causal flag or, with win set, a local window

@@ -187,7 +187,7 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int c = 0; c < C::NCH; ++c)
                     tma_load_4d(tm, base + C::KV_OFF + slot * C::TILE_BYTES + c * C::CHUNK,
-                                bar(C::B_KVFULL + slot), c * 128, U.h, j * C::BN, U.b);
+                                bar(C::B_KVFULL + slot), c * 128, U.h / a.group, j * C::BN, U.b);
                 armed |= 1u << slot;
                 armed_par = (armed_par & ~(1u << slot)) | (phase << slot);
                 if (++slot == C::NSTAGE) { slot = 0; phase ^= 1; }
@@ -398,10 +398,12 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             const UnitF8 U = make_unit_f8<kCausal>(u, a);
             // The Q tile's scale and the largest V scale of the head (the
             // per-tile V scales are folded into P' relative to it).
+            // Q scales per query head, K and V scales per K/V head
             const size_t sbase = (static_cast<size_t>(U.b) * a.H + U.h) * a.n_kv;
+            const size_t kvbase = (static_cast<size_t>(U.b) * (a.H / a.group) + U.h / a.group) * a.n_kv;
             const float qsc = a.q_scale[sbase + U.m];
             float vm = 0.f;
-            for (int jj = lane; jj < a.n_kv; jj += 32) vm = fmaxf(vm, a.v_scale[sbase + jj]);
+            for (int jj = lane; jj < a.n_kv; jj += 32) vm = fmaxf(vm, a.v_scale[kvbase + jj]);
 #pragma unroll
             for (int m = 16; m > 0; m >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, m));
             const float vmax = vm;
@@ -414,8 +416,8 @@ fa_fwd_fp8_1q_kernel(const __grid_constant__ CUtensorMap tm_q,
             // neither sits on the path from S to P'.
             float ks_n, vs_n, sc_n, voff_n, ivr_n;
             auto tile_load = [&](const int j) __attribute__((always_inline)) {
-                ks_n = a.k_scale[sbase + j];
-                vs_n = a.v_scale[sbase + j];
+                ks_n = a.k_scale[kvbase + j];
+                vs_n = a.v_scale[kvbase + j];
             };
             auto tile_consts = [&]() __attribute__((always_inline)) {
                 sc_n = sl2 * qsc * ks_n;

@@ -624,12 +624,15 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             // FP8: the Q tile's scale and the largest V scale of the head
             // (the per-tile V scales are folded into P relative to it).
+            // FP8 scales: Q per query head, K and V per K/V head (grouped heads)
             const size_t sbase = (static_cast<size_t>(U.b) * a.H + U.h) * a.n_kv;
+            const size_t kvbase =
+                kFP8 ? (static_cast<size_t>(U.b) * (a.H / a.group) + U.h / a.group) * a.n_kv : 0;
             float qs = 1.f, vmax = 1.f;
             if constexpr (kFP8) {
                 qs = a.q_scale[sbase + mt];
                 float vm = 0.f;
-                for (int jj = lane; jj < a.n_kv; jj += 32) vm = fmaxf(vm, a.v_scale[sbase + jj]);
+                for (int jj = lane; jj < a.n_kv; jj += 32) vm = fmaxf(vm, a.v_scale[kvbase + jj]);
 #pragma unroll
                 for (int m = 16; m > 0; m >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, m));
                 vmax = vm;
@@ -649,8 +652,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
             float ks_n = 0.f, vs_n = 0.f;
             float sc_n = 0.f, voff_n = 0.f, ivr_n = 1.f;
             auto tile_load = [&](const int jj) __attribute__((always_inline)) {
-                ks_n = a.k_scale[sbase + jj];
-                vs_n = a.v_scale[sbase + jj];
+                ks_n = a.k_scale[kvbase + jj];
+                vs_n = a.v_scale[kvbase + jj];
             };
             auto tile_consts = [&]() __attribute__((always_inline)) {
                 sc_n = sl2 * qs * ks_n;

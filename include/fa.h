@@ -245,6 +245,19 @@ fa_status fa_fwd_fp8(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
                      int causal, void *stream);
 
 /*
+ * fa_fwd_fp8_gqa -- fa_fwd_fp8 with grouped key/value heads (as fa_fwd_gqa):
+ * q8 and q_scale have H heads, k8, v8, k_scale and v_scale have H_kv heads
+ * ([B][N][H_kv][d] codes, [B][H_kv][ceil(N/128)] scales), H_kv >= 1 divides
+ * H, and query head h attends with key/value head h / (H / H_kv).  H_kv = H
+ * is fa_fwd_fp8.  H % H_kv != 0 or H_kv < 1 returns FA_ERR_INVALID_ARG;
+ * other arguments, results and errors as fa_fwd_fp8.
+ */
+fa_status fa_fwd_fp8_gqa(const uint8_t *q8, const uint8_t *k8, const uint8_t *v8,
+                         const float *q_scale, const float *k_scale, const float *v_scale,
+                         void *o, float *lse, int B, int H, int H_kv, int N, int d,
+                         float alpha, int causal, void *stream);
+
+/*
  * fa_bwd -- gradients of the attention of fa_fwd ("FlashAttention-3 on
  * Hopper", ch. 7): with S = alpha Q K^T (masked as in fa_fwd),
  * P = softmax(S) and O = P V, for the upstream gradient dO:

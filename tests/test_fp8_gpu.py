@@ -255,3 +255,44 @@ def test_fp8_ablation_block_scales_and_rotation(gpu_lib):
     assert rm[("tensor", True)] < rm[("tensor", False)]
     assert rm[("block", False)] < rm[("tensor", False)]
     assert abs(rm[("block", True)] - rm[("tensor", True)]) <= 0.022 * rm[("tensor", True)]
+
+
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("H,H_kv", [(8, 2), (6, 1)])
+def test_fp8_gqa_equals_expanded_heads_and_meets_the_gate(gpu_lib, d, causal, H, H_kv):
+    # Grouped K/V heads (fa_fwd_fp8_gqa): query head h reads K/V head
+    # h / (H / H_kv).  Repeating each K/V head's codes and scales for its
+    # query heads and running fa_fwd_fp8 is the same arithmetic, so the bits
+    # must agree; and the result meets the FP8 RMSE gate against FP64
+    # grouped attention on the unquantized inputs.
+    fa = gpu_lib
+    dev = torch.device("cuda")
+    B, N, g = 2, 700, H // H_kv
+    q, k, v = synth.qkv(B, H, N, d, seed=N + d + H_kv, outliers=True)
+    k, v = k[:, :, :H_kv].contiguous(), v[:, :, :H_kv].contiguous()
+    s = torch.from_numpy(synth.hadamard_signs(d)).to(dev)
+    q8, qs = fa.quantize_fp8(q.to(dev), s)
+    k8, ks = fa.quantize_fp8(k.to(dev), s)
+    v8, vs = fa.quantize_fp8(v.to(dev), None, granularity=fa.FA_SCALE_HEAD)
+    a = synth.default_alpha(d)
+    o_g, l_g = fa.attention_fp8(q8, k8, v8, qs, ks, vs, causal=causal, alpha=a)
+    rep = lambda x, dim: x.repeat_interleave(g, dim=dim).contiguous()
+    o_e, l_e = fa.attention_fp8(q8, rep(k8, 2), rep(v8, 2), qs, rep(ks, 1), rep(vs, 1),
+                                causal=causal, alpha=a)
+    assert fa.fa_check_status() == fa.FA_OK
+    assert torch.equal(o_g, o_e) and torch.equal(l_g, l_e)
+    o_ref, _ = oracle.attention_gqa(q, k, v, a, causal, n_threads=THREADS)
+    rmse = float(np.sqrt(np.mean((o_g.float().cpu().numpy() - o_ref) ** 2)))
+    assert rmse <= 1.5e-2, rmse
+
+
+def test_fp8_gqa_rejects_bad_groups(gpu_lib):
+    fa = gpu_lib
+    x8 = torch.zeros((1, 128, 6, 128), dtype=torch.uint8, device="cuda")
+    sc = torch.ones((1, 6, 1), dtype=torch.float32, device="cuda")
+    o = torch.empty((1, 128, 6, 128), dtype=torch.bfloat16, device="cuda")
+    for H_kv in (0, 4):
+        assert fa.fa_fwd_fp8_gqa(x8, x8, x8, sc, sc, sc, o, None, 1, 6, H_kv, 128, 128, 0.1,
+                                 0) == fa.FA_ERR_INVALID_ARG
+
